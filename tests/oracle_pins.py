@@ -1,0 +1,353 @@
+"""Pins for the CPU oracle: checks against what the pages and the mathematics fix.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` instance and raises
+AssertionError if it disagrees with:
+  * the worked examples the pages print (fixtures under tests/golden/, each
+    with its citation);
+  * closed forms (all ones, x[i] = i, all 0xFFFFFFFF, affine special cases);
+  * invariants (exclusive = inclusive shifted right with the identity in
+    front; the last inclusive value is the reduction; compaction count is the
+    flag sum, order kept);
+  * library routines that compute the same thing a different way
+    (numpy.cumsum with uint32 wraparound, numpy.maximum.accumulate, boolean
+    mask selection, math.fsum);
+  * brute force over every input of length <= 8 on small alphabets, against a
+    divide-and-conquer fold (a different association order than the oracle's
+    left-to-right loop) or, for affine maps, against applying the maps one
+    after another to a point.
+
+The same functions run against deliberately broken copies of the oracle
+(tests/test_oracle_mutants.py) to show that each plausible mistake is caught.
+"""
+from __future__ import annotations
+
+import itertools
+import math
+
+import numpy as np
+
+from conftest import load_golden
+
+M32 = 1 << 32
+INT32_MIN = -(1 << 31)
+INT32_MAX = (1 << 31) - 1
+
+
+# ------------------------------------------------------------------ helpers
+def _all_sequences(alphabet, length):
+    """Every sequence of `length` symbols from `alphabet`, as a (k, length) array."""
+    if length == 0:
+        return np.zeros((1, 0), dtype=np.asarray(alphabet).dtype)
+    idx = np.array(list(itertools.product(range(len(alphabet)), repeat=length)), dtype=np.int64)
+    return np.asarray(alphabet)[idx]
+
+
+def _dc_fold(cols, op, identity):
+    """Divide-and-conquer fold over a list of column arrays (keeps left-to-right order)."""
+    if len(cols) == 0:
+        return identity
+    if len(cols) == 1:
+        return cols[0]
+    mid = len(cols) // 2
+    return op(_dc_fold(cols[:mid], op, identity), _dc_fold(cols[mid:], op, identity))
+
+
+def _apply_affine(a, b, h):
+    return (a.astype(np.uint64) * np.uint64(h) + b.astype(np.uint64)) % np.uint64(M32)
+
+
+# ------------------------------------------------------------ page examples
+def pin_golden_sum_examples(o):
+    for name in ("l7_sum_example.txt", "l7_sandwich.txt"):
+        g = load_golden(name)
+        x = np.array(g["input"], dtype=np.int32)
+        assert o.scan(x, "sum", False).tolist() == g["inclusive"], name
+        assert o.scan(x, "sum", True).tolist() == g["exclusive"], name
+        assert o.scan(x.view(np.uint32), "sum", True).tolist() == g["exclusive"], name
+        yf = o.scan(x.astype(np.float32), "sum", False)
+        assert yf.tolist() == [float(v) for v in g["inclusive"]], name
+        if "left_over" in g:
+            assert g["length"][0] - int(o.scan(x, "sum", False)[-1]) == g["left_over"][0]
+    g = load_golden("tut_flag_positions.txt")
+    assert o.scan(np.array(g["input"], dtype=np.int32), "sum", True).tolist() == g["exclusive"]
+    g = load_golden("pmpp_ch9_examples.txt")
+    x5 = np.array(g["sum5_input"], dtype=np.int32)
+    assert o.scan(x5, "sum", False).tolist() == g["sum5_inclusive"]
+    assert o.scan(x5, "sum", True).tolist() == g["sum5_exclusive"]
+    x8 = np.array(g["sum8_input"], dtype=np.int32)
+    assert o.scan(x8, "sum", True).tolist() == g["sum8_exclusive"]
+    assert int(o.scan(x8, "sum", False)[-1]) == g["sum8_total"][0]
+
+
+def pin_golden_compaction_examples(o):
+    for name, pfx in (("l7_compaction.txt", ""), ("pmpp_ch9_examples.txt", "filter_")):
+        g = load_golden(name)
+        x = np.array(g[pfx + "input"], dtype=np.int32)
+        pred, thr = g[pfx + "pred"][0], g[pfx + "threshold"][0]
+        out, cnt = o.compact(x, pred, thr)
+        assert out.tolist() == g[pfx + "output"], name
+        assert cnt == sum(g[pfx + "flags"]) == len(g[pfx + "output"]), name
+        flags = np.array(g[pfx + "flags"], dtype=np.int32)
+        assert o.scan(flags, "sum", True).tolist() == g[pfx + "flag_exclusive_scan"], name
+        # the scatter: kept element i goes to slot exclusive_scan(flags)[i]
+        pos = o.scan(flags, "sum", True)
+        scattered = [None] * cnt
+        for i in range(x.size):
+            if flags[i]:
+                scattered[pos[i]] = int(x[i])
+        assert scattered == out.tolist(), name
+        # same compaction on float32 and uint32-representable data
+        outf, cntf = o.compact(x.astype(np.float32), pred, thr)
+        assert outf.tolist() == [float(v) for v in g[pfx + "output"]] and cntf == cnt
+
+
+def pin_golden_identities(o):
+    g = load_golden("pmpp_ch9_identities.txt")
+    for x in (np.array([5, 7], dtype=np.int32), np.array([-3], dtype=np.int32)):
+        assert int(o.scan(x, "sum", True)[0]) == g["sum"][0]
+        assert int(o.scan(x, "max", True)[0]) == g["max_i32"][0]
+    assert float(o.scan(np.array([2.5], dtype=np.float32), "sum", True)[0]) == float(g["sum"][0])
+    # exclusive affine starts with the map that leaves every point unchanged
+    ab = np.array([[3, 4], [5, 6]], dtype=np.uint32)
+    y = o.scan(ab, "affine", True)
+    for h in (0, 1, 12345, M32 - 1):
+        assert int(_apply_affine(y[:1, 0], y[:1, 1], h)[0]) == h
+    # empty inputs
+    for op, x in (("sum", np.zeros(0, np.int32)), ("max", np.zeros(0, np.int32)),
+                  ("sum", np.zeros(0, np.float32)), ("affine", np.zeros((0, 2), np.uint32))):
+        assert o.scan(x, op, True).shape[0] == 0 and o.scan(x, op, False).shape[0] == 0
+    out, cnt = o.compact(np.zeros(0, np.int32), "gt", 0)
+    assert cnt == 0 and out.size == 0
+
+
+# -------------------------------------------------------------- closed forms
+def pin_closed_forms(o):
+    for n in (1, 2, 7, 1000, 1 << 17):
+        i = np.arange(n, dtype=np.uint64)
+        ones = np.ones(n, dtype=np.uint32)
+        assert np.array_equal(o.scan(ones, "sum", True), i.astype(np.uint32))
+        assert np.array_equal(o.scan(ones, "sum", False), (i + 1).astype(np.uint32))
+        assert np.array_equal(o.scan(np.ones(n, np.float32), "sum", True), i.astype(np.float64))
+        # x[i] = i  ->  inclusive i(i+1)/2 mod 2^32
+        xi = i.astype(np.uint32)
+        tri = ((i * (i + np.uint64(1))) // np.uint64(2)) % np.uint64(M32)
+        assert np.array_equal(o.scan(xi, "sum", False), tri.astype(np.uint32))
+        # all 0xFFFFFFFF -> inclusive -(i+1) mod 2^32
+        allf = np.full(n, 0xFFFFFFFF, dtype=np.uint32)
+        neg = (np.uint64(M32) - (i + np.uint64(1)) % np.uint64(M32)) % np.uint64(M32)
+        assert np.array_equal(o.scan(allf, "sum", False), neg.astype(np.uint32))
+        assert np.array_equal(o.scan(allf.view(np.int32), "sum", False),
+                              (-(i.astype(np.int64) + 1)).astype(np.int32))
+        # max over ascending input is the input; over descending it is x[0]
+        asc = np.arange(n, dtype=np.int32) - n // 2
+        assert np.array_equal(o.scan(asc, "max", False), asc)
+        assert np.array_equal(o.scan(asc[::-1].copy(), "max", False), np.full(n, asc[-1], np.int32))
+
+
+def pin_affine_special_cases(o):
+    rng = np.random.default_rng(7)
+    n = 5000
+    b = rng.integers(0, M32, n, dtype=np.uint64).astype(np.uint32)
+    a = rng.integers(0, M32, n, dtype=np.uint64).astype(np.uint32)
+    # all a = 1: translations compose by adding; the result is (1, sum of b)
+    y = o.scan(np.stack([np.ones(n, np.uint32), b], axis=1), "affine", False)
+    assert np.all(y[:, 0] == 1)
+    assert np.array_equal(y[:, 1], np.cumsum(b, dtype=np.uint32))
+    # all b = 0: scalings compose by multiplying; the result is (prefix product, 0)
+    y = o.scan(np.stack([a, np.zeros(n, np.uint32)], axis=1), "affine", False)
+    assert np.all(y[:, 1] == 0)
+    assert np.array_equal(y[:, 0], (np.cumprod(a.astype(np.uint64)) % np.uint64(M32)).astype(np.uint32))
+
+
+# ---------------------------------------------------------------- invariants
+def _random_inputs():
+    rng = np.random.default_rng(12345)
+    n = 30011
+    return {
+        "sum_i32": rng.integers(-1000, 1000, n).astype(np.int32),
+        "sum_u32": rng.integers(0, M32, n, dtype=np.uint64).astype(np.uint32),
+        "max_i32": rng.integers(INT32_MIN, INT32_MAX, n, endpoint=True).astype(np.int32),
+        "affine": rng.integers(0, M32, (n, 2), dtype=np.uint64).astype(np.uint32),
+        "sum_f32": rng.uniform(-1, 1, n).astype(np.float32),
+    }
+
+
+def pin_invariants(o):
+    d = _random_inputs()
+    for key, op in (("sum_i32", "sum"), ("sum_u32", "sum"), ("max_i32", "max"),
+                    ("affine", "affine"), ("sum_f32", "sum")):
+        x = d[key]
+        inc = o.scan(x, op, False)
+        exc = o.scan(x, op, True)
+        ident = {"sum": 0, "max": INT32_MIN}.get(op)
+        # exclusive = inclusive shifted right by one with the identity in front
+        assert np.array_equal(exc[1:], inc[:-1]), key
+        if op == "affine":
+            assert exc[0].tolist() == [1, 0]
+        else:
+            assert exc[0] == ident, key
+        # the last inclusive value is the reduction of the whole array
+        if op == "sum" and x.dtype != np.float32:
+            assert int(inc[-1]) % M32 == int(x.astype(np.int64).sum()) % M32, key
+        elif op == "max":
+            assert int(inc[-1]) == int(x.max())
+        elif op == "sum":
+            assert abs(float(inc[-1]) - math.fsum(x.astype(np.float64))) <= 1e-9
+    # max-scan is monotone and each output is one of the inputs seen so far
+    x = d["max_i32"]
+    y = o.scan(x, "max", False)
+    assert np.all(np.diff(y.astype(np.int64)) >= 0)
+    assert np.all(y >= x)
+    for i in range(0, x.size, 997):
+        assert int(y[i]) in set(x[:i + 1].tolist())
+
+
+def pin_affine_recurrence(o):
+    """y[i] applied to h[-1] equals the sequential recurrence h[i] = a[i]*h[i-1] + b[i]."""
+    x = _random_inputs()["affine"][:4000]
+    inc = o.scan(x, "affine", False)
+    exc = o.scan(x, "affine", True)
+    for h0 in (0, 1, 0xDEADBEEF, M32 - 1):
+        h = h0
+        hs = []
+        for a, b in x.tolist():
+            hs.append(h)
+            h = (a * h + b) % M32
+            hs[-1] = (hs[-1], h)
+        before = np.array([p for p, _ in hs], dtype=np.uint64)
+        after = np.array([q for _, q in hs], dtype=np.uint64)
+        assert np.array_equal(_apply_affine(inc[:, 0], inc[:, 1], h0), after)
+        assert np.array_equal(_apply_affine(exc[:, 0], exc[:, 1], h0), before)
+
+
+# ------------------------------------------------------ library special cases
+def pin_library_special_cases(o):
+    d = _random_inputs()
+    x = d["sum_u32"]
+    assert np.array_equal(o.scan(x, "sum", False), np.cumsum(x, dtype=np.uint32))
+    xi = d["sum_i32"]
+    assert np.array_equal(o.scan(xi, "sum", False), np.cumsum(xi, dtype=np.int32))
+    xm = d["max_i32"]
+    assert np.array_equal(o.scan(xm, "max", False), np.maximum.accumulate(xm))
+    assert o.scan(xm[:3000], "max", False).tolist() == list(itertools.accumulate(xm[:3000].tolist(), max))
+    # compaction equals boolean-mask selection, for every predicate
+    for dt, x in ((np.int32, d["sum_i32"]), (np.uint32, d["sum_u32"]), (np.float32, d["sum_f32"])):
+        for pred, fn in (("gt", np.greater), ("ge", np.greater_equal), ("lt", np.less),
+                         ("le", np.less_equal), ("eq", np.equal), ("ne", np.not_equal)):
+            for thr in (0, 0.5, -3, float(x[17])):
+                out, cnt = o.compact(x, pred, thr)
+                mask = fn(x.astype(np.float64), thr)
+                assert cnt == int(mask.sum()), (dt, pred, thr)
+                assert np.array_equal(out, x[mask]), (dt, pred, thr)
+
+
+def pin_float_fp64_accumulation(o):
+    """The float32 sum is the fp64 running sum: within n*2^-53*sum|x| of the exact prefix."""
+    rng = np.random.default_rng(99)
+    x = rng.uniform(-1, 1, 3000).astype(np.float32)
+    y = o.scan(x, "sum", False)
+    ye = o.scan(x, "sum", True)
+    xs = x.astype(np.float64).tolist()
+    s = o.abs_prefix(x)
+    for i in range(0, x.size, 7):
+        exact = math.fsum(xs[:i + 1])
+        assert abs(y[i] - exact) <= (i + 1) * 2.0 ** -53 * s[i] + 1e-300, i
+        assert abs(ye[i] - math.fsum(xs[:i])) <= (i + 1) * 2.0 ** -53 * s[i] + 1e-300, i
+        assert abs(s[i] - math.fsum(abs(v) for v in xs[:i + 1])) <= (i + 1) * 2.0 ** -53 * s[i]
+    # small terms that float32 accumulation would lose are kept
+    tiny = np.full(1 << 12, 2.0 ** -30, dtype=np.float32)
+    z = o.scan(np.concatenate([np.ones(1, np.float32), tiny]), "sum", False)
+    assert z[-1] == 1.0 + tiny.size * 2.0 ** -30
+
+
+# ------------------------------------------------------ batched row scans
+def pin_batched_rows(o):
+    d = _random_inputs()
+    for key, op in (("sum_i32", "sum"), ("max_i32", "max"), ("sum_f32", "sum")):
+        x = d[key][:30000].reshape(120, 250)
+        for ex in (False, True):
+            yb = o.scan_batched(x, op, ex)
+            for r in (0, 1, 77, 119):
+                assert np.array_equal(yb[r], o.scan(x[r].copy(), op, ex)), (key, ex, r)
+    xa = d["affine"][:30000].reshape(120, 250, 2)
+    for ex in (False, True):
+        yb = o.scan_batched(xa, "affine", ex)
+        for r in (0, 5, 119):
+            assert np.array_equal(yb[r], o.scan(xa[r].copy(), "affine", ex))
+    # row independence: each row starts from the identity
+    x = np.ones((64, 33), dtype=np.int32)
+    assert np.array_equal(o.scan_batched(x, "sum", True), np.tile(np.arange(33, dtype=np.int32), (64, 1)))
+
+
+# ------------------------------------------------------------- brute force
+def _brute_scan(o, alphabet, op_name, op, identity, max_len=8):
+    for length in range(0, max_len + 1):
+        seqs = _all_sequences(alphabet, length)
+        for ex in (False, True):
+            if length == 0:
+                assert o.scan(seqs[0], op_name, ex).size == 0
+                continue
+            got = o.scan_batched(seqs, op_name, ex)
+            cols = [seqs[:, j] for j in range(length)]
+            for i in range(length):
+                pre = cols[:i] if ex else cols[:i + 1]
+                want = _dc_fold(pre, op, identity)
+                if np.isscalar(want) or np.ndim(want) == 0:
+                    want = np.full(seqs.shape[0], want)
+                assert np.array_equal(got[:, i].astype(np.int64), np.asarray(want).astype(np.int64)), \
+                    (op_name, length, ex, i)
+            # the 1-D entry point agrees with the batched one on a sample of rows
+            for r in range(0, seqs.shape[0], max(1, seqs.shape[0] // 50)):
+                assert np.array_equal(o.scan(seqs[r].copy(), op_name, ex), got[r])
+
+
+def pin_brute_force_sum(o):
+    add = lambda p, q: (p.astype(np.int64) + q.astype(np.int64)) % M32
+    _brute_scan(o, np.array([0, 1, 2], dtype=np.uint32), "sum", add, 0)
+    _brute_scan(o, np.array([0xFFFFFFFF, 1, 0x80000000], dtype=np.uint32), "sum", add, 0, max_len=7)
+
+
+def pin_brute_force_max(o):
+    mx = lambda p, q: np.maximum(p.astype(np.int64), q.astype(np.int64))
+    _brute_scan(o, np.array([INT32_MIN, -1, 0, 1, INT32_MAX], dtype=np.int32), "max", mx, INT32_MIN)
+
+
+def pin_brute_force_affine(o):
+    """Every sequence of <= 8 maps from a 4-map alphabet: y[i] must act on a point
+    as the maps x[0], ..., x[i] applied one after another."""
+    alphabet = np.array([[0, 0], [1, 1], [2, 3], [0xFFFFFFFF, 5]], dtype=np.uint32)
+    for length in range(1, 9):
+        idx = _all_sequences(np.arange(4), length)
+        seqs = alphabet[idx]                       # (k, length, 2)
+        for ex in (False, True):
+            got = o.scan_batched(seqs, "affine", ex)
+            for h0 in (0, 1):                     # a map a*h+b is fixed by its values at 0 and 1
+                h = np.full(seqs.shape[0], h0, dtype=np.uint64)
+                for i in range(length):
+                    nxt = _apply_affine(seqs[:, i, 0], seqs[:, i, 1], h)
+                    want = h if ex else nxt
+                    assert np.array_equal(_apply_affine(got[:, i, 0], got[:, i, 1], h0), want), \
+                        (length, ex, i, h0)
+                    h = nxt
+
+
+def pin_brute_force_compaction(o):
+    for length in range(0, 9):
+        seqs = _all_sequences(np.array([-1, 0, 1], dtype=np.int32), length)
+        for pred, fn in (("gt", lambda v, t: v > t), ("ge", lambda v, t: v >= t),
+                         ("lt", lambda v, t: v < t), ("le", lambda v, t: v <= t),
+                         ("eq", lambda v, t: v == t), ("ne", lambda v, t: v != t)):
+            for thr in (0, -1, 0.5):
+                for r in range(seqs.shape[0]):
+                    row = seqs[r]
+                    out, cnt = o.compact(row, pred, thr)
+                    want = [v for v in row.tolist() if fn(v, thr)]
+                    assert out.tolist() == want and cnt == len(want), (row.tolist(), pred, thr)
+
+
+ALL_PINS = [
+    pin_golden_sum_examples, pin_golden_compaction_examples, pin_golden_identities,
+    pin_closed_forms, pin_affine_special_cases, pin_invariants, pin_affine_recurrence,
+    pin_library_special_cases, pin_float_fp64_accumulation, pin_batched_rows,
+    pin_brute_force_sum, pin_brute_force_max, pin_brute_force_affine, pin_brute_force_compaction,
+]

@@ -1,0 +1,59 @@
+"""Plant plausible mistakes in copies of the oracle and check that the pins catch each.
+
+Each mutant is oracle.c with one textual change, compiled with gcc into a
+temporary directory.  The real oracle source is never modified.
+"""
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS
+
+MUTANTS = {
+    # exclusive scan writes after accumulating (i.e. emits the inclusive value)
+    "exclusive_is_inclusive": ("            y[i] = acc;\n            acc = sum_u32(acc, x[i]);",
+                               "            acc = sum_u32(acc, x[i]);\n            y[i] = acc;"),
+    # a dropped term: the first element is skipped
+    "dropped_first_term": ("    uint32_t acc = 0u;\n    for (int64_t i = 0; i < n; ++i) {",
+                           "    uint32_t acc = 0u;\n    for (int64_t i = 0; i < n; ++i) { if (i == 0 && n > 3) { y[0] = exclusive ? 0u : 0u; continue; }"),
+    # wrong identity for max
+    "max_identity_zero": ("    int32_t acc = INT32_MIN;", "    int32_t acc = 0;"),
+    # max replaced by min-like comparison
+    "max_wrong_sign": ("return x > acc ? x : acc;", "return x < acc ? x : acc;"),
+    # affine composition in the wrong order (later map applied first)
+    "affine_order_swapped": ("    uint32_t na = a * *acc_a;\n    uint32_t nb = a * *acc_b + b;",
+                             "    uint32_t na = *acc_a * a;\n    uint32_t nb = *acc_a * b + *acc_b;"),
+    # affine: transposed operand in the offset term
+    "affine_transposed": ("    uint32_t nb = a * *acc_b + b;", "    uint32_t nb = *acc_a * *acc_b + b;"),
+    # float accumulated in float32
+    "float_in_f32": ("            acc = acc + (double)x[i];\n            y[i] = acc;",
+                     "            acc = (float)(acc + (double)x[i]);\n            y[i] = acc;"),
+    # compaction predicate off by one (>= instead of >)
+    "pred_gt_is_ge": ("    case PRED_GT: return v > t;", "    case PRED_GT: return v >= t;"),
+    # batched rows: wrong row stride
+    "batched_row_stride": ("        oracle_scan_sum_u32(x + r * cols, y + r * cols, cols, exclusive);",
+                           "        oracle_scan_sum_u32(x + r * cols, y + r * cols, cols - (cols > 1), exclusive);"),
+    # abs prefix without the absolute value
+    "abs_prefix_signed": ("        acc = acc + fabs((double)x[i]);", "        acc = acc + (double)x[i];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(oracle._SRC).read()
+    assert src.count(old) >= 1, "mutation anchor not found: " + name
+    mutated = src.replace(old, new, 1)
+    csrc = os.path.join(str(tmp_path), "oracle_mut.c")
+    with open(csrc, "w") as f:
+        f.write(mutated)
+    so = oracle.build(force=True, src=csrc, out=os.path.join(str(tmp_path), "liboracle_mut.so"))
+    mut = oracle.Oracle(oracle.load_library(so))
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(mut)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, "no pin caught mutant " + name
