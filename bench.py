@@ -1,0 +1,439 @@
+#!/usr/bin/env python
+"""Benchmark of the device-wide scan: uint32 exclusive sum, n = 2^30 (4 GiB in, 4 GiB out).
+
+One step = one single-pass scan launch over the whole array (the hot path:
+tile load, register/warp/block scan, decoupled look-back, store).  Inputs are
+seeded SplitMix64 draws generated on the device before timing; they are 32x
+larger than L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  Usage:
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank scans its own replica of the workload on its
+own GPU (no collective on the data path: the work does not shard across
+GPUs); timing is the max over ranks.
+    --suite   also print one extra line per other workload (parity cases)
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "device-wide scan Gelem/s and HBM GB/s vs GB300 peak (uint32 sum, n=2^30)"
+WORKLOAD = "uint32_exsum_n2^30"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "scan_u32_exsum_n2p30_traffic.txt")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=4)
+    ap.add_argument("--variant", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--suite", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_sources_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "stream_compaction_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, if it matches the current kernels."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_sources_sha256") != kernel_sources_hash():
+            return None
+        return int(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "50"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        time.sleep(0.15)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0, t1):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = [l for ts, l in self.lines if t0 - 0.06 <= ts <= t1 + 0.06] or [l for _, l in self.lines[-2:]]
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            p = [c.strip() for c in r.split(",")]
+            if len(p) < 8:
+                continue
+            try:
+                sm.append(float(p[0]))
+                smax.append(float(p[1]))
+                power.append(float(p[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, p[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def gpu_uuid(dev):
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, rank, world):
+    """The oracle, as it stands, on this host's cores (the reference arm of this benchmark)."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from stream_compaction_gb300 import synth
+    spec = synth.WORKLOADS[WORKLOAD]
+    cal_n = 1 << 22
+    xc = synth.make_np(spec, cal_n)
+    t = time.perf_counter()
+    oracle.scan(xc, "sum", True)
+    rate = cal_n / max(time.perf_counter() - t, 1e-6)
+    budget_s = 90.0
+    sample = int(min(spec["n"], max(1 << 16, rate * budget_s / max(1, args.steps + args.warmup))))
+    x = synth.make_np(spec, sample)
+    y = np.empty_like(x)
+    o = oracle.default()
+    for _ in range(args.warmup):
+        o.c.oracle_scan_sum_u32(x.ctypes.data, y.ctypes.data, sample, 1)
+    ts = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        o.c.oracle_scan_sum_u32(x.ctypes.data, y.ctypes.data, sample, 1)
+        ts.append(time.perf_counter() - t)
+    total = sum(ts)
+    value = sample * args.steps / total / 1e9
+    desc = "first %d elements of the %s workload per step (sequential C oracle)" % (sample, WORKLOAD)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "Gelem/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "n_sample": sample},
+            "cpu_baseline": {"value": value, "unit": "Gelem/s", "cores": 1, "kind": "oracle", "sample": desc,
+                             "host_cpus": os.cpu_count()},
+            "e2e": {"value": value, "unit": "Gelem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+def time_launches(fn, steps, warmup, stream):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def suite_lines(args, dev, sc, synth):
+    """Extra lines: kernel timings for the other workloads (L2-flushed between steps)."""
+    import torch
+    s = torch.cuda.current_stream()
+    sp = int(s.cuda_stream)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = []
+
+    def timed(fn, nbytes, steps=50):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        tot = 0.0
+        for _ in range(steps):
+            flush.add_(1)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            fn()
+            e1.record(s)
+            e1.synchronize()
+            tot += e0.elapsed_time(e1)
+        return tot / steps, nbytes
+
+    def emit(name, n, ms, nbytes, extra=None):
+        d = {"suite": name, "n": n, "ms_per_launch": ms, "gelem_s": n / ms / 1e6, "hbm_gbs": nbytes / ms / 1e6}
+        if extra:
+            d.update(extra)
+        print(json.dumps(d), flush=True)
+
+    W = synth.WORKLOADS
+    x = synth.make_torch(W["int32_sum_n1048593"], device=dev)
+    y = torch.empty_like(x)
+    n = x.numel()
+    for ex, fn in ((0, sc.sc_scan_inclusive), (1, sc.sc_scan_exclusive)):
+        ms, b = timed(lambda: fn(sc.SC_I32, sc.SC_SUM, x.data_ptr(), y.data_ptr(), n, sp), 8 * n)
+        emit("int32_sum_n1048593_%s" % ("exclusive" if ex else "inclusive"), n, ms, b, {"l2": "flushed"})
+    x = synth.make_torch(W["float32_exsum_n2^26"], device=dev)
+    y = torch.empty_like(x)
+    n = x.numel()
+    ms, b = timed(lambda: sc.sc_scan_exclusive(sc.SC_F32, sc.SC_SUM, x.data_ptr(), y.data_ptr(), n, sp), 8 * n)
+    emit("float32_exsum_n2^26", n, ms, b)
+    x = synth.make_torch(W["int32_compact_gt0_n2^27"], device=dev)
+    y = torch.empty_like(x)
+    cnt = torch.empty(1, dtype=torch.int64, device=dev)
+    n = x.numel()
+    ms, _ = timed(lambda: sc.sc_compact_if(sc.SC_I32, x.data_ptr(), y.data_ptr(), cnt.data_ptr(), n, sc.SC_GT, 0.0,
+                                           sp), 0)
+    k = int(cnt.item())
+    emit("int32_compact_gt0_n2^27", n, ms, 4 * n + 4 * k, {"kept": k})
+    x = synth.make_torch(W["int32_max_n2^27"], device=dev)
+    y = torch.empty_like(x)
+    n = x.numel()
+    ms, b = timed(lambda: sc.sc_scan_inclusive(sc.SC_I32, sc.SC_MAX, x.data_ptr(), y.data_ptr(), n, sp), 8 * n)
+    emit("int32_max_n2^27", n, ms, b)
+    x = synth.make_torch(W["affine_u32_n2^26"], device=dev)
+    y = torch.empty_like(x)
+    n = x.shape[0]
+    ms, b = timed(lambda: sc.sc_scan_inclusive(sc.SC_AFFINE_U32, sc.SC_COMPOSE, x.data_ptr(), y.data_ptr(), n, sp),
+                  16 * n)
+    emit("affine_u32_n2^26", n, ms, b)
+    x = synth.make_torch(W["int32_rows_65536x4096"], device=dev)
+    y = torch.empty_like(x)
+    n = x.numel()
+    ms, b = timed(lambda: sc.sc_scan_batched(sc.SC_I32, sc.SC_SUM, 1, x.data_ptr(), y.data_ptr(), 65536, 4096, sp),
+                  8 * n, steps=20)
+    emit("int32_rows_65536x4096", n, ms, b)
+    del flush
+
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import stream_compaction_gb300 as sc
+    from stream_compaction_gb300 import build as scbuild, synth
+
+    if not scbuild.up_to_date():
+        scbuild.build()
+    sc.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if sc.sc_set_scan_variant(args.variant) != sc.SC_OK:
+        raise SystemExit("unknown variant %d" % args.variant)
+
+    spec = synth.WORKLOADS[WORKLOAD]
+    n = spec["n"]
+    x = synth.make_torch(spec, device=dev)          # int32 bit patterns of uint32 draws
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+    sp = int(stream.cuda_stream)
+    torch.cuda.synchronize()
+
+    def step():
+        st = sc.sc_scan_exclusive(sc.SC_U32, sc.SC_SUM, x.data_ptr(), y.data_ptr(), n, sp)
+        if st != sc.SC_OK:
+            raise RuntimeError(sc.status_string(st))
+
+    # warm-up (also allocates the stream's workspace, outside the timed region)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if sc.sc_get_device_error(sp) != sc.SC_OK:
+        raise RuntimeError("device error during warm-up")
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(gpu_uuid(dev) if rank == 0 else None) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    l0 = sc.sc_launch_count()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    launches = sc.sc_launch_count() - l0
+    clocks = sampler.stop(t0, t1) if sampler else None
+    ms = e0.elapsed_time(e1)
+    if sc.sc_get_device_error(sp) != sc.SC_OK:
+        raise RuntimeError("device error during the timed region")
+    if world > 1:
+        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+        torch.distributed.barrier()
+    ms_step = ms / args.steps
+    value = world * n / (ms_step * 1e-3) / 1e9       # Gelem/s over all ranks
+    if rank != 0:
+        return
+
+    # spot check of the timed output against a host recomputation of a prefix of it
+    head = 1 << 20
+    xh = x[:head].cpu().numpy().view(np.uint32)
+    want = np.concatenate([[0], np.cumsum(xh[:-1], dtype=np.uint32)])
+    assert np.array_equal(y[:head].cpu().numpy().view(np.uint32), want), "bench output mismatch"
+
+    peak, peak_kind = peaks()
+    alg_bytes = 8 * n
+    achieved = alg_bytes / (ms_step * 1e-3) / 1e9
+    traffic = recorded_traffic()
+
+    # in-run comparison: the pages' hierarchical multi-kernel design on the same input
+    hsteps = max(3, min(args.steps, 100))
+    hms = time_launches(lambda: sc.sc_scan_hierarchical(sc.SC_U32, sc.SC_SUM, 1, x.data_ptr(), y.data_ptr(), n,
+                                                        sp), hsteps, 2, stream) / hsteps
+    # library context: torch.cumsum (inclusive, int32 wraparound) on the same input
+    cms = time_launches(lambda: torch.cumsum(x, 0, dtype=torch.int32, out=y), 20, 2, stream) / 20
+
+    # end to end through the C ABI with pinned host buffers: H2D + scan + D2H per step
+    hx = torch.empty(n, dtype=torch.int32, pin_memory=True)
+    hx.copy_(x)
+    hy = torch.empty(n, dtype=torch.int32, pin_memory=True)
+    sc.sc_scan_host(sc.SC_U32, sc.SC_SUM, 1, hx.data_ptr(), hy.data_ptr(), n, sp)
+    e2e_t = []
+    for _ in range(args.e2e_steps):
+        t = time.perf_counter()
+        st = sc.sc_scan_host(sc.SC_U32, sc.SC_SUM, 1, hx.data_ptr(), hy.data_ptr(), n, sp)
+        e2e_t.append(time.perf_counter() - t)
+        if st != sc.SC_OK:
+            raise RuntimeError(sc.status_string(st))
+    hyn = hy.numpy().view(np.uint32)
+    assert np.array_equal(hyn[:head], want), "e2e output mismatch"
+    e2e_value = n / statistics.mean(e2e_t) / 1e9
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        xn = hx.numpy().view(np.uint32)
+        ts = []
+        for _ in range(3):
+            t = time.perf_counter()
+            ref = oracle.scan(xn, "sum", True)
+            ts.append(time.perf_counter() - t)
+        assert np.array_equal(ref[:head], want) and np.array_equal(ref[-head:], hyn[-head:])
+        del ref
+        cpu = {"value": n / statistics.median(ts) / 1e9, "unit": "Gelem/s", "cores": 1, "kind": "oracle",
+               "sample": "the full n=2^30 workload, 3 runs, median (sequential C loop, one thread)",
+               "host_cpus": os.cpu_count()}
+
+    st_, nt, ipt, ld = sc.sc_scan_variant_info(args.variant)
+    line = {
+        "metric": METRIC, "value": value, "unit": "Gelem/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "n": n, "op": "sum", "exclusive": True,
+                   "l2": "inputs larger than L2 (4 GiB in + 4 GiB out per step), no flush",
+                   "parallelism": "replicas" if world > 1 else "single-gpu",
+                   "tile": {"threads": nt, "items_per_thread": ipt, "loader": ["direct", "transpose"][ld]}},
+        "hbm_gbs": achieved,
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": "Gelem/s", "h2d_bytes_per_step": 4 * n, "d2h_bytes_per_step": 4 * n,
+                "steps": args.e2e_steps, "api": "sc_scan_host (pinned host buffers)"},
+        "gpu_launches": launches,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "peak_kind": peak_kind, "algorithmic_bytes_per_launch": alg_bytes},
+        "cpu_baseline": cpu,
+        "comparison": {"hierarchical_ms": hms, "hierarchical_gelem_s": n / hms / 1e6,
+                       "single_pass_speedup": hms / ms_step,
+                       "torch_cumsum_ms": cms, "torch_cumsum_gelem_s": n / cms / 1e6},
+    }
+    print(json.dumps(line), flush=True)
+    if args.suite:
+        del hx, hy
+        suite_lines(args, dev, sc, synth)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,173 @@
+/*
+ * sc_scan.h -- C ABI of the GB300 (sm_103a) device-wide scan and stream
+ * compaction library (libsc_gb300.so).
+ *
+ * What the calls compute.
+ *   Inclusive scan  y[i] = x[0] (+) x[1] (+) ... (+) x[i].
+ *   Exclusive scan  y[0] = I,  y[i] = x[0] (+) ... (+) x[i-1]  (I: identity of (+)).
+ *   Both as defined in "Lecture 7: Parallel pattern -- prefix sum / scan:
+ *   double buffering and hierarchical algorithms" (UIUC ECE408 course notes),
+ *   section 1 "Scan: inclusive and exclusive", and in "Chapter 9 Parallel
+ *   Patterns: Prefix Sum - Scan Algorithms" (PMPP notes), section 9.1, whose
+ *   identity table gives 0 for addition and -infinity (here INT32_MIN) for max.
+ *   A scan keeps the order of its operands, so (+) needs associativity but not
+ *   commutativity (Lecture 7 notes, section 1).
+ *   Stream compaction keeps, in input order, the elements that satisfy a
+ *   predicate (Lecture 7 notes, section 2 "Applications of Scan"; PMPP notes,
+ *   section 9.6 "Applications of Scan", filtering).
+ *
+ * Operators (dtype, op):
+ *   (SC_I32, SC_SUM), (SC_U32, SC_SUM)  sum modulo 2^32 (two's complement
+ *                                        wraparound; identical bits for both);
+ *   (SC_F32, SC_SUM)                    float32 sum; within a tile in fp32, the
+ *                                        carry between tiles in fp64; result
+ *                                        within 1e-5 * sum_{k<=i} |x[k]| of the
+ *                                        exact prefix (not bitwise
+ *                                        reproducible: the look-back may fold
+ *                                        tile totals in a different grouping
+ *                                        from run to run);
+ *   (SC_I32, SC_MAX)                    max, identity INT32_MIN;
+ *   (SC_AFFINE_U32, SC_COMPOSE)         element i is the map h -> a_i*h + b_i
+ *                                        (mod 2^32), stored as the uint32 pair
+ *                                        (a_i, b_i) (8 bytes, a first);
+ *                                        (a1,b1) (+) (a2,b2) = (a2*a1, a2*b1 + b2)
+ *                                        (the earlier map is applied first;
+ *                                        identity (1, 0)); y[i] applied to h0
+ *                                        gives the recurrence h_i = a_i*h_{i-1} + b_i.
+ *
+ * Conventions for every call below.
+ *   - Pointers named d_* / in / out are DEVICE pointers owned by the caller
+ *     (e.g. torch tensors).  Elements are contiguous.  4-byte types need
+ *     4-byte alignment, affine pairs 8-byte alignment; 16-byte aligned in/out
+ *     take the vectorised path.
+ *   - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t;
+ *     NULL is the legacy default stream).  They never synchronise the host and
+ *     never allocate in steady state: the first call on a (device, stream)
+ *     pair allocates that pair's workspace (or uses one given with
+ *     sc_set_workspace) and grows it only when a larger n arrives.
+ *   - Calls on one stream must not overlap in time with calls on the same
+ *     stream from another host thread; different streams have independent
+ *     workspaces.
+ *   - n == 0 is a successful no-op (compaction writes *d_count = 0).
+ *   - Argument errors are detected on the host before any launch and return
+ *     SC_ERR_INVALID / SC_ERR_UNSUPPORTED.  A failure inside a kernel (a
+ *     look-back wait that exceeds its time bound) is reported by
+ *     sc_get_device_error; the kernel never traps and never hangs.
+ */
+#ifndef SC_SCAN_H
+#define SC_SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so this header needs no CUDA header. */
+typedef struct CUstream_st *sc_stream_t;
+
+typedef enum { SC_I32 = 0, SC_U32 = 1, SC_F32 = 2, SC_AFFINE_U32 = 3 } sc_dtype;
+typedef enum { SC_SUM = 0, SC_MAX = 1, SC_COMPOSE = 2 } sc_op;
+/* Compaction predicate "x <pred> threshold", evaluated as if in double
+ * precision (every int32, uint32 and float32 value is exact in double). */
+typedef enum { SC_GT = 0, SC_GE = 1, SC_LT = 2, SC_LE = 3, SC_EQ = 4, SC_NE = 5 } sc_pred;
+typedef enum {
+    SC_OK = 0,
+    SC_ERR_INVALID = 1,          /* bad pointer, size, enum or alignment */
+    SC_ERR_UNSUPPORTED = 2,      /* valid enums, but this (dtype, op) is not provided */
+    SC_ERR_WORKSPACE = 3,        /* caller-bound workspace too small, or allocation failed */
+    SC_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed */
+    SC_ERR_LOOKBACK_TIMEOUT = 5  /* a kernel gave up waiting on a predecessor tile */
+} sc_status;
+
+/* Library version string. */
+const char *sc_version(void);
+
+/* Human-readable name of a status code (static storage). */
+const char *sc_status_string(sc_status s);
+
+/* Bytes of device workspace a scan or compaction of n elements needs (for
+ * sc_scan_batched: n = rows * cols).  Includes the tile counter, the device
+ * error word and one look-back status slot (8 or 16 bytes) per tile. */
+size_t sc_workspace_bytes(int64_t n);
+
+/* Bind caller-owned device memory `d_ws` (bytes >= sc_workspace_bytes(n) of
+ * the largest call to come, 256-byte aligned) as the workspace of `stream` on
+ * the current device.  The library zeroes it with an async memset on `stream`
+ * and never frees it.  d_ws == NULL unbinds it (the library then allocates
+ * its own on the next call).  Calls whose n needs more than `bytes` return
+ * SC_ERR_WORKSPACE. */
+sc_status sc_set_workspace(void *d_ws, size_t bytes, sc_stream_t stream);
+
+/* Single-pass inclusive / exclusive scan of n elements (one kernel launch).
+ * in == out (in place) is allowed: every tile reads all of its input before it
+ * writes any output, and writes only its own range.  Any other overlap of in
+ * and out is an error (SC_ERR_INVALID). */
+sc_status sc_scan_inclusive(sc_dtype dtype, sc_op op, const void *in, void *out, int64_t n, sc_stream_t stream);
+sc_status sc_scan_exclusive(sc_dtype dtype, sc_op op, const void *in, void *out, int64_t n, sc_stream_t stream);
+
+/* Independent scans of the rows of a row-major rows x cols matrix (leading
+ * dimension cols, contiguous): row r of out is the scan of row r of in, each
+ * starting again from the identity.  One kernel launch: tiles that start a
+ * row take no carry, longer rows chain their tiles through the look-back.
+ * Same dtypes, ops and aliasing rules as sc_scan_inclusive. */
+sc_status sc_scan_batched(sc_dtype dtype, sc_op op, int exclusive, const void *in, void *out,
+                          int64_t rows, int64_t cols, sc_stream_t stream);
+
+/* Fused, order-preserving stream compaction (one kernel launch): out[0..count)
+ * receives, in input order, every in[i] with (in[i] <pred> threshold); the
+ * number kept is written to *d_count (device int64).  out[count..n) is left
+ * untouched.  dtype: SC_I32, SC_U32 or SC_F32.  in and out must not overlap. */
+sc_status sc_compact_if(sc_dtype dtype, const void *in, void *out, int64_t *d_count, int64_t n,
+                        sc_pred pred, double threshold, sc_stream_t stream);
+
+/* The pages' multi-kernel hierarchical design (scan each tile and record its
+ * total; scan the totals, recursively; add each tile's offset back), restated
+ * for sm_103a.  Same results as the single-pass scan (float32: within the same
+ * bound), about twice the memory traffic.  A comparison variant: it needs
+ * extra workspace for the per-level totals (sc_hier_workspace_bytes). */
+sc_status sc_scan_hierarchical(sc_dtype dtype, sc_op op, int exclusive, const void *in, void *out,
+                               int64_t n, sc_stream_t stream);
+size_t sc_hier_workspace_bytes(sc_dtype dtype, int64_t n);
+
+/* Scan of HOST buffers: copies h_in to the device in chunks, scans each chunk
+ * with the single-pass kernel (the running total of the earlier chunks is
+ * carried into the next chunk on the device), and copies the results to h_out,
+ * overlapping the copies in both directions with the kernels.  h_in == h_out
+ * is allowed.  Pinned (page-locked) host memory is needed for the overlap;
+ * pageable memory works but is slower.  Returns after h_out holds the result
+ * (it waits for earlier work on `stream` first).  Device staging memory is
+ * allocated by the library on first use and kept. */
+sc_status sc_scan_host(sc_dtype dtype, sc_op op, int exclusive, const void *h_in, void *h_out, int64_t n,
+                       sc_stream_t stream);
+
+/* Wait for `stream`, then read and clear the device error word of its
+ * workspace.  SC_OK when no kernel reported a failure since the last call. */
+sc_status sc_get_device_error(sc_stream_t stream);
+
+/* Number of kernels this library has launched in this process (all devices). */
+uint64_t sc_launch_count(void);
+
+/* ---- tuning and test hooks (process-wide; affect later launches) ---- */
+
+/* Select one of the precompiled tile shapes of the uint32/int32 sum
+ * (0 = default; see sc_scan_variant_info).  Returns SC_ERR_INVALID for an
+ * unknown variant. */
+sc_status sc_set_scan_variant(int variant);
+/* Threads per CTA, items per thread and loader kind (0 direct, 1 transposed)
+ * of a uint32-sum variant; SC_ERR_INVALID if it does not exist. */
+sc_status sc_scan_variant_info(int variant, int *threads, int *items, int *loader);
+
+/* Look-back test hooks.  stall_tile >= 0: that tile never publishes its
+ * status, so its successors must time out (error SC_ERR_LOOKBACK_TIMEOUT).
+ * delay_tile >= 0: that tile sleeps delay_ns before publishing (exercises
+ * long look-back chains).  timeout_ns: bound on any single look-back wait
+ * (0 restores the default of 2 s).  -1 turns a hook off. */
+sc_status sc_debug_set_lookback(int64_t stall_tile, int64_t delay_tile, uint32_t delay_ns, uint64_t timeout_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SC_SCAN_H */

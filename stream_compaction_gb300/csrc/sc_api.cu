@@ -1,0 +1,610 @@
+// C ABI of the library: argument checks, workspaces, dispatch to the kernels,
+// the host-buffer pipeline and the error word.  See include/sc_scan.h for the
+// contract of every entry point.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cfloat>
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include <cuda_runtime.h>
+
+#include "../../include/sc_scan.h"
+#include "sc_launch.h"
+#include "sc_shapes.h"
+
+namespace {
+
+using scg::CompactParams;
+using scg::HierParams;
+using scg::LookbackCtl;
+using scg::ScanParams;
+
+constexpr size_t kStatusOffset = 256;       // counter at 0, error word at 8
+constexpr int64_t kMinTile = 2048;          // smallest tile of any kernel
+constexpr size_t kSlotBytes = 16;           // one look-back status slot
+constexpr unsigned kMaxEpoch = (1u << 30) - 1;
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
+
+std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_variant{0};
+std::atomic<long long> g_stall_tile{-1};
+std::atomic<long long> g_delay_tile{-1};
+std::atomic<unsigned> g_delay_ns{0};
+std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
+
+// ------------------------------------------------------------ workspaces
+struct Workspace {
+    unsigned char* base = nullptr;
+    size_t bytes = 0;
+    bool owned = false;
+    bool dirty = true;                 // needs a zeroing memset before use
+    unsigned long long counter_base = 0;
+    unsigned epoch = 0;
+};
+
+std::mutex g_ws_mu;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+size_t lookback_bytes(int64_t n) { return kStatusOffset + kSlotBytes * (size_t)ceil_div(std::max<int64_t>(n, 1), kMinTile); }
+
+// Workspace of (current device, stream) with at least `need` bytes, zeroed and
+// ready for the next epoch.  Caller holds g_ws_mu.
+sc_status acquire_ws(cudaStream_t s, size_t need, Workspace** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SC_ERR_CUDA;
+    Workspace& ws = g_ws[{dev, s}];
+    if (ws.bytes < need) {
+        if (ws.base && !ws.owned) return SC_ERR_WORKSPACE;
+        if (ws.base) {
+            cudaFree(ws.base);  // synchronises the device: no kernel still uses it
+            ws.base = nullptr;
+            ws.bytes = 0;
+        }
+        const size_t bytes = std::max(need, (size_t)(1 << 20));
+        void* p = nullptr;
+        if (cudaMalloc(&p, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return SC_ERR_WORKSPACE;
+        }
+        ws.base = static_cast<unsigned char*>(p);
+        ws.bytes = bytes;
+        ws.owned = true;
+        ws.dirty = true;
+    }
+    if (ws.dirty || ws.epoch >= kMaxEpoch) {
+        if (cudaMemsetAsync(ws.base, 0, ws.bytes, s) != cudaSuccess) return SC_ERR_CUDA;
+        ws.counter_base = 0;
+        ws.epoch = 0;
+        ws.dirty = false;
+    }
+    *out = &ws;
+    return SC_OK;
+}
+
+LookbackCtl make_ctl(Workspace& ws, unsigned num_tiles) {
+    LookbackCtl lb;
+    lb.status = reinterpret_cast<unsigned long long*>(ws.base + kStatusOffset);
+    lb.counter = reinterpret_cast<unsigned long long*>(ws.base);
+    lb.error = reinterpret_cast<unsigned int*>(ws.base + 8);
+    lb.counter_base = ws.counter_base;
+    lb.epoch = ++ws.epoch;
+    lb.num_tiles = num_tiles;
+    lb.stall_tile = g_stall_tile.load();
+    lb.delay_tile = g_delay_tile.load();
+    lb.delay_ns = g_delay_ns.load();
+    lb.timeout_ns = g_timeout_ns.load();
+    return lb;
+}
+
+// After a launch: every CTA of the grid takes exactly one tile id, so the
+// counter moved by num_tiles.  A failed launch leaves the counter unknown.
+sc_status finish_launch(Workspace& ws, unsigned num_tiles, cudaError_t e) {
+    g_launches.fetch_add(1);
+    if (e != cudaSuccess) {
+        ws.dirty = true;
+        return SC_ERR_CUDA;
+    }
+    ws.counter_base += num_tiles;
+    return SC_OK;
+}
+
+// ------------------------------------------------------------ validation
+int elem_bytes(sc_dtype d) {
+    switch (d) {
+    case SC_I32: case SC_U32: case SC_F32: return 4;
+    case SC_AFFINE_U32: return 8;
+    default: return 0;
+    }
+}
+
+bool valid_dtype(int d) { return d >= SC_I32 && d <= SC_AFFINE_U32; }
+bool valid_op(int o) { return o >= SC_SUM && o <= SC_COMPOSE; }
+
+// 0 sum u32/i32, 1 sum f32, 2 max i32, 3 affine; -1 unsupported.
+int op_id(sc_dtype d, sc_op o) {
+    if (o == SC_SUM && (d == SC_I32 || d == SC_U32)) return 0;
+    if (o == SC_SUM && d == SC_F32) return 1;
+    if (o == SC_MAX && d == SC_I32) return 2;
+    if (o == SC_COMPOSE && d == SC_AFFINE_U32) return 3;
+    return -1;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// in == out is fine; any other overlap is not.
+bool bad_overlap(const void* a, const void* b, size_t bytes, bool allow_same) {
+    if (a == b) return !allow_same;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + bytes && y < x + bytes;
+}
+
+sc_status check_scan_args(sc_dtype dtype, sc_op op, const void* in, void* out, int64_t n, int* oid) {
+    if (!valid_dtype(dtype) || !valid_op(op) || n < 0) return SC_ERR_INVALID;
+    *oid = op_id(dtype, op);
+    if (*oid < 0) return SC_ERR_UNSUPPORTED;
+    if (n == 0) return SC_OK;
+    if (!in || !out) return SC_ERR_INVALID;
+    const int eb = elem_bytes(dtype);
+    if (!aligned(in, eb) || !aligned(out, eb)) return SC_ERR_INVALID;
+    if ((uint64_t)n > (uint64_t)INT64_MAX / 16) return SC_ERR_INVALID;
+    if (bad_overlap(in, out, (size_t)n * eb, true)) return SC_ERR_INVALID;
+    if (ceil_div(n, kMinTile) > (int64_t)INT_MAX) return SC_ERR_INVALID;  // grid.x limit
+    return SC_OK;
+}
+
+cudaError_t dispatch_scan(int oid, const ScanParams& p, bool excl, bool seg, int variant, cudaStream_t s) {
+    switch (oid) {
+    case 0: return scg::launch_scan<scg::OpSumU32>(p, excl, seg, variant, s);
+    case 1: return scg::launch_scan<scg::OpSumF32>(p, excl, seg, variant, s);
+    case 2: return scg::launch_scan<scg::OpMaxI32>(p, excl, seg, variant, s);
+    case 3: return scg::launch_scan<scg::OpAffineU32>(p, excl, seg, variant, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+// One single-pass scan launch (plain or segmented), with optional carries.
+sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_len, bool excl,
+                   const void* carry_in, void* carry_out, cudaStream_t s) {
+    const int variant = (oid == 0 && seg_len == 0) ? g_variant.load() : 0;
+    const int tile = scg::scan_tile_elems(oid, variant);
+    const unsigned ntiles = (unsigned)ceil_div(n, tile);
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    Workspace* ws = nullptr;
+    sc_status st = acquire_ws(s, lookback_bytes(n), &ws);
+    if (st != SC_OK) return st;
+    ScanParams p;
+    p.in = in;
+    p.out = out;
+    p.n = n;
+    p.seg_len = seg_len;
+    p.vec_ok = aligned(in, 16) && aligned(out, 16);
+    p.carry_in = carry_in;
+    p.carry_out = carry_out;
+    p.lb = make_ctl(*ws, ntiles);
+    return finish_launch(*ws, ntiles, dispatch_scan(oid, p, excl, seg_len > 0, variant, s));
+}
+
+// ------------------------------------------------------ compaction predicate
+// Canonical integer form: keep x when lo <= x <= hi (xor invert), computed
+// exactly from "x <pred> t" with t a double, then clamped to [tmin, tmax].
+scg::PredParams int_pred(sc_pred pred, double t, double tmin, double tmax) {
+    scg::PredParams q{};
+    q.invert = 0;
+    double lo = tmin, hi = tmax;
+    bool empty = false;
+    if (std::isnan(t)) {
+        empty = (pred != SC_NE);  // every comparison with NaN is false, except !=
+    } else {
+        switch (pred) {
+        case SC_GT: lo = std::floor(t) + 1.0; break;
+        case SC_GE: lo = std::ceil(t); break;
+        case SC_LT: hi = std::ceil(t) - 1.0; break;
+        case SC_LE: hi = std::floor(t); break;
+        case SC_EQ:
+        case SC_NE:
+            if (std::floor(t) == t) { lo = hi = t; } else { empty = true; }
+            if (pred == SC_NE) q.invert = 1;
+            break;
+        }
+    }
+    lo = std::max(lo, tmin);
+    hi = std::min(hi, tmax);
+    if (empty || lo > hi) {
+        // empty set; with invert it becomes "everything"
+        q.lo = 1;
+        q.hi = 0;
+        if (tmin < 0) { q.lo = (long long)tmax; q.hi = (long long)tmin; }
+    } else {
+        q.lo = (long long)lo;
+        q.hi = (long long)hi;
+    }
+    return q;
+}
+
+float round_down_f(double t) {
+    float f = (float)t;
+    if ((double)f > t) f = std::nextafter(f, -INFINITY);
+    return f;
+}
+float round_up_f(double t) {
+    float f = (float)t;
+    if ((double)f < t) f = std::nextafter(f, INFINITY);
+    return f;
+}
+
+// Canonical float form: an outcome mask over {x > tf, x == tf, x < tf, NaN}
+// with tf chosen so that the float comparison equals the double one.
+scg::PredParams float_pred(sc_pred pred, double t) {
+    enum : long long { G = 1, E = 2, L = 4, U = 8 };
+    scg::PredParams q{};
+    q.tf = 0.0f;
+    if (std::isnan(t)) {
+        q.lo = (pred == SC_NE) ? (G | E | L | U) : 0;
+        return q;
+    }
+    switch (pred) {
+    case SC_GT: q.tf = round_down_f(t); q.lo = G; break;
+    case SC_GE: q.tf = round_up_f(t); q.lo = G | E; break;
+    case SC_LT: q.tf = round_up_f(t); q.lo = L; break;
+    case SC_LE: q.tf = round_down_f(t); q.lo = L | E; break;
+    case SC_EQ:
+    case SC_NE: {
+        const float f = (float)t;
+        const bool exact = (double)f == t;
+        q.tf = f;
+        if (pred == SC_EQ) q.lo = exact ? E : 0;
+        else q.lo = exact ? (G | L | U) : (G | E | L | U);
+        break;
+    }
+    }
+    return q;
+}
+
+// ------------------------------------------------------ host-buffer pipeline
+struct HostPipe {
+    static constexpr int kBufs = 3;
+    bool ready = false;
+    size_t buf_bytes = 0;
+    void* dbuf[kBufs] = {};
+    void* carry = nullptr;  // two 16-byte slots
+    cudaStream_t h2d = nullptr, cmp = nullptr, d2h = nullptr;
+    cudaEvent_t ev_h2d[kBufs], ev_cmp[kBufs], ev_d2h[kBufs], ev_start;
+    std::mutex mu;
+};
+std::mutex g_pipe_mu;
+std::map<int, HostPipe*> g_pipes;
+constexpr size_t kPipeBufBytes = 64ull << 20;  // 64 MiB per staging buffer
+
+sc_status pipe_init(HostPipe& hp) {
+    if (hp.ready) return SC_OK;
+    for (int i = 0; i < HostPipe::kBufs; ++i)
+        if (cudaMalloc(&hp.dbuf[i], kPipeBufBytes) != cudaSuccess) return SC_ERR_WORKSPACE;
+    if (cudaMalloc(&hp.carry, 64) != cudaSuccess) return SC_ERR_WORKSPACE;
+    if (cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&hp.cmp, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) != cudaSuccess)
+        return SC_ERR_CUDA;
+    for (int i = 0; i < HostPipe::kBufs; ++i) {
+        if (cudaEventCreateWithFlags(&hp.ev_h2d[i], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&hp.ev_cmp[i], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&hp.ev_d2h[i], cudaEventDisableTiming) != cudaSuccess)
+            return SC_ERR_CUDA;
+    }
+    if (cudaEventCreateWithFlags(&hp.ev_start, cudaEventDisableTiming) != cudaSuccess) return SC_ERR_CUDA;
+    hp.buf_bytes = kPipeBufBytes;
+    hp.ready = true;
+    return SC_OK;
+}
+
+}  // namespace
+
+// ============================================================ public ABI
+extern "C" {
+
+const char* sc_version(void) { return "sc_gb300 1.0 (sm_103a)"; }
+
+const char* sc_status_string(sc_status s) {
+    switch (s) {
+    case SC_OK: return "SC_OK";
+    case SC_ERR_INVALID: return "SC_ERR_INVALID: invalid argument";
+    case SC_ERR_UNSUPPORTED: return "SC_ERR_UNSUPPORTED: dtype/op combination not provided";
+    case SC_ERR_WORKSPACE: return "SC_ERR_WORKSPACE: workspace too small or allocation failed";
+    case SC_ERR_CUDA: return "SC_ERR_CUDA: CUDA runtime error";
+    case SC_ERR_LOOKBACK_TIMEOUT: return "SC_ERR_LOOKBACK_TIMEOUT: a tile gave up waiting on its predecessors";
+    default: return "unknown sc_status";
+    }
+}
+
+size_t sc_workspace_bytes(int64_t n) { return lookback_bytes(n < 0 ? 0 : n); }
+
+sc_status sc_set_workspace(void* d_ws, size_t bytes, sc_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SC_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    auto it = g_ws.find({dev, s});
+    if (it != g_ws.end()) {
+        if (it->second.owned && it->second.base) cudaFree(it->second.base);
+        g_ws.erase(it);
+    }
+    if (!d_ws) return SC_OK;
+    if (!aligned(d_ws, 256) || bytes < lookback_bytes(1)) return SC_ERR_INVALID;
+    Workspace& ws = g_ws[{dev, s}];
+    ws.base = static_cast<unsigned char*>(d_ws);
+    ws.bytes = bytes;
+    ws.owned = false;
+    ws.dirty = true;
+    return SC_OK;
+}
+
+static sc_status scan_common(sc_dtype dtype, sc_op op, const void* in, void* out, int64_t n, sc_stream_t stream,
+                             bool excl) {
+    int oid = -1;
+    sc_status st = check_scan_args(dtype, op, in, out, n, &oid);
+    if (st != SC_OK || n == 0) return st;
+    return run_scan(oid, in, out, n, 0, excl, nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sc_status sc_scan_inclusive(sc_dtype dtype, sc_op op, const void* in, void* out, int64_t n, sc_stream_t stream) {
+    return scan_common(dtype, op, in, out, n, stream, false);
+}
+
+sc_status sc_scan_exclusive(sc_dtype dtype, sc_op op, const void* in, void* out, int64_t n, sc_stream_t stream) {
+    return scan_common(dtype, op, in, out, n, stream, true);
+}
+
+sc_status sc_scan_batched(sc_dtype dtype, sc_op op, int exclusive, const void* in, void* out, int64_t rows,
+                          int64_t cols, sc_stream_t stream) {
+    if (rows < 0 || cols < 0) return SC_ERR_INVALID;
+    if (cols > 0 && rows > INT64_MAX / cols) return SC_ERR_INVALID;
+    const int64_t n = rows * cols;
+    int oid = -1;
+    sc_status st = check_scan_args(dtype, op, in, out, n, &oid);
+    if (st != SC_OK || n == 0) return st;
+    const int64_t seg = rows == 1 ? 0 : cols;
+    return run_scan(oid, in, out, n, seg, exclusive != 0, nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sc_status sc_compact_if(sc_dtype dtype, const void* in, void* out, int64_t* d_count, int64_t n, sc_pred pred,
+                        double threshold, sc_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!valid_dtype(dtype) || n < 0 || pred < SC_GT || pred > SC_NE) return SC_ERR_INVALID;
+    if (dtype != SC_I32 && dtype != SC_U32 && dtype != SC_F32) return SC_ERR_UNSUPPORTED;
+    if (!d_count || !aligned(d_count, 8)) return SC_ERR_INVALID;
+    if (n == 0) {
+        if (cudaMemsetAsync(d_count, 0, sizeof(int64_t), s) != cudaSuccess) return SC_ERR_CUDA;
+        return SC_OK;
+    }
+    if (!in || !out || !aligned(in, 4) || !aligned(out, 4)) return SC_ERR_INVALID;
+    if ((uint64_t)n > (uint64_t)INT64_MAX / 16) return SC_ERR_INVALID;
+    if (bad_overlap(in, out, (size_t)n * 4, false)) return SC_ERR_INVALID;
+    if (ceil_div(n, scg::CompactConfig::TILE) > (int64_t)INT_MAX) return SC_ERR_INVALID;
+
+    CompactParams p;
+    p.in = in;
+    p.out = out;
+    p.count = reinterpret_cast<long long*>(d_count);
+    p.n = n;
+    p.vec_ok = aligned(in, 16);
+    if (dtype == SC_I32) p.pred = int_pred(pred, threshold, (double)INT32_MIN, (double)INT32_MAX);
+    else if (dtype == SC_U32) p.pred = int_pred(pred, threshold, 0.0, (double)UINT32_MAX);
+    else p.pred = float_pred(pred, threshold);
+
+    const unsigned ntiles = (unsigned)ceil_div(n, scg::CompactConfig::TILE);
+    const bool wide = n > (int64_t)UINT32_MAX;
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    Workspace* ws = nullptr;
+    sc_status st = acquire_ws(s, lookback_bytes(n), &ws);
+    if (st != SC_OK) return st;
+    p.lb = make_ctl(*ws, ntiles);
+    cudaError_t e;
+    if (dtype == SC_I32) e = scg::launch_compact<int32_t>(p, wide, s);
+    else if (dtype == SC_U32) e = scg::launch_compact<uint32_t>(p, wide, s);
+    else e = scg::launch_compact<float>(p, wide, s);
+    return finish_launch(*ws, ntiles, e);
+}
+
+size_t sc_hier_workspace_bytes(sc_dtype dtype, int64_t n) {
+    if (!valid_dtype(dtype) || n <= 0) return 0;
+    const int oid = dtype == SC_AFFINE_U32 ? 3 : 0;
+    const int64_t t = scg::hier_tile_elems(oid);
+    size_t total = 0;
+    for (int64_t m = n; m > 1;) {
+        const int64_t k = ceil_div(m, t);
+        total += (size_t)ceil_div(k * elem_bytes(dtype), 256) * 256;
+        m = k;
+    }
+    return total + 256;
+}
+
+static cudaError_t dispatch_hier_tiles(int oid, const HierParams& p, bool excl, unsigned nt, cudaStream_t s) {
+    switch (oid) {
+    case 0: return scg::launch_hier_tiles<scg::OpSumU32>(p, excl, nt, s);
+    case 1: return scg::launch_hier_tiles<scg::OpSumF32>(p, excl, nt, s);
+    case 2: return scg::launch_hier_tiles<scg::OpMaxI32>(p, excl, nt, s);
+    case 3: return scg::launch_hier_tiles<scg::OpAffineU32>(p, excl, nt, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+static cudaError_t dispatch_hier_add(int oid, const HierParams& p, unsigned nt, cudaStream_t s) {
+    switch (oid) {
+    case 0: return scg::launch_hier_add<scg::OpSumU32>(p, nt, s);
+    case 1: return scg::launch_hier_add<scg::OpSumF32>(p, nt, s);
+    case 2: return scg::launch_hier_add<scg::OpMaxI32>(p, nt, s);
+    case 3: return scg::launch_hier_add<scg::OpAffineU32>(p, nt, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+// Level l: scan `in` (m elements) into `out` tile by tile, totals into
+// level_buf[l]; recursively exclusive-scan the totals in place; add them back.
+static sc_status hier_level(int oid, int eb, const void* in, void* out, int64_t m, bool excl, unsigned char* scratch,
+                            size_t scratch_off, cudaStream_t s) {
+    const int64_t t = scg::hier_tile_elems(oid);
+    const unsigned nt = (unsigned)ceil_div(m, t);
+    void* totals = scratch + scratch_off;
+    const size_t next_off = scratch_off + (size_t)ceil_div((int64_t)nt * eb, 256) * 256;
+    HierParams p;
+    p.in = in;
+    p.out = out;
+    p.totals = totals;
+    p.offsets = totals;
+    p.n = m;
+    p.vec_ok = aligned(in, 16) && aligned(out, 16);
+    cudaError_t e = dispatch_hier_tiles(oid, p, excl, nt, s);
+    g_launches.fetch_add(1);
+    if (e != cudaSuccess) return SC_ERR_CUDA;
+    if (nt > 1) {
+        sc_status st = hier_level(oid, eb, totals, totals, nt, true, scratch, next_off, s);
+        if (st != SC_OK) return st;
+        e = dispatch_hier_add(oid, p, nt, s);
+        g_launches.fetch_add(1);
+        if (e != cudaSuccess) return SC_ERR_CUDA;
+    }
+    return SC_OK;
+}
+
+sc_status sc_scan_hierarchical(sc_dtype dtype, sc_op op, int exclusive, const void* in, void* out, int64_t n,
+                               sc_stream_t stream) {
+    int oid = -1;
+    sc_status st = check_scan_args(dtype, op, in, out, n, &oid);
+    if (st != SC_OK || n == 0) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t need = kStatusOffset + sc_hier_workspace_bytes(dtype, n);
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    Workspace* ws = nullptr;
+    st = acquire_ws(s, std::max(need, lookback_bytes(n)), &ws);
+    if (st != SC_OK) return st;
+    return hier_level(oid, elem_bytes(dtype), in, out, n, exclusive != 0, ws->base, kStatusOffset, s);
+}
+
+sc_status sc_scan_host(sc_dtype dtype, sc_op op, int exclusive, const void* h_in, void* h_out, int64_t n,
+                       sc_stream_t stream) {
+    int oid = -1;
+    if (!valid_dtype(dtype) || !valid_op(op) || n < 0) return SC_ERR_INVALID;
+    oid = op_id(dtype, op);
+    if (oid < 0) return SC_ERR_UNSUPPORTED;
+    if (n == 0) return SC_OK;
+    if (!h_in || !h_out) return SC_ERR_INVALID;
+    const int eb = elem_bytes(dtype);
+    if (bad_overlap(h_in, h_out, (size_t)n * eb, true)) return SC_ERR_INVALID;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SC_ERR_CUDA;
+    HostPipe* hp;
+    {
+        std::lock_guard<std::mutex> lk(g_pipe_mu);
+        HostPipe*& slot = g_pipes[dev];
+        if (!slot) slot = new HostPipe();
+        hp = slot;
+    }
+    std::lock_guard<std::mutex> lk(hp->mu);
+    sc_status st = pipe_init(*hp);
+    if (st != SC_OK) return st;
+    cudaStream_t caller = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t chunk = (int64_t)(hp->buf_bytes / eb);
+    const int64_t nchunks = ceil_div(n, chunk);
+    if (cudaEventRecord(hp->ev_start, caller) != cudaSuccess) return SC_ERR_CUDA;
+    cudaStreamWaitEvent(hp->h2d, hp->ev_start, 0);
+    cudaStreamWaitEvent(hp->cmp, hp->ev_start, 0);
+    const unsigned char* src = static_cast<const unsigned char*>(h_in);
+    unsigned char* dst = static_cast<unsigned char*>(h_out);
+    unsigned char* carry = static_cast<unsigned char*>(hp->carry);
+    for (int64_t i = 0; i < nchunks; ++i) {
+        const int b = (int)(i % HostPipe::kBufs);
+        const int64_t off = i * chunk;
+        const int64_t cn = std::min(chunk, n - off);
+        const size_t bytes = (size_t)cn * eb;
+        if (i >= HostPipe::kBufs) cudaStreamWaitEvent(hp->h2d, hp->ev_d2h[b], 0);
+        if (cudaMemcpyAsync(hp->dbuf[b], src + off * eb, bytes, cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess)
+            return SC_ERR_CUDA;
+        cudaEventRecord(hp->ev_h2d[b], hp->h2d);
+        cudaStreamWaitEvent(hp->cmp, hp->ev_h2d[b], 0);
+        const void* cin = i > 0 ? carry + 16 * ((i - 1) & 1) : nullptr;
+        void* cout = carry + 16 * (i & 1);
+        st = run_scan(oid, hp->dbuf[b], hp->dbuf[b], cn, 0, exclusive != 0, cin, cout, hp->cmp);
+        if (st != SC_OK) return st;
+        cudaEventRecord(hp->ev_cmp[b], hp->cmp);
+        cudaStreamWaitEvent(hp->d2h, hp->ev_cmp[b], 0);
+        if (cudaMemcpyAsync(dst + off * eb, hp->dbuf[b], bytes, cudaMemcpyDeviceToHost, hp->d2h) != cudaSuccess)
+            return SC_ERR_CUDA;
+        cudaEventRecord(hp->ev_d2h[b], hp->d2h);
+    }
+    if (cudaStreamSynchronize(hp->d2h) != cudaSuccess || cudaStreamSynchronize(hp->cmp) != cudaSuccess)
+        return SC_ERR_CUDA;
+    return sc_get_device_error(reinterpret_cast<sc_stream_t>(hp->cmp));
+}
+
+sc_status sc_get_device_error(sc_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SC_ERR_CUDA;
+    unsigned int* err = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_ws_mu);
+        auto it = g_ws.find({dev, s});
+        if (it != g_ws.end() && it->second.base) err = reinterpret_cast<unsigned int*>(it->second.base + 8);
+    }
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SC_ERR_CUDA;
+    if (!err) return SC_OK;
+    unsigned int h = 0;
+    if (cudaMemcpy(&h, err, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return SC_ERR_CUDA;
+    if (h != 0) {
+        if (cudaMemset(err, 0, sizeof(h)) != cudaSuccess) return SC_ERR_CUDA;
+        return (sc_status)h;
+    }
+    return SC_OK;
+}
+
+uint64_t sc_launch_count(void) { return g_launches.load(); }
+
+sc_status sc_set_scan_variant(int variant) {
+    if (variant < 0 || variant >= scg::kNumSumU32Variants) return SC_ERR_INVALID;
+    g_variant.store(variant);
+    return SC_OK;
+}
+
+sc_status sc_scan_variant_info(int variant, int* threads, int* items, int* loader) {
+    if (variant < 0 || variant >= scg::kNumSumU32Variants) return SC_ERR_INVALID;
+    const scg::ScanShape sh = scg::kShapeSumU32[variant];
+    if (threads) *threads = sh.nt;
+    if (items) *items = sh.ipt;
+    if (loader) *loader = sh.load;
+    return SC_OK;
+}
+
+sc_status sc_debug_set_lookback(int64_t stall_tile, int64_t delay_tile, uint32_t delay_ns, uint64_t timeout_ns) {
+    if (stall_tile < -1 || delay_tile < -1) return SC_ERR_INVALID;
+    if (delay_ns > 1000000000u) return SC_ERR_INVALID;
+    g_stall_tile.store(stall_tile);
+    g_delay_tile.store(delay_tile);
+    g_delay_ns.store(delay_ns);
+    g_timeout_ns.store(timeout_ns == 0 ? kDefaultTimeoutNs : timeout_ns);
+    return SC_OK;
+}
+
+}  // extern "C"
+
+// Tile sizes (host side).
+namespace scg {
+int scan_tile_elems(int op_id, int variant) {
+    const ScanShape sh = scan_shape(op_id, variant);
+    return sh.nt * sh.ipt;
+}
+ScanShape scan_shape(int op_id, int variant) {
+    switch (op_id) {
+    case 0: return (variant >= 0 && variant < kNumSumU32Variants) ? kShapeSumU32[variant] : ScanShape{0, 0, 0};
+    case 1: return variant == 0 ? kShapeSumF32 : ScanShape{0, 0, 0};
+    case 2: return variant == 0 ? kShapeMaxI32 : ScanShape{0, 0, 0};
+    case 3: return variant == 0 ? kShapeAffine : ScanShape{0, 0, 0};
+    default: return ScanShape{0, 0, 0};
+    }
+}
+}  // namespace scg

@@ -1,0 +1,369 @@
+// Device building blocks of the single-pass scan: operators, status words of
+// the decoupled look-back, tile loads/stores, and the thread/warp/block scan.
+//
+// Scan definitions (inclusive y[i] = x[0] (+) ... (+) x[i]; exclusive y[0] = I,
+// y[i] = x[0] (+) ... (+) x[i-1]) follow "Lecture 7: Parallel pattern -- prefix
+// sum / scan" (UIUC ECE408 notes), section 1, and "Chapter 9 Parallel Patterns:
+// Prefix Sum - Scan Algorithms" (PMPP notes), section 9.1.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "sc_params.h"
+
+namespace scg {
+
+// ----------------------------------------------------------------- operators
+// Each operator has an element type T (what the tile is scanned in) and a
+// carry type C (what travels between tiles through the look-back).  Only the
+// float32 sum has C != T: its inter-tile carry is fp64 so that the error of a
+// prefix stays a small multiple of eps * sum|x| however many tiles precede it.
+
+struct OpSumU32 {  // int32 and uint32 sums: two's-complement wraparound mod 2^32
+    using T = uint32_t;
+    using C = uint32_t;
+    __device__ __forceinline__ static T identity() { return 0u; }
+    __device__ __forceinline__ static T op(T a, T b) { return a + b; }
+    __device__ __forceinline__ static C c_identity() { return 0u; }
+    __device__ __forceinline__ static C c_op(C a, C b) { return a + b; }
+    __device__ __forceinline__ static C lift(T a) { return a; }
+    __device__ __forceinline__ static T lower(C c) { return c; }
+};
+
+struct OpSumF32 {
+    using T = float;
+    using C = double;
+    __device__ __forceinline__ static T identity() { return 0.0f; }
+    __device__ __forceinline__ static T op(T a, T b) { return __fadd_rn(a, b); }
+    __device__ __forceinline__ static C c_identity() { return 0.0; }
+    __device__ __forceinline__ static C c_op(C a, C b) { return __dadd_rn(a, b); }
+    __device__ __forceinline__ static C lift(T a) { return (double)a; }
+    __device__ __forceinline__ static T lower(C c) { return __double2float_rn(c); }
+};
+
+struct OpMaxI32 {  // identity INT32_MIN (the "-infinity" of the PMPP identity table)
+    using T = int32_t;
+    using C = int32_t;
+    __device__ __forceinline__ static T identity() { return INT32_MIN; }
+    __device__ __forceinline__ static T op(T a, T b) { return max(a, b); }
+    __device__ __forceinline__ static C c_identity() { return INT32_MIN; }
+    __device__ __forceinline__ static C c_op(C a, C b) { return max(a, b); }
+    __device__ __forceinline__ static C lift(T a) { return a; }
+    __device__ __forceinline__ static T lower(C c) { return c; }
+};
+
+// Affine maps h -> a*h + b (mod 2^32) stored as uint2 {x = a, y = b}.
+// l (+) r applies l first, then r:  (r.a*l.a, r.a*l.b + r.b).  Not commutative,
+// so every combine below keeps the earlier operand on the left.
+struct OpAffineU32 {
+    using T = uint2;
+    using C = uint2;
+    __device__ __forceinline__ static T identity() { return make_uint2(1u, 0u); }
+    __device__ __forceinline__ static T op(T l, T r) { return make_uint2(r.x * l.x, r.x * l.y + r.y); }
+    __device__ __forceinline__ static C c_identity() { return make_uint2(1u, 0u); }
+    __device__ __forceinline__ static C c_op(C l, C r) { return op(l, r); }
+    __device__ __forceinline__ static C lift(T a) { return a; }
+    __device__ __forceinline__ static T lower(C c) { return c; }
+};
+
+// Counts for the fused compaction.
+struct OpCountU32 {
+    using T = uint32_t;
+    using C = uint32_t;
+    __device__ __forceinline__ static T identity() { return 0u; }
+    __device__ __forceinline__ static T op(T a, T b) { return a + b; }
+    __device__ __forceinline__ static C c_identity() { return 0u; }
+    __device__ __forceinline__ static C c_op(C a, C b) { return a + b; }
+    __device__ __forceinline__ static C lift(T a) { return a; }
+    __device__ __forceinline__ static T lower(C c) { return c; }
+};
+
+struct OpCountU64 {
+    using T = uint32_t;                 // per-tile counts fit 32 bits
+    using C = unsigned long long;       // running count may exceed 2^32
+    __device__ __forceinline__ static T identity() { return 0u; }
+    __device__ __forceinline__ static T op(T a, T b) { return a + b; }
+    __device__ __forceinline__ static C c_identity() { return 0ull; }
+    __device__ __forceinline__ static C c_op(C a, C b) { return a + b; }
+    __device__ __forceinline__ static C lift(T a) { return a; }
+    __device__ __forceinline__ static T lower(C c) { return (T)c; }
+};
+
+// ------------------------------------------------------------- bit plumbing
+__device__ __forceinline__ uint32_t to_bits32(uint32_t v) { return v; }
+__device__ __forceinline__ uint32_t to_bits32(int32_t v) { return (uint32_t)v; }
+__device__ __forceinline__ uint32_t to_bits32(float v) { return __float_as_uint(v); }
+__device__ __forceinline__ void from_bits32(uint32_t b, uint32_t& v) { v = b; }
+__device__ __forceinline__ void from_bits32(uint32_t b, int32_t& v) { v = (int32_t)b; }
+__device__ __forceinline__ void from_bits32(uint32_t b, float& v) { v = __uint_as_float(b); }
+
+__device__ __forceinline__ unsigned long long to_bits64(double v) { return (unsigned long long)__double_as_longlong(v); }
+__device__ __forceinline__ unsigned long long to_bits64(uint2 v) { return ((unsigned long long)v.y << 32) | v.x; }
+__device__ __forceinline__ unsigned long long to_bits64(unsigned long long v) { return v; }
+__device__ __forceinline__ void from_bits64(unsigned long long b, double& v) { v = __longlong_as_double((long long)b); }
+__device__ __forceinline__ void from_bits64(unsigned long long b, uint2& v) { v = make_uint2((uint32_t)b, (uint32_t)(b >> 32)); }
+__device__ __forceinline__ void from_bits64(unsigned long long b, unsigned long long& v) { v = b; }
+
+// Warp shuffles for 4- and 8-byte value types.
+template <class V>
+__device__ __forceinline__ V shfl_up_v(V v, int d) {
+    if constexpr (sizeof(V) == 4) {
+        V r; from_bits32(__shfl_up_sync(0xffffffffu, to_bits32(v), d), r); return r;
+    } else {
+        unsigned long long b = to_bits64(v);
+        uint32_t lo = __shfl_up_sync(0xffffffffu, (uint32_t)b, d);
+        uint32_t hi = __shfl_up_sync(0xffffffffu, (uint32_t)(b >> 32), d);
+        V r; from_bits64(((unsigned long long)hi << 32) | lo, r); return r;
+    }
+}
+template <class V>
+__device__ __forceinline__ V shfl_down_v(V v, int d) {
+    if constexpr (sizeof(V) == 4) {
+        V r; from_bits32(__shfl_down_sync(0xffffffffu, to_bits32(v), d), r); return r;
+    } else {
+        unsigned long long b = to_bits64(v);
+        uint32_t lo = __shfl_down_sync(0xffffffffu, (uint32_t)b, d);
+        uint32_t hi = __shfl_down_sync(0xffffffffu, (uint32_t)(b >> 32), d);
+        V r; from_bits64(((unsigned long long)hi << 32) | lo, r); return r;
+    }
+}
+template <class V>
+__device__ __forceinline__ V shfl_idx_v(V v, int src) {
+    if constexpr (sizeof(V) == 4) {
+        V r; from_bits32(__shfl_sync(0xffffffffu, to_bits32(v), src), r); return r;
+    } else {
+        unsigned long long b = to_bits64(v);
+        uint32_t lo = __shfl_sync(0xffffffffu, (uint32_t)b, src);
+        uint32_t hi = __shfl_sync(0xffffffffu, (uint32_t)(b >> 32), src);
+        V r; from_bits64(((unsigned long long)hi << 32) | lo, r); return r;
+    }
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() { uint32_t m; asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m)); return m; }
+__device__ __forceinline__ uint32_t lanemask_le() { uint32_t m; asm("mov.u32 %0, %%lanemask_le;" : "=r"(m)); return m; }
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---------------------------------------------------- look-back status words
+// Strong (relaxed, gpu-scope) accesses: they bypass the non-coherent L1 so a
+// spinning reader sees another SM's store.  The payload lives inside the same
+// 64-bit word as its flag and epoch, so no extra ordering is needed: a word
+// is read whole or not at all.
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void ld_relaxed_v2u64(const unsigned long long* p, unsigned long long& a,
+                                                 unsigned long long& b) {
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_v2u64(unsigned long long* p, unsigned long long a, unsigned long long b) {
+    asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+}
+
+// A 4-byte carry travels in one word: [payload:32 | epoch:30 | flag:2].
+// An 8-byte carry travels in two words (one 16-byte store), each holding one
+// half of the payload and the same [epoch | flag] tag; a reader accepts the
+// pair only when both tags agree, so a half-updated pair reads as "not yet".
+template <class C>
+struct StatusIO {
+    static constexpr int kWords = sizeof(C) == 4 ? 1 : 2;
+
+    __device__ __forceinline__ static void publish(const LookbackCtl& lb, long long tile, unsigned flag, C v) {
+        const unsigned long long tag = ((unsigned long long)lb.epoch << 2) | flag;
+        if constexpr (kWords == 1) {
+            st_relaxed_u64(lb.status + tile, ((unsigned long long)to_bits32(v) << 32) | tag);
+        } else {
+            const unsigned long long b = to_bits64(v);
+            st_relaxed_v2u64(lb.status + 2 * tile, (b << 32) | tag, (b & 0xffffffff00000000ull) | tag);
+        }
+    }
+
+    // Returns the flag (ST_INVALID when the word belongs to another call).
+    __device__ __forceinline__ static unsigned read(const LookbackCtl& lb, long long tile, C& v) {
+        if constexpr (kWords == 1) {
+            const unsigned long long w = ld_relaxed_u64(lb.status + tile);
+            const uint32_t tag = (uint32_t)w;
+            if ((tag >> 2) != lb.epoch) return ST_INVALID;
+            from_bits32((uint32_t)(w >> 32), v);
+            return tag & 3u;
+        } else {
+            unsigned long long w0, w1;
+            ld_relaxed_v2u64(lb.status + 2 * tile, w0, w1);
+            const uint32_t t0 = (uint32_t)w0, t1 = (uint32_t)w1;
+            if (t0 != t1 || (t0 >> 2) != lb.epoch) return ST_INVALID;
+            from_bits64((w1 & 0xffffffff00000000ull) | (w0 >> 32), v);
+            return t0 & 3u;
+        }
+    }
+};
+
+// Record a device-side failure (first error wins).
+__device__ __forceinline__ void raise_error(unsigned int* err, unsigned code) { atomicCAS(err, 0u, code); }
+
+// Warp-collective decoupled look-back for tile `tile` (> 0).  Lane l reads the
+// status of predecessor (end - 32 + l); the window slides 32 tiles back at a
+// time until it holds a tile with an inclusive prefix (P).  Within a window the
+// newest P and every aggregate (A) after it are folded in tile order, older
+// operand on the left, so non-commutative operators are safe.  Every wait is
+// bounded: past lb.timeout_ns (or a poll cap) the warp gives up.  Returns
+// false on timeout or when a predecessor is poisoned.
+template <class Op>
+__device__ bool lookback_prefix(const LookbackCtl& lb, long long tile, typename Op::C& prefix) {
+    using C = typename Op::C;
+    const int lane = threadIdx.x & 31;
+    C acc = Op::c_identity();
+    long long end = tile;
+    unsigned long long t_start = 0;
+    unsigned polls = 0;
+    unsigned sleep_ns = 20;
+    while (true) {
+        const long long pred = end - 32 + lane;
+        C val = Op::c_identity();
+        unsigned flag = ST_PREFIX;  // tiles before 0 act as an identity prefix
+        if (pred >= 0) flag = StatusIO<C>::read(lb, pred, val);
+        if (__any_sync(0xffffffffu, flag == ST_POISON)) return false;
+        if (__any_sync(0xffffffffu, flag == ST_INVALID)) {
+            if (t_start == 0) t_start = global_ns();
+            ++polls;
+            if (polls > (1u << 26) || global_ns() - t_start > lb.timeout_ns) {
+                if (lane == 0) raise_error(lb.error, DEV_LOOKBACK_TIMEOUT);
+                return false;
+            }
+            __nanosleep(sleep_ns);
+            sleep_ns = min(sleep_ns * 2u, 512u);
+            continue;
+        }
+        const uint32_t pm = __ballot_sync(0xffffffffu, flag == ST_PREFIX);
+        const int newest_p = pm ? 31 - __clz(pm) : -1;
+        C x = lane < newest_p ? Op::c_identity() : val;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const C y = shfl_down_v(x, d);
+            if (lane + d < 32) x = Op::c_op(x, y);
+        }
+        acc = Op::c_op(shfl_idx_v(x, 0), acc);
+        if (pm) break;
+        end -= 32;
+    }
+    prefix = acc;
+    return true;
+}
+
+// --------------------------------------------------------------- tile I/O
+// 16-byte vectors <-> items.
+template <class T>
+struct Vec {
+    static constexpr int kPer = 16 / sizeof(T);
+};
+
+__device__ __forceinline__ void unpack(const uint4& r, uint32_t* v) { v[0] = r.x; v[1] = r.y; v[2] = r.z; v[3] = r.w; }
+__device__ __forceinline__ void unpack(const uint4& r, int32_t* v) {
+    v[0] = (int32_t)r.x; v[1] = (int32_t)r.y; v[2] = (int32_t)r.z; v[3] = (int32_t)r.w;
+}
+__device__ __forceinline__ void unpack(const uint4& r, float* v) {
+    v[0] = __uint_as_float(r.x); v[1] = __uint_as_float(r.y); v[2] = __uint_as_float(r.z); v[3] = __uint_as_float(r.w);
+}
+__device__ __forceinline__ void unpack(const uint4& r, uint2* v) { v[0] = make_uint2(r.x, r.y); v[1] = make_uint2(r.z, r.w); }
+
+__device__ __forceinline__ uint4 pack(const uint32_t* v) { return make_uint4(v[0], v[1], v[2], v[3]); }
+__device__ __forceinline__ uint4 pack(const int32_t* v) { return make_uint4((uint32_t)v[0], (uint32_t)v[1], (uint32_t)v[2], (uint32_t)v[3]); }
+__device__ __forceinline__ uint4 pack(const float* v) {
+    return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
+}
+__device__ __forceinline__ uint4 pack(const uint2* v) { return make_uint4(v[0].x, v[0].y, v[1].x, v[1].y); }
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ void st_stream(uint4* p, const uint4& r) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(r.x), "r"(r.y), "r"(r.z), "r"(r.w)
+                 : "memory");
+}
+
+// Loader kinds.
+//   LOAD_DIRECT: each thread reads its own IPT contiguous items with 16-byte loads.
+//   LOAD_XPOSE : each warp reads its 32*IPT items fully coalesced (lane-contiguous
+//                16-byte vectors) and transposes them to the blocked arrangement
+//                through a swizzled shared-memory buffer private to the warp.
+enum { LOAD_DIRECT = 0, LOAD_XPOSE = 1 };
+
+// XOR swizzle of 16-byte chunk c inside a warp's buffer: keeps both the striped
+// writes and the blocked reads (stride IPT*sizeof(T) bytes) free of bank conflicts.
+__device__ __forceinline__ int swz(int c) { return c ^ ((c >> 3) & 7); }
+
+template <class T, int IPT, int kLoad>
+__device__ __forceinline__ void load_full_tile(const T* __restrict__ tile_in, T (&v)[IPT], uint4* warp_buf) {
+    constexpr int NV = IPT / Vec<T>::kPer;
+    const int lane = threadIdx.x & 31;
+    uint4 r[NV];
+    if constexpr (kLoad == LOAD_DIRECT) {
+        const uint4* src = reinterpret_cast<const uint4*>(tile_in) + threadIdx.x * NV;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) r[j] = __ldg(src + j);
+    } else {
+        const uint4* src = reinterpret_cast<const uint4*>(tile_in) + (threadIdx.x >> 5) * 32 * NV;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) r[j] = ld_stream(src + j * 32 + lane);
+#pragma unroll
+        for (int j = 0; j < NV; ++j) warp_buf[swz(j * 32 + lane)] = r[j];
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < NV; ++j) r[j] = warp_buf[swz(lane * NV + j)];
+    }
+#pragma unroll
+    for (int j = 0; j < NV; ++j) unpack(r[j], &v[j * Vec<T>::kPer]);
+}
+
+template <class T, int IPT, int kLoad>
+__device__ __forceinline__ void store_full_tile(T* __restrict__ tile_out, const T (&v)[IPT], uint4* warp_buf) {
+    constexpr int NV = IPT / Vec<T>::kPer;
+    const int lane = threadIdx.x & 31;
+    uint4 r[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) r[j] = pack(&v[j * Vec<T>::kPer]);
+    if constexpr (kLoad == LOAD_DIRECT) {
+        uint4* dst = reinterpret_cast<uint4*>(tile_out) + threadIdx.x * NV;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) dst[j] = r[j];
+    } else {
+        __syncwarp();  // every lane has finished reading the load transpose
+#pragma unroll
+        for (int j = 0; j < NV; ++j) warp_buf[swz(lane * NV + j)] = r[j];
+        __syncwarp();
+        uint4* dst = reinterpret_cast<uint4*>(tile_out) + (threadIdx.x >> 5) * 32 * NV;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) st_stream(dst + j * 32 + lane, warp_buf[swz(j * 32 + lane)]);
+    }
+}
+
+// Partial (last) tile, or pointers that are not 16-byte aligned: element loads
+// with a bound check; slots past the end hold the identity (so they do not
+// change any prefix) and are never stored.
+template <class T, int IPT>
+__device__ __forceinline__ void load_partial_tile(const T* __restrict__ tile_in, T (&v)[IPT], long long valid, T ident) {
+    const long long base = (long long)threadIdx.x * IPT;
+#pragma unroll
+    for (int k = 0; k < IPT; ++k) v[k] = (base + k < valid) ? tile_in[base + k] : ident;
+}
+
+template <class T, int IPT>
+__device__ __forceinline__ void store_partial_tile(T* __restrict__ tile_out, const T (&v)[IPT], long long valid) {
+    const long long base = (long long)threadIdx.x * IPT;
+#pragma unroll
+    for (int k = 0; k < IPT; ++k)
+        if (base + k < valid) tile_out[base + k] = v[k];
+}
+
+}  // namespace scg

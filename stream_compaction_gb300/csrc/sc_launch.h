@@ -1,0 +1,57 @@
+// Kernel launchers (host side), one set per translation unit.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "sc_params.h"
+
+namespace scg {
+
+struct OpSumU32;
+struct OpSumF32;
+struct OpMaxI32;
+struct OpAffineU32;
+
+// Tile shape of the fused compaction: 256 threads x 16 items.
+struct CompactConfig {
+    static constexpr int NT = 256;
+    static constexpr int IPT = 16;
+    static constexpr int TILE = NT * IPT;
+};
+
+// Single-pass scan tile shapes.  Variant 0 is the default of every operator;
+// the uint32 sum also carries alternative shapes (selected through the tuning
+// hook) so that tile size, block size and loader can be compared on the GPU
+// without a rebuild.
+struct ScanShape {
+    int nt;    // threads per CTA
+    int ipt;   // items per thread
+    int load;  // LOAD_DIRECT / LOAD_XPOSE
+};
+
+constexpr int kNumSumU32Variants = 5;
+
+// Tile size (elements) of operator `op_id` (0 sum u32, 1 sum f32, 2 max i32,
+// 3 affine) in the given variant; 0 if that variant does not exist.
+int scan_tile_elems(int op_id, int variant);
+ScanShape scan_shape(int op_id, int variant);
+
+template <class Op>
+cudaError_t launch_scan(const ScanParams& p, bool exclusive, bool segmented, int variant, cudaStream_t s);
+template <> cudaError_t launch_scan<OpSumU32>(const ScanParams&, bool, bool, int, cudaStream_t);
+template <> cudaError_t launch_scan<OpSumF32>(const ScanParams&, bool, bool, int, cudaStream_t);
+template <> cudaError_t launch_scan<OpMaxI32>(const ScanParams&, bool, bool, int, cudaStream_t);
+template <> cudaError_t launch_scan<OpAffineU32>(const ScanParams&, bool, bool, int, cudaStream_t);
+
+template <class T>
+cudaError_t launch_compact(const CompactParams& p, bool wide_count, cudaStream_t s);
+
+// Hierarchical (scan-then-propagate) comparison variant.
+constexpr int kHierNT = 256;
+int hier_tile_elems(int op_id);
+template <class Op>
+cudaError_t launch_hier_tiles(const HierParams& p, bool exclusive, unsigned ntiles, cudaStream_t s);
+template <class Op>
+cudaError_t launch_hier_add(const HierParams& p, unsigned ntiles, cudaStream_t s);
+
+}  // namespace scg

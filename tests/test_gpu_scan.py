@@ -1,0 +1,154 @@
+"""GPU parity: single-pass scans against the CPU oracle, element by element.
+
+Integer sums, int32 max and affine composition must match bit for bit; float32
+sums must satisfy |y_gpu[i] - y_ref[i]| <= 1e-5 * sum_{k<=i} |x[k]| (fp64
+oracle).  Sizes span one element to many tiles with ragged tails; pointers are
+16-byte aligned (vector path) and merely element-aligned (scalar path); scans
+also run in place.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from gpu_helpers import check_f32, ensure_lib, gpu_scan
+from stream_compaction_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+T = 4096  # default tile of the 4-byte operators (affine: 2048)
+SIZES = [1, 2, 3, 31, 32, 33, 1000, T - 1, T, T + 1, 2 * T - 1, 2 * T + 1, 7 * T + 13, 33 * T + 5,
+         (1 << 20) + 17, 100 * T + 4095]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_lib()
+
+
+def _input(kind, n, seed):
+    rng = np.random.default_rng(seed)
+    if kind == "i32":
+        return rng.integers(-1000, 1000, n).astype(np.int32)
+    if kind == "u32":
+        return rng.integers(0, 1 << 32, n, dtype=np.uint64).astype(np.uint32)
+    if kind == "maxi32":
+        return rng.integers(-(1 << 31), (1 << 31) - 1, n, endpoint=True).astype(np.int32)
+    if kind == "f32":
+        return rng.uniform(-1, 1, n).astype(np.float32)
+    if kind == "affine":
+        return rng.integers(0, 1 << 32, (n, 2), dtype=np.uint64).astype(np.uint32)
+    raise ValueError(kind)
+
+
+CASES = [("i32", "sum"), ("u32", "sum"), ("maxi32", "max"), ("affine", "affine"), ("f32", "sum")]
+
+
+@pytest.mark.parametrize("kind,op", CASES)
+@pytest.mark.parametrize("exclusive", [False, True])
+@pytest.mark.parametrize("n", SIZES)
+def test_scan_sizes(kind, op, exclusive, n):
+    x = _input(kind, n, seed=n * 7 + len(kind))
+    y = gpu_scan(x, op, exclusive)
+    ref = oracle.scan(x, op, exclusive)
+    if kind == "f32":
+        check_f32(y, ref, oracle.abs_prefix(x), "n=%d" % n)
+    else:
+        assert np.array_equal(y, ref)
+
+
+@pytest.mark.parametrize("kind,op", CASES)
+@pytest.mark.parametrize("exclusive", [False, True])
+@pytest.mark.parametrize("n", [T + 3, 5 * T, 9 * T + 1])
+def test_scan_unaligned_and_inplace(kind, op, exclusive, n):
+    x = _input(kind, n, seed=99 + n)
+    ref = oracle.scan(x, op, exclusive)
+    off = 2 if kind == "affine" else 1  # element-aligned, not 16-byte aligned
+    for y in (gpu_scan(x, op, exclusive, offset=off), gpu_scan(x, op, exclusive, inplace=True),
+              gpu_scan(x, op, exclusive, offset=off, inplace=True)):
+        if kind == "f32":
+            check_f32(y, ref, oracle.abs_prefix(x))
+        else:
+            assert np.array_equal(y, ref)
+
+
+def test_closed_forms_on_gpu():
+    n = 3 * T + 11
+    ones = np.ones(n, dtype=np.uint32)
+    assert np.array_equal(gpu_scan(ones, "sum", True), np.arange(n, dtype=np.uint32))
+    allf = np.full(n, 0xFFFFFFFF, dtype=np.uint32)
+    assert np.array_equal(gpu_scan(allf, "sum", False),
+                          (-(np.arange(n, dtype=np.int64) + 1)).astype(np.int32).view(np.uint32))
+    # float32 all ones: exact integers below 2^24
+    fo = np.ones(n, dtype=np.float32)
+    assert np.array_equal(gpu_scan(fo, "sum", True), np.arange(n, dtype=np.float32))
+    # identities in front of exclusive scans
+    assert gpu_scan(np.array([5, 6], np.int32), "max", True)[0] == np.iinfo(np.int32).min
+    ya = gpu_scan(np.array([[3, 4], [5, 6]], np.uint32), "affine", True)
+    assert ya[0].tolist() == [1, 0]
+
+
+@pytest.mark.parametrize("variant", range(5))
+def test_uint32_variants(variant):
+    import stream_compaction_gb300 as sc
+    assert sc.sc_set_scan_variant(variant) == sc.SC_OK
+    try:
+        for n in (1, 4097, 8191, 8192, 8193, 77 * 4096 + 1234):
+            x = _input("u32", n, seed=variant * 1000 + n)
+            for ex in (False, True):
+                assert np.array_equal(gpu_scan(x, "sum", ex), oracle.scan(x, "sum", ex)), (variant, n, ex)
+                assert np.array_equal(gpu_scan(x, "sum", ex, offset=1), oracle.scan(x, "sum", ex))
+    finally:
+        sc.sc_set_scan_variant(0)
+
+
+def test_repeated_runs_are_exact():
+    """A passing run proves little for a racy protocol: repeat with many grid sizes."""
+    import stream_compaction_gb300 as sc
+    rng = np.random.default_rng(5)
+    for it in range(60):
+        sc.sc_set_scan_variant(it % 5)
+        n = int(rng.integers(1, 3 << 20))
+        x = _input("u32", n, seed=it)
+        assert np.array_equal(gpu_scan(x, "sum", it % 2 == 0), oracle.scan(x, "sum", it % 2 == 0)), (it, n)
+    sc.sc_set_scan_variant(0)
+
+
+# ------------------------------------------------------- benchmark workloads
+def _workload(name):
+    import torch
+    spec = synth.WORKLOADS[name]
+    xt = synth.make_torch(spec, device="cuda")
+    torch.cuda.synchronize()
+    x = xt.cpu().numpy()
+    return x
+
+
+def test_workload_int32_sum_n1048593():
+    x = _workload("int32_sum_n1048593")
+    for ex in (False, True):
+        assert np.array_equal(gpu_scan(x, "sum", ex), oracle.scan(x, "sum", ex))
+
+
+def test_workload_float32_exsum_n2p26():
+    x = _workload("float32_exsum_n2^26")
+    y = gpu_scan(x, "sum", True)
+    worst = check_f32(y, oracle.scan(x, "sum", True), oracle.abs_prefix(x), "float32 n=2^26")
+    assert worst < 1e-5
+
+
+def test_workload_int32_max_n2p27():
+    x = _workload("int32_max_n2^27").view(np.int32)
+    assert np.array_equal(gpu_scan(x, "max", False), oracle.scan(x, "max", False))
+
+
+def test_workload_affine_n2p26():
+    x = _workload("affine_u32_n2^26").view(np.uint32)
+    assert np.array_equal(gpu_scan(x, "affine", False), oracle.scan(x, "affine", False))
+
+
+def test_workload_uint32_exsum_n2p30():
+    """The headline workload at full size: every one of the 2^30 outputs is compared."""
+    x = _workload("uint32_exsum_n2^30").view(np.uint32)
+    y = gpu_scan(x, "sum", True)
+    ref = oracle.scan(x, "sum", True)
+    assert np.array_equal(y, ref)
