@@ -273,6 +273,20 @@ def suite_lines(args, dev, sc, synth):
     del flush
 
 
+def combine_ranks(ms_local: float, units_local: int, world: int, device):
+    """Max of the timed region over ranks, and whole-job throughput (Gelem/s):
+    every rank processed units_local elements in at most that time."""
+    ms = ms_local
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        tt = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+        dist.barrier()
+    return ms, world * units_local / (ms * 1e-3) / 1e9
+
+
 def run_ours(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -329,13 +343,8 @@ def run_ours(args, rank, world, local_rank):
     ms = e0.elapsed_time(e1)
     if sc.sc_get_device_error(sp) != sc.SC_OK:
         raise RuntimeError("device error during the timed region")
-    if world > 1:
-        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
-        torch.distributed.barrier()
+    ms, value = combine_ranks(ms, n * args.steps, world, dev)
     ms_step = ms / args.steps
-    value = world * n / (ms_step * 1e-3) / 1e9       # Gelem/s over all ranks
     if rank != 0:
         return
 
