@@ -142,6 +142,38 @@ size_t sc_hier_workspace_bytes(sc_dtype dtype, int64_t n);
 sc_status sc_scan_host(sc_dtype dtype, sc_op op, int exclusive, const void *h_in, void *h_out, int64_t n,
                        sc_stream_t stream);
 
+/* ---- scan without any allocation ----
+ *
+ * sc_scan_noalloc computes exactly what sc_scan_inclusive (exclusive == 0) or
+ * sc_scan_exclusive (exclusive != 0) compute, with the same dtypes, operators
+ * and aliasing rules, but it never allocates device memory.  The pages have no
+ * counterpart to this entry point; it exists for callers that cannot call
+ * cudaMalloc: code running where the device allocator is unavailable or must
+ * not be touched (inside another framework's memory pool, in an allocator's
+ * own bookkeeping, or in latency-critical paths that cannot risk the implicit
+ * synchronisation cudaMalloc/cudaFree may cause).  The caller passes the
+ * input and output buffers as usual.
+ *
+ * The look-back workspace it needs lives in a fixed array inside the
+ * library's device image: about 1 MiB (256 bytes + 16 bytes per 2048
+ * elements of SC_NOALLOC_MAX_N), held on every GPU that loads the library
+ * until the process exits.
+ *   - n > SC_NOALLOC_MAX_N is rejected with SC_ERR_WORKSPACE before any launch.
+ *   - The first call on a device looks up the array's device address on that
+ *     device; make that first call before any stream capture begins.
+ *   - All calls on a device share the one array: calls whose work can overlap
+ *     on the GPU (other streams, other host threads) race and corrupt each
+ *     other.  Order them on one stream, or serialise them.
+ *   - Each call clears the counter and error word it uses with a 16-byte
+ *     cudaMemsetAsync on `stream`, then launches one scan kernel.
+ *   - There is no error query for this path: look-back waits stay bounded,
+ *     and a wait that gives up (only if a CTA is starved for seconds) leaves
+ *     that call's output incomplete without a report.  Its launches are not
+ *     counted by sc_launch_count. */
+#define SC_NOALLOC_MAX_N (1LL << 27)
+sc_status sc_scan_noalloc(sc_dtype dtype, sc_op op, int exclusive, const void *in, void *out, int64_t n,
+                          sc_stream_t stream);
+
 /* Wait for `stream`, then read and clear the device error word of its
  * workspace.  SC_OK when no kernel reported a failure since the last call. */
 sc_status sc_get_device_error(sc_stream_t stream);

@@ -45,6 +45,7 @@ SIGNATURES = {
     "sc_scan_hierarchical": ([_INT, _INT, _INT, _P, _P, _I64, _P], _INT),
     "sc_hier_workspace_bytes": ([_INT, _I64], _SZ),
     "sc_scan_host": ([_INT, _INT, _INT, _P, _P, _I64, _P], _INT),
+    "sc_scan_noalloc": ([_INT, _INT, _INT, _P, _P, _I64, _P], _INT),
     "sc_get_device_error": ([_P], _INT),
     "sc_launch_count": ([], _U64),
     "sc_set_scan_variant": ([_INT], _INT),
@@ -132,6 +133,13 @@ def sc_hier_workspace_bytes(dtype: int, n: int) -> int:
 
 def sc_scan_host(dtype: int, op: int, exclusive: int, h_in: int, h_out: int, n: int, stream: int) -> int:
     return load().sc_scan_host(dtype, op, exclusive, h_in, h_out, n, stream)
+
+
+def sc_scan_noalloc(dtype: int, op: int, exclusive: int, d_in: int, d_out: int, n: int, stream: int) -> int:
+    return load().sc_scan_noalloc(dtype, op, exclusive, d_in, d_out, n, stream)
+
+
+SC_NOALLOC_MAX_N = 1 << 27
 
 
 def sc_get_device_error(stream: int) -> int:
