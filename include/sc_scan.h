@@ -183,12 +183,16 @@ uint64_t sc_launch_count(void);
 
 /* ---- tuning and test hooks (process-wide; affect later launches) ---- */
 
-/* Select one of the precompiled tile shapes of the uint32/int32 sum
- * (0 = default; see sc_scan_variant_info).  Returns SC_ERR_INVALID for an
- * unknown variant. */
+/* Select the kernel of the uint32/int32 sum.  0 (default): the persistent
+ * TMA-pipelined kernel wherever it applies (16-byte aligned arrays of at least
+ * one 16 KiB tile), else the one-tile-per-CTA kernel; v >= 1: one of the
+ * precompiled one-tile-per-CTA shapes (see sc_scan_variant_info), kept for
+ * on-GPU comparison.  Returns SC_ERR_INVALID for an unknown variant. */
 sc_status sc_set_scan_variant(int variant);
-/* Threads per CTA, items per thread and loader kind (0 direct, 1 transposed)
- * of a uint32-sum variant; SC_ERR_INVALID if it does not exist. */
+/* Threads per CTA, items per thread and loader kind (0 direct loads,
+ * 1 coalesced loads + shared-memory transpose, 2 persistent TMA pipeline;
+ * for 2, threads are the CTA's compute threads) of a uint32-sum variant;
+ * SC_ERR_INVALID if it does not exist. */
 sc_status sc_scan_variant_info(int variant, int *threads, int *items, int *loader);
 
 /* Look-back test hooks.  stall_tile >= 0: that tile never publishes its
@@ -197,6 +201,16 @@ sc_status sc_scan_variant_info(int variant, int *threads, int *items, int *loade
  * long look-back chains).  timeout_ns: bound on any single look-back wait
  * (0 restores the default of 2 s).  -1 turns a hook off. */
 sc_status sc_debug_set_lookback(int64_t stall_tile, int64_t delay_tile, uint32_t delay_ns, uint64_t timeout_ns);
+
+/* Phase timers of the instrumented uint32-sum variants (sc_scan_variant_info
+ * lists them; they are for measurement, not production).  Waits for `stream`,
+ * copies the 8 counters accumulated by that stream's launches into out8 and
+ * clears them: [0] tiles, [1] ns until tile ids were known, [2] ns loading and
+ * scanning tiles, [3] ns in the look-back, [4] look-back windows read,
+ * [5] polls that found a predecessor not yet published, [6] ns from the
+ * prefix to the end of the stores, [7] ns of whole tiles (all summed over
+ * tiles). */
+sc_status sc_debug_lookback_stats(sc_stream_t stream, uint64_t *out8);
 
 #ifdef __cplusplus
 }

@@ -51,6 +51,7 @@ SIGNATURES = {
     "sc_set_scan_variant": ([_INT], _INT),
     "sc_scan_variant_info": ([_INT, ctypes.POINTER(_INT), ctypes.POINTER(_INT), ctypes.POINTER(_INT)], _INT),
     "sc_debug_set_lookback": ([_I64, _I64, _U32, _U64], _INT),
+    "sc_debug_lookback_stats": ([_P, ctypes.POINTER(_U64)], _INT),
 }
 
 _lock = threading.Lock()
@@ -162,6 +163,12 @@ def sc_scan_variant_info(variant: int):
 
 def sc_debug_set_lookback(stall_tile: int, delay_tile: int, delay_ns: int, timeout_ns: int) -> int:
     return load().sc_debug_set_lookback(stall_tile, delay_tile, delay_ns, timeout_ns)
+
+
+def sc_debug_lookback_stats(stream: int):
+    buf = (_U64 * 8)()
+    st = load().sc_debug_lookback_stats(stream, buf)
+    return st, list(buf)
 
 
 # ------------------------------------------------------------ tensor layer

@@ -26,10 +26,14 @@ using scg::LookbackCtl;
 using scg::ScanParams;
 
 constexpr size_t kStatusOffset = 256;       // counter at 0, error word at 8
+constexpr size_t kStatsOffset = 64;         // 8 phase-timer counters of instrumented variants
 constexpr int64_t kMinTile = 2048;          // smallest tile of any kernel
 constexpr size_t kSlotBytes = 16;           // one look-back status slot
 constexpr unsigned kMaxEpoch = (1u << 30) - 1;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
+// Public variant numbers of the uint32 sum: 0 persistent TMA kernel, 1 .. N the
+// one-tile-per-CTA shapes (shape v - 1), N + 1 the instrumented TMA kernel.
+constexpr int kTmaStatsVariant = scg::kNumSumU32Variants + 1;
 
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_variant{0};
@@ -101,6 +105,7 @@ LookbackCtl make_ctl(Workspace& ws, unsigned num_tiles) {
     lb.delay_tile = g_delay_tile.load();
     lb.delay_ns = g_delay_ns.load();
     lb.timeout_ns = g_timeout_ns.load();
+    lb.stats = reinterpret_cast<unsigned long long*>(ws.base + kStatsOffset);
     return lb;
 }
 
@@ -170,11 +175,45 @@ cudaError_t dispatch_scan(int oid, const ScanParams& p, bool excl, bool seg, int
     }
 }
 
+int num_sms() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int v = cache[dev].load();
+    if (v == 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev].store(v);
+    }
+    return v;
+}
+
+cudaError_t dispatch_scan_tma(int oid, const ScanParams& p, bool excl, unsigned grid, cudaStream_t s, bool stats) {
+    switch (oid) {
+    case 0: return scg::launch_scan_tma<scg::OpSumU32>(p, excl, grid, s, stats);
+    case 1: return scg::launch_scan_tma<scg::OpSumF32>(p, excl, grid, s, false);
+    case 2: return scg::launch_scan_tma<scg::OpMaxI32>(p, excl, grid, s, false);
+    case 3: return scg::launch_scan_tma<scg::OpAffineU32>(p, excl, grid, s, false);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
 // One single-pass scan launch (plain or segmented), with optional carries.
+// Public variant 0 is the persistent TMA kernel where it applies (16-byte
+// aligned, unsegmented, at least one full tile); every other case, and public
+// variants v >= 1 of the uint32 sum, use the one-tile-per-CTA kernel (shape
+// v - 1; shape 0 by default).
 sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_len, bool excl,
                    const void* carry_in, void* carry_out, cudaStream_t s) {
-    const int variant = (oid == 0 && seg_len == 0) ? g_variant.load() : 0;
-    const int tile = scg::scan_tile_elems(oid, variant);
+    const int api_variant = (oid == 0 && seg_len == 0) ? g_variant.load() : 0;
+    const bool vec_ok = aligned(in, 16) && aligned(out, 16);
+    const int eb = oid == 3 ? 8 : 4;
+    const int64_t tma_tile = scg::tma_tile_elems(eb);
+    const bool tma_stats = api_variant == kTmaStatsVariant;
+    const bool use_tma = (api_variant == 0 || tma_stats) && seg_len == 0 && vec_ok && n >= tma_tile &&
+                         n / tma_tile * 128 < (int64_t)INT_MAX && num_sms() > 0;
+    const int legacy_variant = (api_variant == 0 || tma_stats) ? 0 : api_variant - 1;
+    // units of the look-back: chunks of the persistent kernel, tiles otherwise
+    const int64_t tile = use_tma ? tma_tile * scg::tma_chunk_tiles() : scg::scan_tile_elems(oid, legacy_variant);
     const unsigned ntiles = (unsigned)ceil_div(n, tile);
     std::lock_guard<std::mutex> lk(g_ws_mu);
     Workspace* ws = nullptr;
@@ -185,11 +224,16 @@ sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_le
     p.out = out;
     p.n = n;
     p.seg_len = seg_len;
-    p.vec_ok = aligned(in, 16) && aligned(out, 16);
+    p.vec_ok = vec_ok;
     p.carry_in = carry_in;
     p.carry_out = carry_out;
     p.lb = make_ctl(*ws, ntiles);
-    return finish_launch(*ws, ntiles, dispatch_scan(oid, p, excl, seg_len > 0, variant, s));
+    if (use_tma) {
+        const unsigned grid = (unsigned)std::min<int64_t>(num_sms(), ntiles);
+        const cudaError_t e = dispatch_scan_tma(oid, p, excl, grid, s, tma_stats);
+        return finish_launch(*ws, ntiles + grid * (unsigned)scg::tma_ids_per_cta(), e);
+    }
+    return finish_launch(*ws, ntiles, dispatch_scan(oid, p, excl, seg_len > 0, legacy_variant, s));
 }
 
 // ------------------------------------------------------ compaction predicate
@@ -558,6 +602,11 @@ sc_status sc_get_device_error(sc_stream_t stream) {
     if (cudaMemcpy(&h, err, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return SC_ERR_CUDA;
     if (h != 0) {
         if (cudaMemset(err, 0, sizeof(h)) != cudaSuccess) return SC_ERR_CUDA;
+        // a kernel that gave up may not have consumed its tile ids: start the
+        // next call from a cleared workspace
+        std::lock_guard<std::mutex> lk(g_ws_mu);
+        auto it = g_ws.find({dev, s});
+        if (it != g_ws.end()) it->second.dirty = true;
         return (sc_status)h;
     }
     return SC_OK;
@@ -565,15 +614,42 @@ sc_status sc_get_device_error(sc_stream_t stream) {
 
 uint64_t sc_launch_count(void) { return g_launches.load(); }
 
+sc_status sc_debug_lookback_stats(sc_stream_t stream, uint64_t* out8) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!out8) return SC_ERR_INVALID;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SC_ERR_CUDA;
+    unsigned char* base = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_ws_mu);
+        auto it = g_ws.find({dev, s});
+        if (it != g_ws.end()) base = it->second.base;
+    }
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SC_ERR_CUDA;
+    if (!base) {
+        for (int i = 0; i < 8; ++i) out8[i] = 0;
+        return SC_OK;
+    }
+    if (cudaMemcpy(out8, base + kStatsOffset, 64, cudaMemcpyDeviceToHost) != cudaSuccess) return SC_ERR_CUDA;
+    if (cudaMemset(base + kStatsOffset, 0, 64) != cudaSuccess) return SC_ERR_CUDA;
+    return SC_OK;
+}
+
 sc_status sc_set_scan_variant(int variant) {
-    if (variant < 0 || variant >= scg::kNumSumU32Variants) return SC_ERR_INVALID;
+    if (variant < 0 || variant > kTmaStatsVariant) return SC_ERR_INVALID;
     g_variant.store(variant);
     return SC_OK;
 }
 
 sc_status sc_scan_variant_info(int variant, int* threads, int* items, int* loader) {
-    if (variant < 0 || variant >= scg::kNumSumU32Variants) return SC_ERR_INVALID;
-    const scg::ScanShape sh = scg::kShapeSumU32[variant];
+    if (variant < 0 || variant > kTmaStatsVariant) return SC_ERR_INVALID;
+    if (variant == 0 || variant == kTmaStatsVariant) {  // persistent TMA kernel: compute threads, items per compute thread
+        if (threads) *threads = 256;
+        if (items) *items = scg::tma_tile_elems(4) / 256;
+        if (loader) *loader = 2;
+        return SC_OK;
+    }
+    const scg::ScanShape sh = scg::kShapeSumU32[variant - 1];
     if (threads) *threads = sh.nt;
     if (items) *items = sh.ipt;
     if (loader) *loader = sh.load;

@@ -209,29 +209,54 @@ struct StatusIO {
 // Record a device-side failure (first error wins).
 __device__ __forceinline__ void raise_error(unsigned int* err, unsigned code) { atomicCAS(err, 0u, code); }
 
-// Warp-collective decoupled look-back for tile `tile` (> 0).  Lane l reads the
-// status of predecessor (end - 32 + l); the window slides 32 tiles back at a
-// time until it holds a tile with an inclusive prefix (P).  Within a window the
-// newest P and every aggregate (A) after it are folded in tile order, older
-// operand on the left, so non-commutative operators are safe.  Every wait is
-// bounded: past lb.timeout_ns (or a poll cap) the warp gives up.  Returns
-// false on timeout or when a predecessor is poisoned.
-template <class Op>
-__device__ bool lookback_prefix(const LookbackCtl& lb, long long tile, typename Op::C& prefix) {
+// Warp-collective decoupled look-back for tile `tile` (> 0).  A window covers
+// the 32*kPer predecessors [end - 32*kPer, end): lane l reads the kPer
+// consecutive tiles starting at end - 32*kPer + l*kPer, all loads issued
+// back to back, so one round trip to L2 inspects 32*kPer tiles.  The window
+// slides back until it holds a tile with an inclusive prefix (P).  Only the
+// tiles after the newest P in the window need to be published (A or P);
+// older ones are never waited for.  The newest P and every aggregate (A)
+// after it are folded in tile order, older operand on the left, so
+// non-commutative operators are safe.  Every wait is bounded:
+// past lb.timeout_ns (or a poll cap) the warp gives up.  Returns false on
+// timeout or when a predecessor is poisoned.
+template <class Op, int kPer = 1>
+__device__ bool lookback_prefix(const LookbackCtl& lb, long long tile, typename Op::C& prefix,
+                                unsigned* windows_out = nullptr, unsigned* polls_out = nullptr) {
     using C = typename Op::C;
+    constexpr int W = 32 * kPer;
     const int lane = threadIdx.x & 31;
     C acc = Op::c_identity();
     long long end = tile;
     unsigned long long t_start = 0;
     unsigned polls = 0;
-    unsigned sleep_ns = 20;
+    unsigned sleep_ns = 16;
     while (true) {
-        const long long pred = end - 32 + lane;
-        C val = Op::c_identity();
-        unsigned flag = ST_PREFIX;  // tiles before 0 act as an identity prefix
-        if (pred >= 0) flag = StatusIO<C>::read(lb, pred, val);
-        if (__any_sync(0xffffffffu, flag == ST_POISON)) return false;
-        if (__any_sync(0xffffffffu, flag == ST_INVALID)) {
+        const long long first = end - W + (long long)lane * kPer;
+        C val[kPer];
+        unsigned flag[kPer];
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            val[j] = Op::c_identity();
+            flag[j] = ST_PREFIX;  // tiles before 0 act as an identity prefix
+            if (first + j >= 0) flag[j] = StatusIO<C>::read(lb, first + j, val[j]);
+        }
+        int newest_p = -1;  // index j of the newest P in this lane
+#pragma unroll
+        for (int j = 0; j < kPer; ++j)
+            if (flag[j] == ST_PREFIX) newest_p = j;
+        const uint32_t pm = __ballot_sync(0xffffffffu, newest_p >= 0);
+        const int hp = pm ? 31 - __clz(pm) : -1;  // newest lane holding a P
+        // only the tiles after the newest P matter: they must all be published
+        bool poison = false, invalid = false;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const bool after = lane > hp || (lane == hp && j > newest_p);
+            poison |= after && flag[j] == ST_POISON;
+            invalid |= after && flag[j] == ST_INVALID;
+        }
+        if (__any_sync(0xffffffffu, poison)) return false;
+        if (__any_sync(0xffffffffu, invalid)) {
             if (t_start == 0) t_start = global_ns();
             ++polls;
             if (polls > (1u << 26) || global_ns() - t_start > lb.timeout_ns) {
@@ -239,21 +264,102 @@ __device__ bool lookback_prefix(const LookbackCtl& lb, long long tile, typename 
                 return false;
             }
             __nanosleep(sleep_ns);
-            sleep_ns = min(sleep_ns * 2u, 512u);
+            sleep_ns = min(sleep_ns * 2u, 256u);
             continue;
         }
-        const uint32_t pm = __ballot_sync(0xffffffffu, flag == ST_PREFIX);
-        const int newest_p = pm ? 31 - __clz(pm) : -1;
-        C x = lane < newest_p ? Op::c_identity() : val;
+        C x = Op::c_identity();
+        if (lane >= hp) {
+            const int j0 = lane == hp ? newest_p : 0;
+#pragma unroll
+            for (int j = 0; j < kPer; ++j)
+                if (j >= j0) x = Op::c_op(x, val[j]);
+        }
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
             const C y = shfl_down_v(x, d);
             if (lane + d < 32) x = Op::c_op(x, y);
         }
         acc = Op::c_op(shfl_idx_v(x, 0), acc);
+        if (windows_out) ++*windows_out;
         if (pm) break;
-        end -= 32;
+        end -= W;
     }
+    if (polls_out) *polls_out = polls;
+    prefix = acc;
+    return true;
+}
+
+// Look-back with an adaptive window for callers that run many look-backs at
+// once: the first window is 32 tiles (one status word per lane) and each
+// window that holds no inclusive prefix doubles the next one, up to
+// 32 * kMaxPer tiles.  Waits back off from 64 ns to 256 ns between polls.
+// Same contract as lookback_prefix.
+template <class Op, int kMaxPer>
+__device__ bool lookback_prefix_adaptive(const LookbackCtl& lb, long long tile, typename Op::C& prefix,
+                                         unsigned* windows_out = nullptr, unsigned* polls_out = nullptr) {
+    using C = typename Op::C;
+    const int lane = threadIdx.x & 31;
+    C acc = Op::c_identity();
+    long long end = tile;
+    int per = 1;
+    unsigned long long t_start = 0;
+    unsigned polls = 0;
+    unsigned sleep_ns = 64;
+    while (true) {
+        const long long first = end - 32LL * per + (long long)lane * per;
+        C val[kMaxPer];
+        unsigned flag[kMaxPer];
+#pragma unroll
+        for (int j = 0; j < kMaxPer; ++j) {
+            val[j] = Op::c_identity();
+            flag[j] = ST_PREFIX;  // tiles before 0 act as an identity prefix
+            if (j < per && first + j >= 0) flag[j] = StatusIO<C>::read(lb, first + j, val[j]);
+        }
+        int newest_p = -1;
+#pragma unroll
+        for (int j = 0; j < kMaxPer; ++j)
+            if (j < per && flag[j] == ST_PREFIX) newest_p = j;
+        const uint32_t pm = __ballot_sync(0xffffffffu, newest_p >= 0);
+        const int hp = pm ? 31 - __clz(pm) : -1;
+        // only the tiles after the newest P matter: they must all be published
+        bool poison = false, invalid = false;
+#pragma unroll
+        for (int j = 0; j < kMaxPer; ++j) {
+            const bool after = j < per && (lane > hp || (lane == hp && j > newest_p));
+            poison |= after && flag[j] == ST_POISON;
+            invalid |= after && flag[j] == ST_INVALID;
+        }
+        if (__any_sync(0xffffffffu, poison)) return false;
+        if (__any_sync(0xffffffffu, invalid)) {
+            if (t_start == 0) t_start = global_ns();
+            ++polls;
+            if (polls > (1u << 26) || global_ns() - t_start > lb.timeout_ns) {
+                if (lane == 0) raise_error(lb.error, DEV_LOOKBACK_TIMEOUT);
+                return false;
+            }
+            __nanosleep(sleep_ns);
+            sleep_ns = min(sleep_ns * 2u, 256u);
+            continue;
+        }
+        C x = Op::c_identity();
+        if (lane >= hp) {
+            const int j0 = lane == hp ? newest_p : 0;
+#pragma unroll
+            for (int j = 0; j < kMaxPer; ++j)
+                if (j < per && j >= j0) x = Op::c_op(x, val[j]);
+        }
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const C y = shfl_down_v(x, d);
+            if (lane + d < 32) x = Op::c_op(x, y);
+        }
+        acc = Op::c_op(shfl_idx_v(x, 0), acc);
+        if (windows_out) ++*windows_out;
+        if (pm) break;
+        end -= 32LL * per;
+        per = min(per * 2, kMaxPer);
+    }
+    if (polls_out) *polls_out = polls;
     prefix = acc;
     return true;
 }

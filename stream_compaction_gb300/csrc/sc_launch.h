@@ -24,12 +24,15 @@ struct CompactConfig {
 // hook) so that tile size, block size and loader can be compared on the GPU
 // without a rebuild.
 struct ScanShape {
-    int nt;    // threads per CTA
-    int ipt;   // items per thread
-    int load;  // LOAD_DIRECT / LOAD_XPOSE
+    int nt;     // threads per CTA
+    int ipt;    // items per thread
+    int load;   // LOAD_DIRECT / LOAD_XPOSE
+    int lb;     // look-back status words read per lane per round trip
+    int minb;   // minimum resident CTAs per SM requested from the compiler
+    int stats;  // 1: instrumented (phase timers), for measurement only
 };
 
-constexpr int kNumSumU32Variants = 5;
+constexpr int kNumSumU32Variants = 15;
 
 // Tile size (elements) of operator `op_id` (0 sum u32, 1 sum f32, 2 max i32,
 // 3 affine) in the given variant; 0 if that variant does not exist.
@@ -42,6 +45,18 @@ template <> cudaError_t launch_scan<OpSumU32>(const ScanParams&, bool, bool, int
 template <> cudaError_t launch_scan<OpSumF32>(const ScanParams&, bool, bool, int, cudaStream_t);
 template <> cudaError_t launch_scan<OpMaxI32>(const ScanParams&, bool, bool, int, cudaStream_t);
 template <> cudaError_t launch_scan<OpAffineU32>(const ScanParams&, bool, bool, int, cudaStream_t);
+
+// Persistent TMA-pipelined scan (16-byte aligned arrays of at least one full
+// 16 KiB tile, no segments).  Its look-back runs over chunks of
+// tma_chunk_tiles() tiles: p.lb.num_tiles holds the number of chunks, and the
+// counter advances by num_chunks + grid * tma_ids_per_cta() per launch.
+// stats: instrumented build (uint32 sum only).
+int tma_tile_elems(int elem_bytes);
+int tma_chunk_tiles();
+int tma_ids_per_cta();
+int tma_threads();
+template <class Op>
+cudaError_t launch_scan_tma(const ScanParams& p, bool exclusive, unsigned grid, cudaStream_t s, bool stats);
 
 template <class T>
 cudaError_t launch_compact(const CompactParams& p, bool wide_count, cudaStream_t s);

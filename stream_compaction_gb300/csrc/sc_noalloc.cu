@@ -126,6 +126,7 @@ extern "C" sc_status sc_scan_noalloc(sc_dtype dtype, sc_op op, int exclusive, co
     p.lb.delay_tile = -1;
     p.lb.delay_ns = 0;
     p.lb.timeout_ns = 2000000000ull;
+    p.lb.stats = nullptr;
     cudaError_t e;
     switch (oid) {
     case 0: e = scg::launch_scan<scg::OpSumU32>(p, exclusive != 0, false, 0, s); break;

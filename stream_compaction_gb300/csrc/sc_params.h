@@ -22,6 +22,7 @@ struct LookbackCtl {
     long long delay_tile;           // test hook: tile that sleeps before publishing (-1: off)
     unsigned int delay_ns;
     unsigned long long timeout_ns;  // bound on any single look-back wait
+    unsigned long long* stats;      // instrumented variants only: 8 counters (see sc_scan.cuh)
 };
 
 struct ScanParams {

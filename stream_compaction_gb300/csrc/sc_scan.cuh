@@ -35,8 +35,13 @@ __device__ __forceinline__ void hook_delay(unsigned ns) {
     for (int i = 0; i < (1 << 20) && global_ns() - t0 < ns; ++i) __nanosleep(1000);
 }
 
-template <class Op, int NT, int IPT, bool kExcl, bool kSeg, int kLoad>
-__global__ void __launch_bounds__(NT) scan_kernel(const ScanParams p) {
+// Instrumented variants (kStats) add, per tile, the time spent in each phase
+// to 8 counters: [0] tiles, [1] ns until the tile id is known, [2] ns loading
+// and scanning the tile, [3] ns in the look-back, [4] look-back windows read,
+// [5] polls that found a predecessor not yet published, [6] ns from the
+// prefix to the end of the stores, [7] ns of the whole tile.
+template <class Op, int NT, int IPT, bool kExcl, bool kSeg, int kLoad, int kLb = 1, int kMinB = 1, bool kStats = false>
+__global__ void __launch_bounds__(NT, kMinB) scan_kernel(const ScanParams p) {
     using T = typename Op::T;
     using C = typename Op::C;
     constexpr int NW = NT / 32;
@@ -52,11 +57,15 @@ __global__ void __launch_bounds__(NT) scan_kernel(const ScanParams p) {
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    unsigned long long t0 = 0, t1 = 0, t2 = 0, t3 = 0, t4 = 0;
+    unsigned windows = 0, polls = 0;
+    if (kStats && tid == 0) t0 = global_ns();
     if (tid == 0) {
         s_tile = (unsigned)(atomicAdd(p.lb.counter, 1ull) - p.lb.counter_base);
         s_abort = 0;
     }
     __syncthreads();
+    if (kStats && tid == 0) t1 = global_ns();
     const long long tile = s_tile;
     const long long tile_start = tile * TILE;
     const long long valid = min((long long)TILE, p.n - tile_start);
@@ -99,6 +108,7 @@ __global__ void __launch_bounds__(NT) scan_kernel(const ScanParams p) {
         s_whead[warp] = kSeg ? (wmask != 0u) : 0;
     }
     __syncthreads();
+    if (kStats && tid == 0) t2 = global_ns();
 
     // block combine: carry from the warps before this one
     T wcarry = Op::identity();
@@ -132,7 +142,8 @@ __global__ void __launch_bounds__(NT) scan_kernel(const ScanParams p) {
             } else {
                 const bool complete = kSeg && thead;  // aggregate already starts at a head
                 if (lane == 0) StatusIO<C>::publish(p.lb, tile, complete ? ST_PREFIX : ST_AGGREGATE, agg);
-                ok = lookback_prefix<Op>(p.lb, tile, prefix);
+                ok = lookback_prefix<Op, kLb>(p.lb, tile, prefix, kStats ? &windows : nullptr,
+                                              kStats ? &polls : nullptr);
                 if (ok && !complete && lane == 0) StatusIO<C>::publish(p.lb, tile, ST_PREFIX, Op::c_op(prefix, agg));
                 if (!ok && lane == 0) StatusIO<C>::publish(p.lb, tile, ST_POISON, agg);
             }
@@ -145,6 +156,7 @@ __global__ void __launch_bounds__(NT) scan_kernel(const ScanParams p) {
         }
     }
     __syncthreads();
+    if (kStats && tid == 0) t3 = global_ns();
     if (s_abort) return;
 
     // carry into the thread's first item: tile prefix (+) warp carry (+) lane carry,
@@ -170,6 +182,21 @@ __global__ void __launch_bounds__(NT) scan_kernel(const ScanParams p) {
 
     if (full) store_full_tile<T, IPT, kLoad>(tout, v, wbuf);
     else store_partial_tile<T, IPT>(tout, v, valid);
+    if constexpr (kStats) {
+        __syncthreads();
+        if (tid == 0) {
+            t4 = global_ns();
+            unsigned long long* st = p.lb.stats;
+            atomicAdd(st + 0, 1ull);
+            atomicAdd(st + 1, t1 - t0);
+            atomicAdd(st + 2, t2 - t1);
+            atomicAdd(st + 3, t3 - t2);
+            atomicAdd(st + 4, (unsigned long long)windows);
+            atomicAdd(st + 5, (unsigned long long)polls);
+            atomicAdd(st + 6, t4 - t3);
+            atomicAdd(st + 7, t4 - t0);
+        }
+    }
 }
 
 }  // namespace scg

@@ -3,7 +3,7 @@
 
 namespace scg {
 
-#define SHAPE(i) kShapeSumU32[i].nt, kShapeSumU32[i].ipt, kShapeSumU32[i].load
+#define SHAPE(i) SC_SHAPE_ARGS(kShapeSumU32[i])
 
 template <>
 cudaError_t launch_scan<OpSumU32>(const ScanParams& p, bool exclusive, bool segmented, int variant, cudaStream_t s) {
@@ -17,6 +17,16 @@ cudaError_t launch_scan<OpSumU32>(const ScanParams& p, bool exclusive, bool segm
     case 2: return launch_shape_plain<OpSumU32, SHAPE(2)>(p, exclusive, s);
     case 3: return launch_shape_plain<OpSumU32, SHAPE(3)>(p, exclusive, s);
     case 4: return launch_shape_plain<OpSumU32, SHAPE(4)>(p, exclusive, s);
+    case 5: return launch_shape_plain<OpSumU32, SHAPE(5)>(p, exclusive, s);
+    case 6: return launch_shape_plain<OpSumU32, SHAPE(6)>(p, exclusive, s);
+    case 7: return launch_shape_plain<OpSumU32, SHAPE(7)>(p, exclusive, s);
+    case 8: return launch_shape_plain<OpSumU32, SHAPE(8)>(p, exclusive, s);
+    case 9: return launch_shape_plain<OpSumU32, SHAPE(9)>(p, exclusive, s);
+    case 10: return launch_shape_plain<OpSumU32, SHAPE(10)>(p, exclusive, s);
+    case 11: return launch_shape_plain<OpSumU32, SHAPE(11)>(p, exclusive, s);
+    case 12: return launch_shape_plain<OpSumU32, SHAPE(12)>(p, exclusive, s);
+    case 13: return launch_shape_plain<OpSumU32, SHAPE(13)>(p, exclusive, s);
+    case 14: return launch_shape_plain<OpSumU32, SHAPE(14)>(p, exclusive, s);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 
 T = 4096  # default tile of the 4-byte operators (affine: 2048)
 SIZES = [1, 2, 3, 31, 32, 33, 1000, T - 1, T, T + 1, 2 * T - 1, 2 * T + 1, 7 * T + 13, 33 * T + 5,
-         (1 << 20) + 17, 100 * T + 4095]
+         (1 << 20) + 17, 100 * T + 4095, 1000 * T + 17, 3000 * T - 1]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -87,7 +87,7 @@ def test_closed_forms_on_gpu():
     assert ya[0].tolist() == [1, 0]
 
 
-@pytest.mark.parametrize("variant", range(5))
+@pytest.mark.parametrize("variant", range(16))
 def test_uint32_variants(variant):
     import stream_compaction_gb300 as sc
     assert sc.sc_set_scan_variant(variant) == sc.SC_OK
@@ -106,7 +106,7 @@ def test_repeated_runs_are_exact():
     import stream_compaction_gb300 as sc
     rng = np.random.default_rng(5)
     for it in range(60):
-        sc.sc_set_scan_variant(it % 5)
+        sc.sc_set_scan_variant(it % 16)
         n = int(rng.integers(1, 3 << 20))
         x = _input("u32", n, seed=it)
         assert np.array_equal(gpu_scan(x, "sum", it % 2 == 0), oracle.scan(x, "sum", it % 2 == 0)), (it, n)
