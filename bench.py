@@ -405,7 +405,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": WORKLOAD, "n": n, "op": "sum", "exclusive": True,
                    "l2": "inputs larger than L2 (4 GiB in + 4 GiB out per step), no flush",
                    "parallelism": "replicas" if world > 1 else "single-gpu",
-                   "tile": {"threads": nt, "items_per_thread": ipt, "loader": ["direct", "transpose"][ld]}},
+                   "tile": {"threads": nt, "items_per_thread": ipt, "loader": ["direct", "transpose", "persistent-tma"][ld]}},
         "hbm_gbs": achieved,
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "Gelem/s", "h2d_bytes_per_step": 4 * n, "d2h_bytes_per_step": 4 * n,

@@ -31,9 +31,17 @@ constexpr int64_t kMinTile = 2048;          // smallest tile of any kernel
 constexpr size_t kSlotBytes = 16;           // one look-back status slot
 constexpr unsigned kMaxEpoch = (1u << 30) - 1;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
-// Public variant numbers of the uint32 sum: 0 persistent TMA kernel, 1 .. N the
-// one-tile-per-CTA shapes (shape v - 1), N + 1 the instrumented TMA kernel.
+// Public variant numbers of the uint32 sum: 0 persistent TMA kernel (shape 0),
+// 1 .. N the one-tile-per-CTA shapes (shape v - 1), N + 1 the instrumented TMA
+// kernel, N + 1 + c (c >= 1) the persistent kernel in shape c.
 constexpr int kTmaStatsVariant = scg::kNumSumU32Variants + 1;
+int max_variant() { return kTmaStatsVariant + scg::tma_num_cfgs() - 1; }
+// Persistent-kernel shape of a public variant, or -1 for the one-tile-per-CTA kernel.
+int tma_cfg_of(int v) {
+    if (v == 0 || v == kTmaStatsVariant) return 0;
+    if (v > kTmaStatsVariant && v <= max_variant()) return v - kTmaStatsVariant;
+    return -1;
+}
 
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_variant{0};
@@ -187,12 +195,13 @@ int num_sms() {
     return v;
 }
 
-cudaError_t dispatch_scan_tma(int oid, const ScanParams& p, bool excl, unsigned grid, cudaStream_t s, bool stats) {
+cudaError_t dispatch_scan_tma(int oid, const ScanParams& p, bool excl, unsigned grid, cudaStream_t s, bool stats,
+                              int cfg) {
     switch (oid) {
-    case 0: return scg::launch_scan_tma<scg::OpSumU32>(p, excl, grid, s, stats);
-    case 1: return scg::launch_scan_tma<scg::OpSumF32>(p, excl, grid, s, false);
-    case 2: return scg::launch_scan_tma<scg::OpMaxI32>(p, excl, grid, s, false);
-    case 3: return scg::launch_scan_tma<scg::OpAffineU32>(p, excl, grid, s, false);
+    case 0: return scg::launch_scan_tma<scg::OpSumU32>(p, excl, grid, s, stats, cfg);
+    case 1: return scg::launch_scan_tma<scg::OpSumF32>(p, excl, grid, s, false, 0);
+    case 2: return scg::launch_scan_tma<scg::OpMaxI32>(p, excl, grid, s, false, 0);
+    case 3: return scg::launch_scan_tma<scg::OpAffineU32>(p, excl, grid, s, false, 0);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -207,13 +216,16 @@ sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_le
     const int api_variant = (oid == 0 && seg_len == 0) ? g_variant.load() : 0;
     const bool vec_ok = aligned(in, 16) && aligned(out, 16);
     const int eb = oid == 3 ? 8 : 4;
-    const int64_t tma_tile = scg::tma_tile_elems(eb);
+    const int cfg = tma_cfg_of(api_variant);
+    scg::TmaShape sh{0, 0, 0, 0};
+    if (cfg >= 0) scg::tma_shape(cfg, &sh);
+    const int64_t tma_tile = cfg >= 0 ? sh.tile_bytes / eb : 0;
     const bool tma_stats = api_variant == kTmaStatsVariant;
-    const bool use_tma = (api_variant == 0 || tma_stats) && seg_len == 0 && vec_ok && n >= tma_tile &&
-                         n / tma_tile * 128 < (int64_t)INT_MAX && num_sms() > 0;
-    const int legacy_variant = (api_variant == 0 || tma_stats) ? 0 : api_variant - 1;
+    const bool use_tma = cfg >= 0 && seg_len == 0 && vec_ok && n >= tma_tile &&
+                         n / tma_tile * (sh.tile_bytes / 128) < (int64_t)INT_MAX && num_sms() > 0;
+    const int legacy_variant = (cfg >= 0 || api_variant == 0) ? 0 : api_variant - 1;
     // units of the look-back: chunks of the persistent kernel, tiles otherwise
-    const int64_t tile = use_tma ? tma_tile * scg::tma_chunk_tiles() : scg::scan_tile_elems(oid, legacy_variant);
+    const int64_t tile = use_tma ? tma_tile * sh.chunk_tiles : scg::scan_tile_elems(oid, legacy_variant);
     const unsigned ntiles = (unsigned)ceil_div(n, tile);
     std::lock_guard<std::mutex> lk(g_ws_mu);
     Workspace* ws = nullptr;
@@ -230,7 +242,7 @@ sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_le
     p.lb = make_ctl(*ws, ntiles);
     if (use_tma) {
         const unsigned grid = (unsigned)std::min<int64_t>(num_sms(), ntiles);
-        const cudaError_t e = dispatch_scan_tma(oid, p, excl, grid, s, tma_stats);
+        const cudaError_t e = dispatch_scan_tma(oid, p, excl, grid, s, tma_stats, cfg);
         return finish_launch(*ws, ntiles + grid * (unsigned)scg::tma_ids_per_cta(), e);
     }
     return finish_launch(*ws, ntiles, dispatch_scan(oid, p, excl, seg_len > 0, legacy_variant, s));
@@ -636,16 +648,19 @@ sc_status sc_debug_lookback_stats(sc_stream_t stream, uint64_t* out8) {
 }
 
 sc_status sc_set_scan_variant(int variant) {
-    if (variant < 0 || variant > kTmaStatsVariant) return SC_ERR_INVALID;
+    if (variant < 0 || variant > max_variant()) return SC_ERR_INVALID;
     g_variant.store(variant);
     return SC_OK;
 }
 
 sc_status sc_scan_variant_info(int variant, int* threads, int* items, int* loader) {
-    if (variant < 0 || variant > kTmaStatsVariant) return SC_ERR_INVALID;
-    if (variant == 0 || variant == kTmaStatsVariant) {  // persistent TMA kernel: compute threads, items per compute thread
-        if (threads) *threads = 256;
-        if (items) *items = scg::tma_tile_elems(4) / 256;
+    if (variant < 0 || variant > max_variant()) return SC_ERR_INVALID;
+    const int cfg = tma_cfg_of(variant);
+    if (cfg >= 0) {  // persistent TMA kernel: compute threads, 4-byte items per compute thread
+        scg::TmaShape sh{0, 0, 0, 0};
+        scg::tma_shape(cfg, &sh);
+        if (threads) *threads = sh.compute_threads;
+        if (items) *items = sh.tile_bytes / 4 / sh.compute_threads;
         if (loader) *loader = 2;
         return SC_OK;
     }

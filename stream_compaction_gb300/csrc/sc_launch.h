@@ -47,16 +47,22 @@ template <> cudaError_t launch_scan<OpMaxI32>(const ScanParams&, bool, bool, int
 template <> cudaError_t launch_scan<OpAffineU32>(const ScanParams&, bool, bool, int, cudaStream_t);
 
 // Persistent TMA-pipelined scan (16-byte aligned arrays of at least one full
-// 16 KiB tile, no segments).  Its look-back runs over chunks of
-// tma_chunk_tiles() tiles: p.lb.num_tiles holds the number of chunks, and the
-// counter advances by num_chunks + grid * tma_ids_per_cta() per launch.
-// stats: instrumented build (uint32 sum only).
-int tma_tile_elems(int elem_bytes);
-int tma_chunk_tiles();
+// tile, no segments).  Its look-back runs over chunks of chunk_tiles tiles:
+// p.lb.num_tiles holds the number of chunks, and the counter advances by
+// num_chunks + grid * tma_ids_per_cta() per launch.  Shape 0 is the default of
+// every operator; shapes 1 .. tma_num_cfgs()-1 exist for the uint32 sum only.
+// stats: instrumented build (uint32 sum, shape 0).
+struct TmaShape {
+    int tile_bytes;
+    int chunk_tiles;
+    int compute_threads;
+    int threads;
+};
+int tma_num_cfgs();
 int tma_ids_per_cta();
-int tma_threads();
+bool tma_shape(int cfg, TmaShape* sh);
 template <class Op>
-cudaError_t launch_scan_tma(const ScanParams& p, bool exclusive, unsigned grid, cudaStream_t s, bool stats);
+cudaError_t launch_scan_tma(const ScanParams& p, bool exclusive, unsigned grid, cudaStream_t s, bool stats, int cfg);
 
 template <class T>
 cudaError_t launch_compact(const CompactParams& p, bool wide_count, cudaStream_t s);

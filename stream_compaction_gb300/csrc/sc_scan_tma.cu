@@ -42,60 +42,80 @@ namespace scg {
 
 namespace {
 
-constexpr int kSA = 6;                  // pass-1 stages: fresh tiles from HBM
-constexpr int kSB = 6;                  // pass-2 stages: the same tiles again, expected from L2
-constexpr int kChunk = 4;               // tiles per counter tick and per look-back status
-constexpr int kChunkSlots = 6;          // chunk bookkeeping ring
-constexpr int kRing = 32;               // per-tile bookkeeping ring
-constexpr int kR1 = 16;                 // pass-1-done barrier ring
-constexpr int kLag = 12;                // pass 2 of tile k follows pass 1 of tile k + kLag
-constexpr int kComputeWarps = 16;
-constexpr int kLbWarps = 3;
-constexpr int kStoreWarps = 2;
-constexpr int kBookWarp = kComputeWarps + kLbWarps;
-constexpr int kProducerA = kBookWarp + 1;
-constexpr int kProducerB = kProducerA + 1;
-constexpr int kStoreWarp0 = kProducerB + 1;
-constexpr int kThreads = 32 * (kStoreWarp0 + kStoreWarps);
-constexpr int kCompute = 32 * kComputeWarps;
-constexpr int kTileBytes = 16384;       // 128 rows of 128 bytes
-constexpr int kRows = kTileBytes / 128;
-constexpr int kBytesPerThread = kTileBytes / kCompute;  // 32: two 16-byte chunks per compute thread
-constexpr int kThreadsPerRow = 128 / kBytesPerThread;
+// Shape of the persistent kernel: tile bytes, fresh / re-load ring depths,
+// compute warps, pass-1 to pass-2 lag (tiles) and tiles per chunk.
+template <int TileBytes, int SA, int SB, int CW, int Lag, int Chunk>
+struct TmaCfg {
+    static constexpr int kTileBytes = TileBytes;  // rows of 128 bytes
+    static constexpr int kSA = SA;                // pass-1 stages: fresh tiles from HBM
+    static constexpr int kSB = SB;                // pass-2 stages: the same tiles again, from L2
+    static constexpr int kChunk = Chunk;          // tiles per counter tick and per look-back status
+    static constexpr int kLag = Lag;              // pass 2 of tile k follows pass 1 of tile k + kLag
+    static constexpr int kComputeWarps = CW;
+    static constexpr int kChunkSlots = 6;         // chunk bookkeeping ring
+    static constexpr int kRing = 64;              // per-tile bookkeeping ring
+    static constexpr int kR1 = 32;                // pass-1-done barrier ring
+    static constexpr int kLbWarps = 3;
+    static constexpr int kStoreWarps = SB % 2 == 0 ? 2 : 1;
+    static constexpr int kBookWarp = kComputeWarps + kLbWarps;
+    static constexpr int kProducerA = kBookWarp + 1;
+    static constexpr int kProducerB = kProducerA + 1;
+    static constexpr int kStoreWarp0 = kProducerB + 1;
+    static constexpr int kThreads = 32 * (kStoreWarp0 + kStoreWarps);
+    static constexpr int kCompute = 32 * kComputeWarps;
+    static constexpr int kRows = kTileBytes / 128;
+    static constexpr int kBytesPerThread = kTileBytes / kCompute;
+    static constexpr int kThreadsPerRow = 128 / kBytesPerThread;
+    static constexpr int kCtrlBytes = 16384;
+    static constexpr int kSmemBytes = (kSA + kSB) * kTileBytes + 1024 + kCtrlBytes;
+
+    // Parity waits on an mbarrier are exact only if the waiter is at most one
+    // phase behind.  Each ring below is waited on in order by one thread or
+    // warp (or by warps that always own the same slots), and its producer
+    // cannot run a full ring ahead of its consumer; these constraints keep
+    // that true.
+    static_assert(kChunkSlots % kLbWarps == 0, "a look-back warp owns fixed chunk slots");
+    static_assert(kSB % kStoreWarps == 0, "a store warp owns fixed pass-2 stages");
+    static_assert(kR1 > kLag && kLag >= kSB, "pass-1-done ring covers the lag");
+    static_assert(kRing >= kSA + kLag + kSB + 4, "tile ring outlives every reader");
+    static_assert(kChunkSlots * kChunk >= kLag + 2 * kChunk, "chunk ring covers the lag");
+    static_assert(kBytesPerThread % 16 == 0 && kBytesPerThread <= 128, "16-byte chunks within one row");
+    static_assert(kRows <= 256, "one TMA box per stage");
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+
+    struct Ctrl {
+        unsigned long long a_full[kSA], a_empty[kSA];
+        unsigned long long b_full[kSB], b_empty[kSB], written[kSB];
+        unsigned long long p1done[kR1];
+        unsigned long long wready[kR1];                   // all compute warps wrote their pass-1 totals
+        unsigned long long agg[kChunkSlots], pre[kChunkSlots];
+        unsigned tile[kRing];
+        unsigned long long offset[kRing];                 // carry-typed: fold of the chunk's earlier tiles
+        unsigned long long wtot[kRing][kComputeWarps];    // element-typed warp totals from pass 1
+        unsigned long long chunk_agg[kChunkSlots], chunk_prefix[kChunkSlots];
+        long long chunk_id[kChunkSlots];
+        int ok;
+        int end_k;                                        // iteration that carried the end-of-work sentinel
+        int consumed_a;                                   // last pass-1 fill the compute warps waited for
+        int consumed_b;                                   // last pass-2 fill the compute warps waited for
+    };
+    static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
+};
+
+// The shapes compiled in.  0 is the default of every operator (32 KiB tiles,
+// 3 + 3 stages, 8 compute warps, pass-2 lag of 6 tiles, 2-tile chunks: the
+// fastest of the shapes measured on GB300 for 2^30 uint32); the others are
+// uint32-sum variants kept for on-GPU comparison.
+using Cfg0 = TmaCfg<32768, 3, 3, 8, 6, 2>;
+using Cfg1 = TmaCfg<16384, 6, 6, 16, 12, 4>;
+using Cfg2 = TmaCfg<32768, 3, 3, 16, 6, 2>;
+using Cfg3 = TmaCfg<16384, 6, 6, 8, 12, 4>;
+using Cfg4 = TmaCfg<32768, 3, 3, 8, 8, 2>;
+constexpr int kNumCfgs = 5;
+
 constexpr int kLbPer = 8;               // at most 8 status words per lane: 256-chunk windows
 constexpr unsigned kSentinel = 0xffffffffu;  // end of work
 constexpr unsigned kVoid = 0xfffffffeu;      // past the last tile, inside the last chunk
-constexpr int kCtrlBytes = 8192;
-constexpr int kSmemBytes = (kSA + kSB) * kTileBytes + 1024 + kCtrlBytes;
-
-// Parity waits on an mbarrier are exact only if the waiter is at most one
-// phase behind.  Each ring below is waited on in order by one thread or warp
-// (or by warps that always own the same slots), and its producer cannot run a
-// full ring ahead of its consumer; these constants keep that true.
-static_assert(kChunkSlots % kLbWarps == 0, "a look-back warp owns fixed chunk slots");
-static_assert(kSB % kStoreWarps == 0, "a store warp owns fixed pass-2 stages");
-static_assert(kR1 > kLag - 0 && kLag >= kSB, "pass-1-done ring covers the lag");
-static_assert(kRing >= kSA + kLag + kSB + 4, "tile ring outlives every reader");
-static_assert(kChunkSlots * kChunk >= kLag + 2 * kChunk, "chunk ring covers the lag");
-
-struct Ctrl {
-    unsigned long long a_full[kSA], a_empty[kSA];
-    unsigned long long b_full[kSB], b_empty[kSB], written[kSB];
-    unsigned long long p1done[kR1];
-    unsigned long long wready[kR1];                   // all compute warps wrote their pass-1 totals
-    unsigned long long agg[kChunkSlots], pre[kChunkSlots];
-    unsigned tile[kRing];
-    unsigned long long offset[kRing];                 // carry-typed: fold of the chunk's earlier tiles
-    unsigned long long wtot[kRing][kComputeWarps];    // element-typed warp totals from pass 1
-    unsigned long long chunk_agg[kChunkSlots], chunk_prefix[kChunkSlots];
-    long long chunk_id[kChunkSlots];
-    unsigned long long run;                           // running chunk aggregate (bookkeeping warp)
-    int ok;
-    int end_k;                                        // iteration that carried the end-of-work sentinel
-    int consumed_a;                                   // last pass-1 fill the compute warps waited for
-    int consumed_b;                                   // last pass-2 fill the compute warps waited for
-};
-static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
 template <class V>
 __device__ __forceinline__ unsigned long long pack_bits(V v) {
@@ -148,12 +168,19 @@ __device__ __forceinline__ void vstore(int* p, int v) { *reinterpret_cast<volati
 // [5] look-back polls that found a predecessor not yet published, [6] ns
 // look-back warps waited for chunk aggregates, [7] ns the fresh-tile producer
 // waited for a free stage.
-template <class Op, bool kExcl, bool kStats>
-__global__ void __launch_bounds__(kThreads, 1)
+template <class Op, bool kExcl, bool kStats, class Cfg>
+__global__ void __launch_bounds__(Cfg::kThreads, 1)
     scan_tma_kernel(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtensorMap tm_out,
                     const ScanParams p, const long long n_full_tiles) {
     using T = typename Op::T;
     using C = typename Op::C;
+    using Ctrl = typename Cfg::Ctrl;
+    constexpr int kTileBytes = Cfg::kTileBytes, kSA = Cfg::kSA, kSB = Cfg::kSB, kChunk = Cfg::kChunk;
+    constexpr int kLag = Cfg::kLag, kComputeWarps = Cfg::kComputeWarps, kChunkSlots = Cfg::kChunkSlots;
+    constexpr int kRing = Cfg::kRing, kR1 = Cfg::kR1, kLbWarps = Cfg::kLbWarps, kStoreWarps = Cfg::kStoreWarps;
+    constexpr int kBookWarp = Cfg::kBookWarp, kProducerA = Cfg::kProducerA, kProducerB = Cfg::kProducerB;
+    constexpr int kStoreWarp0 = Cfg::kStoreWarp0, kCompute = Cfg::kCompute, kRows = Cfg::kRows;
+    constexpr int kBytesPerThread = Cfg::kBytesPerThread, kThreadsPerRow = Cfg::kThreadsPerRow;
     constexpr int IPT = kBytesPerThread / sizeof(T);
     constexpr int TILE = kCompute * IPT;
     constexpr int NV = kBytesPerThread / 16;  // 16-byte chunks per compute thread
@@ -204,6 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // atomic's latency, late enough that chunks are published in about the
         // order in which they were handed out
         unsigned long long a0 = atomicAdd(ctr, 1ull);
+        // fresh tiles stay in L2 until their pass-2 re-load
+        const uint64_t keep = l2_policy_evict_last();
         int issued = -1;
         long long c = 0;
         unsigned long long waited = 0;
@@ -229,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             issued = k;
             if (!done && t < n_full_tiles) {
                 mbar_arrive_expect_tx(B(ctl->a_full[s]), kTileBytes);
-                tma_load_2d(stageA + s * kTileBytes, &tm_in, 0, (int)(t * kRows), B(ctl->a_full[s]));
+                tma_load_2d_hint(stageA + s * kTileBytes, &tm_in, 0, (int)(t * kRows), B(ctl->a_full[s]), keep);
             } else {
                 mbar_arrive(B(ctl->a_full[s]));  // sentinel, void slot, or the ragged last tile
             }
@@ -248,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------- producer B: re-loads for pass 2
     if (warp == kProducerB) {
         if (lane != 0) return;
+        const uint64_t drop = l2_policy_evict_first();  // last use of the input tile
         int issued = -1;
         for (int j = 0;; ++j) {
             const int s = j % kSB;
@@ -259,7 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             issued = j;
             if (tu != kVoid && (long long)tu < n_full_tiles) {
                 mbar_arrive_expect_tx(B(ctl->b_full[s]), kTileBytes);
-                tma_load_2d(stageB + s * kTileBytes, &tm_in, 0, (int)((long long)tu * kRows), B(ctl->b_full[s]));
+                tma_load_2d_hint(stageB + s * kTileBytes, &tm_in, 0, (int)((long long)tu * kRows), B(ctl->b_full[s]),
+                                 drop);
             } else {
                 mbar_arrive(B(ctl->b_full[s]));  // void slot or the ragged last tile
             }
@@ -275,12 +306,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the store has read it.
     if (warp >= kStoreWarp0) {
         if (lane != 0) return;
+        const uint64_t stream = l2_policy_evict_first();  // outputs are not read again here
         for (int j = warp - kStoreWarp0;; j += kStoreWarps) {
             const int s = j % kSB;
             if (*end_k <= j || !bar_wait(B(ctl->written[s]), (j / kSB) & 1, wait_limit, end_k, j)) break;
             const unsigned tu = ctl->tile[j % kRing];
             if (tu != kVoid && (long long)tu < n_full_tiles) {
-                tma_store_2d(&tm_out, 0, (int)((long long)tu * kRows), stageB + s * kTileBytes);
+                tma_store_2d_hint(&tm_out, 0, (int)((long long)tu * kRows), stageB + s * kTileBytes, stream);
                 bulk_commit();
                 bulk_wait_read_all();
             }
@@ -551,20 +583,26 @@ bool encoder() {
     return g_encode != nullptr;
 }
 
-// The first `rows` rows of 128 bytes at `base`, boxes of kRows rows, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, unsigned long long rows) {
+// The first `rows` rows of 128 bytes at `base`, boxes of `box_rows` rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, unsigned long long rows, unsigned box_rows) {
     const cuuint64_t dims[2] = {32, rows};
     const cuuint64_t strides[1] = {128};
-    const cuuint32_t box[2] = {32, (cuuint32_t)kRows};
+    const cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <class Op, bool kExcl, bool kStats>
-cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const ScanParams& p, long long nfull,
-                       unsigned grid, cudaStream_t s) {
+template <class Op, bool kExcl, bool kStats, class Cfg>
+cudaError_t launch_one(const ScanParams& p, unsigned grid, cudaStream_t s) {
+    using T = typename Op::T;
+    const long long tile = Cfg::kTileBytes / sizeof(T);
+    const long long nfull = p.n / tile;
+    if (!encoder()) return cudaErrorNotSupported;
+    CUtensorMap a, b;
+    const unsigned long long rows = (unsigned long long)nfull * Cfg::kRows;
+    if (!make_map(&a, p.in, rows, Cfg::kRows) || !make_map(&b, p.out, rows, Cfg::kRows)) return cudaErrorInvalidValue;
     // the large dynamic shared-memory opt-in is per device
     static std::atomic<unsigned long long> done_mask{0};
     int dev = 0;
@@ -572,44 +610,68 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const ScanPar
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(done_mask.load() & bit)) {
-        e = cudaFuncSetAttribute(scan_tma_kernel<Op, kExcl, kStats>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes);
+        e = cudaFuncSetAttribute(scan_tma_kernel<Op, kExcl, kStats, Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg::kSmemBytes);
         if (e != cudaSuccess) return e;
         done_mask.fetch_or(bit);
     }
-    scan_tma_kernel<Op, kExcl, kStats><<<grid, kThreads, kSmemBytes, s>>>(a, b, p, nfull);
+    scan_tma_kernel<Op, kExcl, kStats, Cfg><<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(a, b, p, nfull);
     return cudaGetLastError();
+}
+
+template <class Op, class Cfg>
+cudaError_t launch_cfg(const ScanParams& p, bool exclusive, unsigned grid, cudaStream_t s, bool stats) {
+    if (stats) {
+        if constexpr (std::is_same<Op, OpSumU32>::value)
+            return exclusive ? launch_one<Op, true, true, Cfg>(p, grid, s) : launch_one<Op, false, true, Cfg>(p, grid, s);
+        return cudaErrorInvalidValue;
+    }
+    return exclusive ? launch_one<Op, true, false, Cfg>(p, grid, s) : launch_one<Op, false, false, Cfg>(p, grid, s);
+}
+
+template <class Cfg>
+void cfg_info(TmaShape* sh) {
+    sh->tile_bytes = Cfg::kTileBytes;
+    sh->chunk_tiles = Cfg::kChunk;
+    sh->compute_threads = Cfg::kCompute;
+    sh->threads = Cfg::kThreads;
 }
 
 }  // namespace
 
-int tma_tile_elems(int elem_bytes) { return kTileBytes / elem_bytes; }
-int tma_chunk_tiles() { return kChunk; }
+int tma_num_cfgs() { return kNumCfgs; }
 int tma_ids_per_cta() { return 2; }  // one requested ahead + the one that ends the CTA's loop
-int tma_threads() { return kThreads; }
 
-template <class Op>
-cudaError_t launch_scan_tma(const ScanParams& p, bool exclusive, unsigned grid, cudaStream_t s, bool stats) {
-    using T = typename Op::T;
-    const long long tile = kTileBytes / sizeof(T);
-    const long long nfull = p.n / tile;
-    if (!encoder()) return cudaErrorNotSupported;
-    CUtensorMap a, b;
-    if (!make_map(&a, p.in, (unsigned long long)nfull * kRows) || !make_map(&b, p.out, (unsigned long long)nfull * kRows))
-        return cudaErrorInvalidValue;
-    if (stats) {
-        if constexpr (std::is_same<Op, OpSumU32>::value)
-            return exclusive ? launch_one<Op, true, true>(a, b, p, nfull, grid, s)
-                             : launch_one<Op, false, true>(a, b, p, nfull, grid, s);
-        return cudaErrorInvalidValue;
+bool tma_shape(int cfg, TmaShape* sh) {
+    switch (cfg) {
+    case 0: cfg_info<Cfg0>(sh); return true;
+    case 1: cfg_info<Cfg1>(sh); return true;
+    case 2: cfg_info<Cfg2>(sh); return true;
+    case 3: cfg_info<Cfg3>(sh); return true;
+    case 4: cfg_info<Cfg4>(sh); return true;
+    default: return false;
     }
-    return exclusive ? launch_one<Op, true, false>(a, b, p, nfull, grid, s)
-                     : launch_one<Op, false, false>(a, b, p, nfull, grid, s);
 }
 
-template cudaError_t launch_scan_tma<OpSumU32>(const ScanParams&, bool, unsigned, cudaStream_t, bool);
-template cudaError_t launch_scan_tma<OpSumF32>(const ScanParams&, bool, unsigned, cudaStream_t, bool);
-template cudaError_t launch_scan_tma<OpMaxI32>(const ScanParams&, bool, unsigned, cudaStream_t, bool);
-template cudaError_t launch_scan_tma<OpAffineU32>(const ScanParams&, bool, unsigned, cudaStream_t, bool);
+template <class Op>
+cudaError_t launch_scan_tma(const ScanParams& p, bool exclusive, unsigned grid, cudaStream_t s, bool stats, int cfg) {
+    if (cfg == 0) return launch_cfg<Op, Cfg0>(p, exclusive, grid, s, stats);
+    if constexpr (std::is_same<Op, OpSumU32>::value) {
+        if (stats) return cudaErrorInvalidValue;
+        switch (cfg) {
+        case 1: return launch_cfg<Op, Cfg1>(p, exclusive, grid, s, false);
+        case 2: return launch_cfg<Op, Cfg2>(p, exclusive, grid, s, false);
+        case 3: return launch_cfg<Op, Cfg3>(p, exclusive, grid, s, false);
+        case 4: return launch_cfg<Op, Cfg4>(p, exclusive, grid, s, false);
+        default: break;
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+template cudaError_t launch_scan_tma<OpSumU32>(const ScanParams&, bool, unsigned, cudaStream_t, bool, int);
+template cudaError_t launch_scan_tma<OpSumF32>(const ScanParams&, bool, unsigned, cudaStream_t, bool, int);
+template cudaError_t launch_scan_tma<OpMaxI32>(const ScanParams&, bool, unsigned, cudaStream_t, bool, int);
+template cudaError_t launch_scan_tma<OpAffineU32>(const ScanParams&, bool, unsigned, cudaStream_t, bool, int);
 
 }  // namespace scg

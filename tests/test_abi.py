@@ -69,7 +69,7 @@ def test_host_side_argument_checks(lib):
     # tuning and test hooks
     assert sc.sc_set_scan_variant(99) == sc.SC_ERR_INVALID
     st, t, i, l = sc.sc_scan_variant_info(0)
-    assert st == sc.SC_OK and t * i == 4096
+    assert st == sc.SC_OK and l == 2 and t * i * 4 >= 16384  # persistent TMA kernel, >= 16 KiB tiles
     assert sc.sc_debug_set_lookback(-5, -1, 0, 0) == sc.SC_ERR_INVALID
     assert sc.sc_debug_set_lookback(-1, -1, 0, 0) == sc.SC_OK
     assert sc.sc_workspace_bytes(1 << 30) >= 8 * ((1 << 30) // 4096)

@@ -16,8 +16,8 @@ from stream_compaction_gb300 import synth
 pytestmark = pytest.mark.gpu
 
 T = 4096  # default tile of the 4-byte operators (affine: 2048)
-SIZES = [1, 2, 3, 31, 32, 33, 1000, T - 1, T, T + 1, 2 * T - 1, 2 * T + 1, 7 * T + 13, 33 * T + 5,
-         (1 << 20) + 17, 100 * T + 4095, 1000 * T + 17, 3000 * T - 1]
+SIZES = [1, 2, 3, 31, 32, 33, 1000, T - 1, T, T + 1, 2 * T - 1, 2 * T + 1, 2 * T + 2, 4 * T - 1, 4 * T + 1,
+         7 * T + 13, 33 * T + 5, (1 << 20) + 17, 100 * T + 4095, 1000 * T + 17, 3000 * T - 1]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -87,12 +87,22 @@ def test_closed_forms_on_gpu():
     assert ya[0].tolist() == [1, 0]
 
 
-@pytest.mark.parametrize("variant", range(16))
+def _num_variants():
+    import stream_compaction_gb300 as sc
+    v = 0
+    while sc.sc_scan_variant_info(v)[0] == sc.SC_OK:
+        v += 1
+    return v
+
+
+@pytest.mark.parametrize("variant", range(21))
 def test_uint32_variants(variant):
     import stream_compaction_gb300 as sc
+    if variant >= _num_variants():
+        pytest.skip("variant not compiled")
     assert sc.sc_set_scan_variant(variant) == sc.SC_OK
     try:
-        for n in (1, 4097, 8191, 8192, 8193, 77 * 4096 + 1234):
+        for n in (1, 4097, 8191, 8192, 8193, 16385, 77 * 4096 + 1234, 301 * 8192 + 77):
             x = _input("u32", n, seed=variant * 1000 + n)
             for ex in (False, True):
                 assert np.array_equal(gpu_scan(x, "sum", ex), oracle.scan(x, "sum", ex)), (variant, n, ex)
@@ -106,7 +116,7 @@ def test_repeated_runs_are_exact():
     import stream_compaction_gb300 as sc
     rng = np.random.default_rng(5)
     for it in range(60):
-        sc.sc_set_scan_variant(it % 16)
+        sc.sc_set_scan_variant(it % _num_variants())
         n = int(rng.integers(1, 3 << 20))
         x = _input("u32", n, seed=it)
         assert np.array_equal(gpu_scan(x, "sum", it % 2 == 0), oracle.scan(x, "sum", it % 2 == 0)), (it, n)
