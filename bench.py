@@ -44,6 +44,10 @@ def parse():
     ap.add_argument("--variant", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--suite", action="store_true")
+    ap.add_argument("--profile-case", type=int, default=0, metavar="N",
+                    help="no timing: run the headline scan on the first N elements --steps times (for ncu)")
+    ap.add_argument("--profile-op", default="scan", choices=["scan", "compact", "rows", "hier"],
+                    help="which kernel --profile-case runs")
     return ap.parse_args()
 
 
@@ -424,8 +428,50 @@ def run_ours(args, rank, world, local_rank):
         suite_lines(args, dev, sc, synth)
 
 
+def profile_case(args):
+    """A bare invocation of one kernel for profilers: no timing, no host copies."""
+    import torch
+    import stream_compaction_gb300 as sc
+    from stream_compaction_gb300 import build as scbuild, synth
+    if not scbuild.up_to_date():
+        scbuild.build()
+    sc.load()
+    sc.sc_set_scan_variant(args.variant)
+    n = args.profile_case
+    sp = int(torch.cuda.current_stream().cuda_stream)
+    if args.profile_op == "compact":
+        x = synth.make_torch(synth.WORKLOADS["int32_compact_gt0_n2^27"], n=n, device="cuda")
+        y = torch.empty_like(x)
+        cnt = torch.empty(1, dtype=torch.int64, device="cuda")
+        run = lambda: sc.sc_compact_if(sc.SC_I32, x.data_ptr(), y.data_ptr(), cnt.data_ptr(), n, sc.SC_GT, 0.0, sp)
+    elif args.profile_op == "rows":
+        cols = 4096
+        n = n // cols * cols
+        x = synth.make_torch(synth.WORKLOADS["int32_rows_65536x4096"], n=n, device="cuda")
+        y = torch.empty_like(x)
+        run = lambda: sc.sc_scan_batched(sc.SC_I32, sc.SC_SUM, 1, x.data_ptr(), y.data_ptr(), n // cols, cols, sp)
+    else:
+        x = synth.make_torch(synth.WORKLOADS[WORKLOAD], n=n, device="cuda")
+        y = torch.empty_like(x)
+        if args.profile_op == "hier":
+            run = lambda: sc.sc_scan_hierarchical(sc.SC_U32, sc.SC_SUM, 1, x.data_ptr(), y.data_ptr(), n, sp)
+        else:
+            run = lambda: sc.sc_scan_exclusive(sc.SC_U32, sc.SC_SUM, x.data_ptr(), y.data_ptr(), n, sp)
+    for _ in range(max(1, args.steps)):
+        st = run()
+        if st != sc.SC_OK:
+            raise SystemExit(sc.status_string(st))
+    torch.cuda.synchronize()
+    if sc.sc_get_device_error(sp) != sc.SC_OK:
+        raise SystemExit("device error")
+    print("profile case ok: %s n=%d x%d" % (args.profile_op, n, max(1, args.steps)))
+
+
 def main():
     args = parse()
+    if args.profile_case:
+        profile_case(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
