@@ -49,6 +49,7 @@ SIGNATURES = {
     "sc_get_device_error": ([_P], _INT),
     "sc_launch_count": ([], _U64),
     "sc_set_scan_variant": ([_INT], _INT),
+    "sc_set_compact_variant": ([_INT], _INT),
     "sc_scan_variant_info": ([_INT, ctypes.POINTER(_INT), ctypes.POINTER(_INT), ctypes.POINTER(_INT)], _INT),
     "sc_debug_set_lookback": ([_I64, _I64, _U32, _U64], _INT),
     "sc_debug_lookback_stats": ([_P, ctypes.POINTER(_U64)], _INT),
@@ -153,6 +154,10 @@ def sc_launch_count() -> int:
 
 def sc_set_scan_variant(variant: int) -> int:
     return load().sc_set_scan_variant(variant)
+
+
+def sc_set_compact_variant(variant: int) -> int:
+    return load().sc_set_compact_variant(variant)
 
 
 def sc_scan_variant_info(variant: int):

@@ -45,6 +45,7 @@ int tma_cfg_of(int v) {
 
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_variant{0};
+std::atomic<int> g_compact_variant{0};  // 0, 1: persistent kernel shapes; 2: one tile per CTA
 std::atomic<long long> g_stall_tile{-1};
 std::atomic<long long> g_delay_tile{-1};
 std::atomic<unsigned> g_delay_ns{0};
@@ -454,14 +455,27 @@ sc_status sc_compact_if(sc_dtype dtype, const void* in, void* out, int64_t* d_co
     else if (dtype == SC_U32) p.pred = int_pred(pred, threshold, 0.0, (double)UINT32_MAX);
     else p.pred = float_pred(pred, threshold);
 
-    const unsigned ntiles = (unsigned)ceil_div(n, scg::CompactConfig::TILE);
     const bool wide = n > (int64_t)UINT32_MAX;
+    // persistent kernel for 16-byte aligned inputs of at least one full tile
+    const int64_t ptile = scg::compact_tma_tile_elems();
+    const int cvar = g_compact_variant.load();
+    const bool use_tma = p.vec_ok && n >= ptile && n / ptile * (ptile * 4 / 128) < (int64_t)INT_MAX && num_sms() > 0 &&
+                         cvar < 2;
+    const int64_t unit = use_tma ? ptile * scg::compact_tma_chunk_tiles() : scg::CompactConfig::TILE;
+    const unsigned ntiles = (unsigned)ceil_div(n, unit);
     std::lock_guard<std::mutex> lk(g_ws_mu);
     Workspace* ws = nullptr;
     sc_status st = acquire_ws(s, lookback_bytes(n), &ws);
     if (st != SC_OK) return st;
     p.lb = make_ctl(*ws, ntiles);
     cudaError_t e;
+    if (use_tma) {
+        const unsigned grid = (unsigned)std::min<int64_t>(num_sms(), ntiles);
+        if (dtype == SC_I32) e = scg::launch_compact_tma<int32_t>(p, wide, grid, s, cvar);
+        else if (dtype == SC_U32) e = scg::launch_compact_tma<uint32_t>(p, wide, grid, s, cvar);
+        else e = scg::launch_compact_tma<float>(p, wide, grid, s, cvar);
+        return finish_launch(*ws, ntiles + grid * (unsigned)scg::tma_ids_per_cta(), e);
+    }
     if (dtype == SC_I32) e = scg::launch_compact<int32_t>(p, wide, s);
     else if (dtype == SC_U32) e = scg::launch_compact<uint32_t>(p, wide, s);
     else e = scg::launch_compact<float>(p, wide, s);
@@ -650,6 +664,12 @@ sc_status sc_debug_lookback_stats(sc_stream_t stream, uint64_t* out8) {
 sc_status sc_set_scan_variant(int variant) {
     if (variant < 0 || variant > max_variant()) return SC_ERR_INVALID;
     g_variant.store(variant);
+    return SC_OK;
+}
+
+sc_status sc_set_compact_variant(int variant) {
+    if (variant < 0 || variant > 2) return SC_ERR_INVALID;
+    g_compact_variant.store(variant);
     return SC_OK;
 }
 

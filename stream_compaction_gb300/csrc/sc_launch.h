@@ -67,6 +67,15 @@ cudaError_t launch_scan_tma(const ScanParams& p, bool exclusive, unsigned grid, 
 template <class T>
 cudaError_t launch_compact(const CompactParams& p, bool wide_count, cudaStream_t s);
 
+// Persistent TMA-pipelined compaction (16-byte aligned input of at least one
+// full tile): look-back over chunks of compact_tma_chunk_tiles() tiles of
+// compact_tma_tile_elems() elements; p.lb.num_tiles holds the number of
+// chunks; the counter advances by num_chunks + grid * tma_ids_per_cta().
+int compact_tma_tile_elems();
+int compact_tma_chunk_tiles();
+template <class T>
+cudaError_t launch_compact_tma(const CompactParams& p, bool wide_count, unsigned grid, cudaStream_t s, int shape);
+
 // Hierarchical (scan-then-propagate) comparison variant.
 constexpr int kHierNT = 256;
 int hier_tile_elems(int op_id);

@@ -36,11 +36,14 @@
 #include "sc_device.cuh"
 #include "sc_launch.h"
 #include "sc_scan.cuh"
+#include "sc_persist.cuh"
 #include "sc_tma.cuh"
 
 namespace scg {
 
 namespace {
+
+using namespace persist;
 
 // Shape of the persistent kernel: tile bytes, fresh / re-load ring depths,
 // compute warps, pass-1 to pass-2 lag (tiles) and tiles per chunk.
@@ -117,48 +120,6 @@ constexpr int kLbPer = 8;               // at most 8 status words per lane: 256-
 constexpr unsigned kSentinel = 0xffffffffu;  // end of work
 constexpr unsigned kVoid = 0xfffffffeu;      // past the last tile, inside the last chunk
 
-template <class V>
-__device__ __forceinline__ unsigned long long pack_bits(V v) {
-    if constexpr (sizeof(V) == 4) return to_bits32(v);
-    else return to_bits64(v);
-}
-template <class V>
-__device__ __forceinline__ V unpack_bits(unsigned long long b) {
-    V v;
-    if constexpr (sizeof(V) == 4) from_bits32((uint32_t)b, v);
-    else from_bits64(b, v);
-    return v;
-}
-
-// Bounded wait on an mbarrier phase: gives up (false) after `limit_ns`, or
-// as soon as *end_k (when given) is <= k (iteration k will never come).
-__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns,
-                                         const volatile int* end_k = nullptr, int k = 0) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    for (unsigned i = 1; i < (1u << 30); ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (end_k && *end_k <= k) return false;
-        if ((i & 15u) == 0 && global_ns() - t0 > limit_ns) return false;
-    }
-    return false;
-}
-
-// Warp-uniform variant: lane 0 waits, the verdict is broadcast, and every
-// lane then observes the completed phase itself (so each lane's later reads of
-// what the phase protects are ordered after it).
-__device__ __forceinline__ bool warp_bar_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns,
-                                              const volatile int* end_k = nullptr, int k = 0) {
-    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;  // usually already complete
-    bool good = true;
-    if ((threadIdx.x & 31) == 0) good = bar_wait(bar, parity, limit_ns, end_k, k);
-    good = __shfl_sync(0xffffffffu, good, 0);
-    if (good) good = mbar_try_wait(bar, parity);
-    return __all_sync(0xffffffffu, good);
-}
-
-__device__ __forceinline__ int vload(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
-__device__ __forceinline__ void vstore(int* p, int v) { *reinterpret_cast<volatile int*>(p) = v; }
 
 }  // namespace
 
@@ -566,55 +527,17 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 // ----------------------------------------------------------------- host side
 namespace {
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
-
-bool encoder() {
-    std::call_once(g_encode_once, [] {
-        void* fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-        else
-            cudaGetLastError();
-    });
-    return g_encode != nullptr;
-}
-
-// The first `rows` rows of 128 bytes at `base`, boxes of `box_rows` rows, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, unsigned long long rows, unsigned box_rows) {
-    const cuuint64_t dims[2] = {32, rows};
-    const cuuint64_t strides[1] = {128};
-    const cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <class Op, bool kExcl, bool kStats, class Cfg>
 cudaError_t launch_one(const ScanParams& p, unsigned grid, cudaStream_t s) {
     using T = typename Op::T;
     const long long tile = Cfg::kTileBytes / sizeof(T);
     const long long nfull = p.n / tile;
-    if (!encoder()) return cudaErrorNotSupported;
     CUtensorMap a, b;
     const unsigned long long rows = (unsigned long long)nfull * Cfg::kRows;
     if (!make_map(&a, p.in, rows, Cfg::kRows) || !make_map(&b, p.out, rows, Cfg::kRows)) return cudaErrorInvalidValue;
-    // the large dynamic shared-memory opt-in is per device
     static std::atomic<unsigned long long> done_mask{0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    const cudaError_t e = allow_smem(scan_tma_kernel<Op, kExcl, kStats, Cfg>, Cfg::kSmemBytes, done_mask);
     if (e != cudaSuccess) return e;
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (!(done_mask.load() & bit)) {
-        e = cudaFuncSetAttribute(scan_tma_kernel<Op, kExcl, kStats, Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Cfg::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        done_mask.fetch_or(bit);
-    }
     scan_tma_kernel<Op, kExcl, kStats, Cfg><<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(a, b, p, nfull);
     return cudaGetLastError();
 }

@@ -38,6 +38,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same probe, but a thread whose phase is not yet complete may sleep until
+// it completes or `suspend_ns` pass (instead of a short, system-chosen time),
+// so waiting warps take no issue slots from the working ones.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t suspend_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(suspend_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // 2-D tiled TMA load: box at coordinates (x, y) of the tensor map into shared
 // memory, completion counted in bytes on `bar`.  x must keep x * 4 bytes a
 // multiple of 16 (here x is always 0).

@@ -194,3 +194,32 @@ def test_scan_host_other_ops(kind, op):
         check_f32(y, ref, oracle.abs_prefix(x))
     else:
         assert np.array_equal(y, ref)
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2])
+def test_compact_kernel_variants(variant):
+    """Every compaction kernel (persistent with 8 or 16 compute warps, one tile per CTA)
+    gives the oracle's result, for ragged sizes, all predicates and both count widths' paths."""
+    import stream_compaction_gb300 as sc
+    assert sc.sc_set_compact_variant(variant) == sc.SC_OK
+    try:
+        rng = np.random.default_rng(variant)
+        for n in (8192, 8193, 16384 * 3 + 5, 1000003, (1 << 22) + 7):
+            for dtype in ("i32", "u32", "f32"):
+                if dtype == "i32":
+                    x = rng.integers(-(1 << 20), 1 << 20, n).astype(np.int32)
+                    thr = 0
+                elif dtype == "u32":
+                    x = rng.integers(0, 1 << 32, n, dtype=np.uint64).astype(np.uint32)
+                    thr = float(1 << 31)
+                else:
+                    x = rng.uniform(-1, 1, n).astype(np.float32)
+                    thr = 0.25
+                for pred in ("gt", "le", "ne"):
+                    out, c, full = gpu_compact(x, pred, thr)
+                    ref, rc = oracle.compact(x, pred, thr)
+                    assert c == rc and np.array_equal(out.view(np.int32), ref.view(np.int32)), (n, dtype, pred)
+                    if c < n:
+                        assert np.all(full[c:n].view(np.int32) == -7)
+    finally:
+        sc.sc_set_compact_variant(0)
