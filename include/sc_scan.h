@@ -190,7 +190,7 @@ uint64_t sc_launch_count(void);
  * on-GPU comparison.  Returns SC_ERR_INVALID for an unknown variant. */
 sc_status sc_set_scan_variant(int variant);
 /* Select the fused-compaction kernel: 0 (default) the persistent TMA kernel
- * with 16 compute warps, 1 the same with 8 compute warps, 2 the
+ * with 8 compute warps, 1 the same with 16 compute warps, 2 the
  * one-tile-per-CTA kernel (inputs that are not 16-byte aligned, or smaller than
  * one 32 KiB tile, always use the latter).  SC_ERR_INVALID otherwise. */
 sc_status sc_set_compact_variant(int variant);

@@ -9,23 +9,25 @@
 // flags never reach memory and the scan of the flags is the same chained,
 // decoupled look-back over chunk counts as the persistent scan uses:
 //
-//   producer A      chunk ids from the atomic counter, fresh tiles by TMA;
-//   compute warps   pass 1: each warp evaluates the predicate on its part of a
-//                   fresh tile, keeps one 32-bit flag mask per 128-byte row
-//                   in shared memory and counts the kept elements (the stage
-//                   is freed at once);
-//                   pass 2 (kLag tiles later, the tile re-loaded from L2):
-//                   each warp packs its kept elements in order inside its own
-//                   part of the stage (the row masks + popcount give
-//                   consecutive slots), then writes them as one contiguous
-//                   run: the 16-byte aligned middle by a bulk copy, up to
-//                   3 + 3 edge elements by plain stores;
-//   bookkeeping     tile counts, chunk counts, chunk aggregates published;
+//   producer A      chunk ids from the atomic counter, fresh tiles by TMA
+//                   (kept in L2 for the re-load);
+//   compute warps   pass 1 (tile k): each warp evaluates the predicate on its
+//                   rows of the fresh tile and keeps, per 128-byte row, a
+//                   32-bit flag mask and the rank of the row's first kept
+//                   element within the warp's part; it counts its kept
+//                   elements and frees the stage at once;
+//                   pass 2 (tile k - kLag, re-loaded from L2 by producer B,
+//                   run in the same instruction stream as pass 1 of tile k):
+//                   each lane moves one 16-byte chunk per step and stores its
+//                   kept elements to consecutive output slots; a warp's stores
+//                   cover one contiguous run, which L2 merges into whole lines;
+//   bookkeeping     tile and warp offsets within a chunk, chunk aggregates
+//                   published;
 //   look-back       chunk prefixes; the last chunk also writes the count;
 //   producer B      the pass-2 re-loads.
 //
-// Each input element is read from HBM once and each kept element written
-// once.
+// Each input element is read from HBM once (and once more from L2) and each
+// kept element is written once.
 #include <atomic>
 #include <type_traits>
 
@@ -64,20 +66,20 @@ constexpr int kRows = kTileBytes / 128;
 constexpr int kSA = 3;                  // pass-1 stages: fresh tiles from HBM
 constexpr int kSB = 3;                  // pass-2 stages: the same tiles again, from L2
 constexpr int kChunk = 2;               // tiles per counter tick and per look-back status
-constexpr int kLag = 6;                 // pass 2 of tile k follows pass 1 of tile k + kLag
+constexpr int kLag = 8;                 // pass 2 of tile k follows pass 1 of tile k + kLag
 constexpr int kLbWarps = 3;
 constexpr int kChunkSlots = 6;
-constexpr int kRing = 64;
+constexpr int kRing = 32;
 constexpr int kR1 = 32;
 constexpr int TILE = kTileBytes / 4;    // 8192 four-byte elements
 constexpr int kLbPer = 8;
 constexpr unsigned kSentinel = 0xffffffffu;
 constexpr unsigned kVoid = 0xfffffffeu;
-constexpr int kCtrlBytes = 16384;
+constexpr int kCtrlBytes = 30720;
 constexpr int kSmemBytes = (kSA + kSB) * kTileBytes + 1024 + kCtrlBytes;
 constexpr int kMaxComputeWarps = 16;
-constexpr int kMaskRing = 8;            // tiles whose row masks are kept (pass 1 -> pass 2)
-static_assert(kMaskRing > kLag, "row masks outlive the lag");
+constexpr int kMaskRing = 12;           // tiles whose row information is kept (pass 1 -> pass 2)
+static_assert(kMaskRing > kLag, "row information outlives the lag");
 
 // Compute-warp count of a compaction shape: each warp owns kRowsPerWarp rows
 // (128 bytes each) of a tile in both passes.
@@ -108,10 +110,13 @@ struct Ctrl {
     unsigned long long b_full[kSB], b_empty[kSB];
     unsigned long long p1done[kR1], wready[kR1];
     unsigned long long agg[kChunkSlots], pre[kChunkSlots];
+    // per row of a tile, from pass 1: the flag mask (one bit per element of the
+    // 32-element row) and the rank of the row's first kept element within its
+    // warp part
+    uint2 rowinfo[kMaskRing][kRows];
     unsigned tile[kRing];
-    unsigned long long offset[kRing];        // count of kept elements in the chunk's earlier tiles
     unsigned wcnt[kRing][kMaxComputeWarps];  // kept elements per warp part, from pass 1
-    unsigned rowmask[kMaskRing][kRows];      // pass 1's flags, one bit per element of each 32-element row
+    unsigned woff[kRing][kMaxComputeWarps];  // kept elements of the chunk before each warp part
     unsigned long long chunk_agg[kChunkSlots], chunk_prefix[kChunkSlots];
     long long chunk_id[kChunkSlots];
     int end_k;
@@ -120,21 +125,6 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
-__device__ __forceinline__ uint32_t lds32(uint32_t a) {
-    uint32_t r;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(a) : "memory");
-    return r;
-}
-__device__ __forceinline__ void sts32(uint32_t a, uint32_t v) {
-    asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
-}
-__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
-                 : "memory");
-}
-
-template <class T>
-__device__ __forceinline__ uint32_t bits_of(T v) { return to_bits32(v); }
 template <class T>
 __device__ __forceinline__ T from_bits(uint32_t b) { T v; from_bits32(b, v); return v; }
 
@@ -253,29 +243,35 @@ __global__ void __launch_bounds__(CompactShape<CW>::kThreads, 1)
 
     // ------------------------------------------------------- bookkeeping
     if (warp == kBookWarp) {
-        C run = CntOp::c_identity();
+        unsigned run = 0;  // kept elements of the chunk's earlier tiles (at most kChunk * TILE)
         for (int k = 0;; ++k) {
             if (!warp_bar_wait(B(ctl->wready[k % kR1]), (k / kR1) & 1, wait_limit, end_k, k)) break;
             const unsigned w = lane < kComputeWarps ? ctl->wcnt[k % kRing][lane] : 0u;
-            const unsigned tcnt = __reduce_add_sync(0xffffffffu, w);
+            unsigned incl = w;
+#pragma unroll
+            for (int d = 1; d < kComputeWarps; d <<= 1) {
+                const unsigned y = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d) incl += y;
+            }
             const int pos = k % kChunk;
-            if (pos == 0) run = CntOp::c_identity();
+            if (pos == 0) run = 0;
+            if (lane < kComputeWarps) ctl->woff[k % kRing][lane] = run + incl - w;
+            run += __shfl_sync(0xffffffffu, incl, kComputeWarps - 1);
+            __syncwarp();
             if (lane == 0) {
-                ctl->offset[k % kRing] = (unsigned long long)run;
-                run = CntOp::c_op(run, CntOp::lift(tcnt));
                 if (pos == kChunk - 1) {
                     const int q = k / kChunk;
                     const long long c = ((long long)ctl->tile[(k - pos) % kRing]) / kChunk;
-                    ctl->chunk_agg[q % kChunkSlots] = (unsigned long long)run;
+                    const C agg = CntOp::lift(run);
+                    ctl->chunk_agg[q % kChunkSlots] = (unsigned long long)agg;
                     ctl->chunk_id[q % kChunkSlots] = c;
                     const bool stalled = p.lb.stall_tile >= 0 && p.lb.stall_tile / kChunk == c;
                     if (p.lb.delay_tile >= 0 && p.lb.delay_tile / kChunk == c) hook_delay(p.lb.delay_ns);
-                    if (!stalled) StatusIO<C>::publish(p.lb, c, c == 0 ? ST_PREFIX : ST_AGGREGATE, run);
+                    if (!stalled) StatusIO<C>::publish(p.lb, c, c == 0 ? ST_PREFIX : ST_AGGREGATE, agg);
                     mbar_arrive(B(ctl->agg[q % kChunkSlots]));
                 }
                 mbar_arrive(B(ctl->p1done[k % kR1]));
             }
-            run = __shfl_sync(0xffffffffu, run, 0);
         }
         return;
     }
@@ -309,7 +305,6 @@ __global__ void __launch_bounds__(CompactShape<CW>::kThreads, 1)
     // -------------------------------------------------------------- compute
     const int ctid = threadIdx.x;
     bool ok = true;
-    int pending = -1;  // stage whose bulk copy may still be reading (lane 0 of each warp)
     T* const out = static_cast<T*>(p.out);
 
     auto wait = [&](uint32_t b, uint32_t parity) {
@@ -320,155 +315,126 @@ __global__ void __launch_bounds__(CompactShape<CW>::kThreads, 1)
         }
         return good;
     };
-    // Lane 0: once the previous run's bulk copy has read the stage, free it.
-    auto release_pending = [&]() {
-        if (lane == 0 && pending >= 0) {
-            bulk_wait_read_all();
-            mbar_arrive(B(ctl->b_empty[pending]));
-            pending = -1;
-        }
-    };
 
-    // pass 1: kept elements in this warp's part of fresh tile k
-    // (thread = kChunksPerThread 16-byte chunks of one row)
+    // pass 1 (tile k, fresh from HBM): thread = kChunksPerThread 16-byte chunks
+    // of one row; flags land at their bit positions in the row's mask
     const int p1_row = ctid / kThreadsPerRow;
     const int p1_c0 = (ctid % kThreadsPerRow) * kChunksPerThread;
-    auto pass1 = [&](int k, int s, unsigned tu) {
-        uint32_t mine = 0;  // this thread's flags, already at their bit positions in the row
-        if (tu != kVoid) {
-            const long long t = tu;
-            if (t < n_full_tiles) {
-                const uint32_t row = stageA + s * kTileBytes + p1_row * 128;
+    auto p1_flags = [&](int s) {
+        const uint32_t row = stageA + s * kTileBytes + p1_row * 128;
+        uint4 raw[kChunksPerThread];
 #pragma unroll
-                for (int j = 0; j < kChunksPerThread; ++j) {
-                    T e[4];
-                    unpack(lds128(row + (((p1_c0 + j) ^ (p1_row & 7)) << 4)), e);
+        for (int c = 0; c < kChunksPerThread; ++c) raw[c] = lds128(row + (((p1_c0 + c) ^ (p1_row & 7)) << 4));
+        uint32_t mine = 0;
 #pragma unroll
-                    for (int w = 0; w < 4; ++w)
-                        if (keep_elem(e[w], p.pred)) mine |= 1u << ((p1_c0 + j) * 4 + w);
-                }
-            } else {
-                const long long first = t * TILE + (long long)ctid * kPerThread;
-                const T* in = static_cast<const T*>(p.in) + first;
-                const long long valid = p.n - first;
+        for (int c = 0; c < kChunksPerThread; ++c) {
+            T e[4];
+            unpack(raw[c], e);
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+                if (keep_elem(e[w], p.pred)) mine |= 1u << ((p1_c0 + c) * 4 + w);
+        }
+        return mine;
+    };
+    auto p1_flags_partial = [&](long long t) {  // the last, partial tile: from global memory
+        const long long first = t * TILE + (long long)ctid * kPerThread;
+        const T* in = static_cast<const T*>(p.in) + first;
+        const long long valid = p.n - first;
+        uint32_t mine = 0;
 #pragma unroll 4
-                for (int w = 0; w < kPerThread; ++w)
-                    if (w < valid && keep_elem(in[w], p.pred)) mine |= 1u << (p1_c0 * 4 + w);
-            }
+        for (int w = 0; w < kPerThread; ++w)
+            if (w < valid && keep_elem(in[w], p.pred)) mine |= 1u << (p1_c0 * 4 + w);
+        return mine;
+    };
+    // row masks with the rank of each row's first kept element, and the warp's count
+    auto p1_publish = [&](int k, uint32_t mine) {
+        const unsigned cnt = __popc(mine);
+        unsigned incl = cnt;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const unsigned y = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += y;
         }
         uint32_t rowm = mine;
         if constexpr (kThreadsPerRow == 2) rowm |= __shfl_xor_sync(0xffffffffu, mine, 1);
-        if (ctid % kThreadsPerRow == 0) ctl->rowmask[k % kMaskRing][p1_row] = rowm;
-        const unsigned wsum = __reduce_add_sync(0xffffffffu, (unsigned)__popc(mine));
-        if (lane == 0) ctl->wcnt[k % kRing][warp] = wsum;
+        if (ctid % kThreadsPerRow == 0) ctl->rowinfo[k % kMaskRing][p1_row] = make_uint2(rowm, incl - cnt);
+        if (lane == 31) ctl->wcnt[k % kRing][warp] = incl;
+    };
+
+    // pass 2 (tile j, re-loaded from L2): write this warp's kept elements to
+    // their output slots.  Each lane moves one 16-byte chunk per step and stores
+    // its kept elements to consecutive slots; a warp's stores cover one
+    // contiguous run, which L2 merges into whole lines.
+    constexpr int kSteps = kRowsPerWarp / 4;           // 4 rows (128 elements) per step
+    const uint32_t q_c = lane & 7, q_r = lane >> 3;    // step lane: 16-byte chunk q_c of row 4g + q_r
+    const uint32_t lowmask = (1u << (4 * q_c)) - 1u;   // elements of the row before the chunk
+    // the chunk's place in shared memory, 128-byte swizzle term (4g + q_r) & 7
+    const uint32_t ch_even = q_r * 128 + ((q_c ^ q_r) << 4);
+    const uint32_t ch_odd = q_r * 128 + ((q_c ^ (q_r | 4u)) << 4);
+    auto p2_load = [&](int j, uint4 (&v)[kSteps]) {
+        const uint32_t part = stageB + (j % kSB) * kTileBytes + warp * kWarpBytes;
+#pragma unroll
+        for (int g = 0; g < kSteps; ++g) v[g] = lds128(part + g * 512 + ((g & 1) ? ch_odd : ch_even));
+    };
+    auto p2_out = [&](int j) {  // output slot of the warp part's first kept element
+        return out + (long long)(ctl->chunk_prefix[(j / kChunk) % kChunkSlots] + ctl->woff[j % kRing][warp]);
+    };
+    // row information of each step's row (read before any store, so that no
+    // shared-memory load waits behind a global store)
+    auto p2_rows = [&](int j, uint2 (&r)[kSteps]) {
+        const uint2* ri = &ctl->rowinfo[j % kMaskRing][warp * kRowsPerWarp + q_r];
+#pragma unroll
+        for (int g = 0; g < kSteps; ++g) r[g] = ri[4 * g];
+    };
+    auto p2_store = [&](const uint4 (&v)[kSteps], const uint2 (&r)[kSteps], T* wout) {
+#pragma unroll
+        for (int g = 0; g < kSteps; ++g) {
+            const uint32_t nib = r[g].x >> (4 * q_c);
+            T* const o = wout + (r[g].y + __popc(r[g].x & lowmask));
+            if (nib & 1u) o[0] = from_bits<T>(v[g].x);
+            if (nib & 2u) o[nib & 1u] = from_bits<T>(v[g].y);
+            if (nib & 4u) o[__popc(nib & 3u)] = from_bits<T>(v[g].z);
+            if (nib & 8u) o[__popc(nib & 7u)] = from_bits<T>(v[g].w);
+        }
+    };
+
+    // general forms (first kLag tiles, the partial tile, void tiles, the drain)
+    auto pass1 = [&](int k, int s, unsigned tu) {
+        uint32_t mine = 0;
+        if (tu != kVoid) mine = (long long)tu < n_full_tiles ? p1_flags(s) : p1_flags_partial((long long)tu);
+        p1_publish(k, mine);
         __syncwarp();
         if (lane == 0) {
             mbar_arrive(B(ctl->a_empty[s]));
             mbar_arrive(B(ctl->wready[k % kR1]));
         }
     };
-
-    // pass 2: pack this warp's kept elements of tile j in order and write them out.
-    // Element ranks come from pass 1's row masks: rank = kept elements of the
-    // warp's part before it.  Rank r goes to slot r - h of the warp's part of
-    // the stage, where h (0..3) is the number of leading elements before the
-    // first 16-byte boundary of the output run; those h go to the top slots
-    // kW - h .. kW - 1 (slot (r - h) mod kW), which no other rank reaches since
-    // ranks stay below kW.  Slots 0 .. mid - 1 then leave by one bulk copy,
-    // the head and the tail (< 4 elements) by plain stores.
-    constexpr int kSteps = kRowsPerWarp / 4;           // 4 rows (128 elements) per step
-    constexpr unsigned kW = kRowsPerWarp * 32;         // slots (elements) of a warp's part
-    const uint32_t q_c = lane & 7, q_r = lane >> 3;    // step lane: 16-byte chunk q_c of row 4g + q_r
-    const uint32_t lowmask = (1u << (4 * q_c)) - 1u;   // elements of the row before the chunk
-    // the chunk's place in shared memory, 128-byte swizzle term (4g + q_r) & 7
-    const uint32_t ch_even = q_r * 128 + ((q_c ^ q_r) << 4);
-    const uint32_t ch_odd = q_r * 128 + ((q_c ^ (q_r | 4u)) << 4);
     auto pass2 = [&](int j) {
-        const int s = j % kSB;
-        const int q = j / kChunk;
         const unsigned tu = ctl->tile[j % kRing];
-        release_pending();
-        if (tu == kVoid) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(B(ctl->b_empty[s]));
-            return;
-        }
-        const long long t = tu;
-        // output position of this warp's first kept element
-        const unsigned wv = lane < kComputeWarps ? ctl->wcnt[j % kRing][lane] : 0u;
-        unsigned incl = wv;
-#pragma unroll
-        for (int d = 1; d < kComputeWarps; d <<= 1) {
-            const unsigned y = __shfl_up_sync(0xffffffffu, incl, d);
-            if (lane >= d) incl += y;
-        }
-        const unsigned wpre = warp > 0 ? __shfl_sync(0xffffffffu, incl, warp - 1) : 0u;
-        const unsigned wcnt = __shfl_sync(0xffffffffu, wv, warp);
-        const long long gw = (long long)(ctl->chunk_prefix[q % kChunkSlots] + ctl->offset[j % kRing]) + wpre;
-        const uintptr_t a0 = reinterpret_cast<uintptr_t>(out + gw);
-        const unsigned h = min(wcnt, (unsigned)(((16u - (unsigned)(a0 & 15u)) & 15u) >> 2));
-        const unsigned mid = (wcnt - h) & ~3u;
-        const uint32_t region = stageB + s * kTileBytes + warp * kWarpBytes;
-        // lane r < kRowsPerWarp: row r's mask and the rank (minus h) of its first kept element
-        const uint32_t mr = lane < kRowsPerWarp ? ctl->rowmask[j % kMaskRing][warp * kRowsPerWarp + lane] : 0u;
-        unsigned rin = __popc(mr);
-#pragma unroll
-        for (int d = 1; d < kRowsPerWarp; d <<= 1) {
-            const unsigned y = __shfl_up_sync(0xffffffffu, rin, d);
-            if (lane >= d) rin += y;
-        }
-        const int rfirst = (int)(rin - __popc(mr)) - (int)h;
-        if (t < n_full_tiles) {
-            // every lane reads all its chunks before any lane writes: the
-            // packing overwrites the part in place
-            uint4 v[kSteps];
-#pragma unroll
-            for (int g = 0; g < kSteps; ++g) v[g] = lds128(region + g * 512 + ((g & 1) ? ch_odd : ch_even));
-            __syncwarp();
-#pragma unroll
-            for (int g = 0; g < kSteps; ++g) {
-                const int row = 4 * g + (int)q_r;
-                const uint32_t m = __shfl_sync(0xffffffffu, mr, row);
-                const int e = __shfl_sync(0xffffffffu, rfirst, row) + __popc(m & lowmask);
-                const uint32_t nib = m >> (4 * q_c);
-                if (e >= 0) {
-                    const uint32_t a = region + 4u * (uint32_t)e;
-                    if (nib & 1u) sts32(a, v[g].x);
-                    if (nib & 2u) sts32(a + 4u * (nib & 1u), v[g].y);
-                    if (nib & 4u) sts32(a + 4u * __popc(nib & 3u), v[g].z);
-                    if (nib & 8u) sts32(a + 4u * __popc(nib & 7u), v[g].w);
-                } else {  // holds some of the warp's first h kept elements
-                    const uint32_t w4[4] = {v[g].x, v[g].y, v[g].z, v[g].w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        if ((nib >> i) & 1u)
-                            sts32(region + 4u * ((uint32_t)(e + __popc(nib & ((1u << i) - 1u))) & (kW - 1u)), w4[i]);
+        if (tu != kVoid) {
+            T* const wout = p2_out(j);
+            const long long t = tu;
+            if (t < n_full_tiles) {
+                uint4 v[kSteps];
+                uint2 r[kSteps];
+                p2_load(j, v);
+                p2_rows(j, r);
+                p2_store(v, r, wout);
+            } else {
+                const T* in = static_cast<const T*>(p.in) + t * TILE + (long long)warp * (kRowsPerWarp * 32);
+                const uint2* ri = &ctl->rowinfo[j % kMaskRing][warp * kRowsPerWarp];
+                const uint32_t below = lanemask_lt();
+                for (int jj = 0; jj < kRowsPerWarp; ++jj) {
+                    const uint2 r = ri[jj];
+                    if ((r.x >> lane) & 1u) wout[r.y + __popc(r.x & below)] = in[jj * 32 + lane];
                 }
             }
-        } else {  // the partial last tile: values from global memory, one row per step
-            const uint32_t* in = static_cast<const uint32_t*>(p.in) + t * TILE + (long long)warp * kW;
-            const uint32_t below = lanemask_lt();
-            for (int jj = 0; jj < kRowsPerWarp; ++jj) {
-                const uint32_t m = __shfl_sync(0xffffffffu, mr, jj);
-                const int e = __shfl_sync(0xffffffffu, rfirst, jj) + __popc(m & below);
-                if ((m >> lane) & 1u) sts32(region + 4u * ((uint32_t)e & (kW - 1u)), in[jj * 32 + lane]);
-            }
         }
-        fence_proxy_async();
         __syncwarp();
-        const unsigned tail = wcnt - h - mid;  // < 4
-        if (lane < h) out[gw + lane] = from_bits<T>(lds32(region + 4u * (kW - h + lane)));
-        else if (lane >= 4 && lane - 4 < tail) out[gw + h + mid + (lane - 4)] = from_bits<T>(lds32(region + 4u * (mid + lane - 4)));
-        if (lane == 0) {
-            if (mid > 0) {
-                bulk_s2g(out + gw + h, region, mid * 4);
-                bulk_commit();
-                pending = s;
-            } else {
-                mbar_arrive(B(ctl->b_empty[s]));
-            }
-        }
+        if (lane == 0) mbar_arrive(B(ctl->b_empty[j % kSB]));
     };
+    const auto pre_bar = [&](int j) { return B(ctl->pre[(j / kChunk) % kChunkSlots]); };
+    const auto pre_par = [&](int j) { return (uint32_t)(((j / kChunk) / kChunkSlots) & 1); };
 
     int k = 0;
     bool draining = true;
@@ -478,12 +444,36 @@ __global__ void __launch_bounds__(CompactShape<CW>::kThreads, 1)
         if (ctid == 0) vstore(&ctl->consumed_a, k);
         const unsigned tu = ctl->tile[k % kRing];
         if (tu == kSentinel) break;
-        pass1(k, s, tu);
         const int j = k - kLag;
-        if (j >= 0) {
-            if (!wait(B(ctl->b_full[j % kSB]), (j / kSB) & 1)) { draining = false; break; }
-            if (ctid == 0) vstore(&ctl->consumed_b, j);
-            if (!wait(B(ctl->pre[(j / kChunk) % kChunkSlots]), ((j / kChunk) / kChunkSlots) & 1)) { draining = false; break; }
+        if (j < 0) {
+            pass1(k, s, tu);
+            continue;
+        }
+        if (!wait(B(ctl->b_full[j % kSB]), (j / kSB) & 1)) { draining = false; break; }
+        if (ctid == 0) vstore(&ctl->consumed_b, j);
+        const unsigned tj = ctl->tile[j % kRing];
+        if ((long long)tu < n_full_tiles && (long long)tj < n_full_tiles) {
+            // the common case, both tiles full, in one instruction stream: pass
+            // 2's loads first, so that their latency hides behind pass 1's
+            // arithmetic; pass 1 never waits for a prefix, so this CTA's chunk
+            // aggregates (which other chunks' look-backs wait for) are not held up
+            uint4 v[kSteps];
+            uint2 r[kSteps];
+            p2_load(j, v);
+            p2_rows(j, r);
+            p1_publish(k, p1_flags(s));
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(B(ctl->wready[k % kR1]));
+                mbar_arrive(B(ctl->a_empty[s]));
+            }
+            if (!wait(pre_bar(j), pre_par(j))) { draining = false; break; }
+            p2_store(v, r, p2_out(j));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B(ctl->b_empty[j % kSB]));
+        } else {
+            pass1(k, s, tu);
+            if (!wait(pre_bar(j), pre_par(j))) { draining = false; break; }
             pass2(j);
         }
     }
@@ -491,10 +481,9 @@ __global__ void __launch_bounds__(CompactShape<CW>::kThreads, 1)
         for (int j = (k > kLag ? k - kLag : 0); j < k; ++j) {
             if (!wait(B(ctl->b_full[j % kSB]), (j / kSB) & 1)) break;
             if (ctid == 0) vstore(&ctl->consumed_b, j);
-            if (!wait(B(ctl->pre[(j / kChunk) % kChunkSlots]), ((j / kChunk) / kChunkSlots) & 1)) break;
+            if (!wait(pre_bar(j), pre_par(j))) break;
             pass2(j);
         }
-    if (lane == 0) bulk_wait_all();  // this warp's copies must finish before the CTA's shared memory is released
 }
 
 // ----------------------------------------------------------------- host side
@@ -517,13 +506,13 @@ cudaError_t launch_ct(const CompactParams& p, unsigned grid, cudaStream_t s) {
 int compact_tma_tile_elems() { return TILE; }
 int compact_tma_chunk_tiles() { return kChunk; }
 
-// shape 0: 16 compute warps (the default, fastest measured), shape 1: 8 compute warps
+// shape 0: 8 compute warps (the default, fastest measured), shape 1: 16 compute warps
 template <class T>
 cudaError_t launch_compact_tma(const CompactParams& p, bool wide_count, unsigned grid, cudaStream_t s, int shape) {
     if (shape == 0)
-        return wide_count ? launch_ct<T, OpCountU64, 16>(p, grid, s) : launch_ct<T, OpCountU32, 16>(p, grid, s);
-    if (shape == 1)
         return wide_count ? launch_ct<T, OpCountU64, 8>(p, grid, s) : launch_ct<T, OpCountU32, 8>(p, grid, s);
+    if (shape == 1)
+        return wide_count ? launch_ct<T, OpCountU64, 16>(p, grid, s) : launch_ct<T, OpCountU32, 16>(p, grid, s);
     return cudaErrorInvalidValue;
 }
 

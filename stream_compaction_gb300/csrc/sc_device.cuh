@@ -293,15 +293,17 @@ __device__ bool lookback_prefix(const LookbackCtl& lb, long long tile, typename 
 // once: the first window is 32 tiles (one status word per lane) and each
 // window that holds no inclusive prefix doubles the next one, up to
 // 32 * kMaxPer tiles.  Waits back off from 64 ns to 256 ns between polls.
-// Same contract as lookback_prefix.
-template <class Op, int kMaxPer>
+// Same contract as lookback_prefix.  The first window covers 32 * kFirstPer
+// predecessors.
+template <class Op, int kMaxPer, int kFirstPer = 1>
 __device__ bool lookback_prefix_adaptive(const LookbackCtl& lb, long long tile, typename Op::C& prefix,
                                          unsigned* windows_out = nullptr, unsigned* polls_out = nullptr) {
+    static_assert(kFirstPer >= 1 && kFirstPer <= kMaxPer, "first window");
     using C = typename Op::C;
     const int lane = threadIdx.x & 31;
     C acc = Op::c_identity();
     long long end = tile;
-    int per = 1;
+    int per = kFirstPer;
     unsigned long long t_start = 0;
     unsigned polls = 0;
     unsigned sleep_ns = 64;
