@@ -16,7 +16,6 @@ GPUs); timing is the max over ranks.
 from __future__ import annotations
 
 import argparse
-import glob
 import hashlib
 import json
 import os
@@ -48,6 +47,8 @@ def parse():
                     help="no timing: run the headline scan on the first N elements --steps times (for ncu)")
     ap.add_argument("--profile-op", default="scan", choices=["scan", "compact", "rows", "hier"],
                     help="which kernel --profile-case runs")
+    ap.add_argument("--compact-variant", type=int, default=0,
+                    help="compaction kernel for --profile-op compact (sc_set_compact_variant)")
     return ap.parse_args()
 
 
@@ -60,9 +61,13 @@ def peaks():
         return 6800.0, "fallback"
 
 
+# The sources the headline kernel (the persistent TMA scan) is compiled from.
+HEADLINE_SOURCES = ("sc_scan_tma.cu", "sc_persist.cuh", "sc_tma.cuh", "sc_device.cuh", "sc_params.h", "sc_launch.h")
+
+
 def kernel_sources_hash() -> str:
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "stream_compaction_gb300", "csrc", "*"))):
+    for p in sorted(os.path.join(ROOT, "stream_compaction_gb300", "csrc", f) for f in HEADLINE_SOURCES):
         with open(p, "rb") as f:
             h.update(os.path.basename(p).encode())
             h.update(f.read())
@@ -437,6 +442,8 @@ def profile_case(args):
         scbuild.build()
     sc.load()
     sc.sc_set_scan_variant(args.variant)
+    if sc.sc_set_compact_variant(args.compact_variant) != sc.SC_OK:
+        raise SystemExit("unknown compaction variant %d" % args.compact_variant)
     n = args.profile_case
     sp = int(torch.cuda.current_stream().cuda_stream)
     if args.profile_op == "compact":
