@@ -5,27 +5,35 @@
 // microseconds under full HBM load (each status probe is an L2 round trip of
 // about 1 us, and predecessors are often not yet published), which is most of
 // a one-tile-per-CTA kernel's lifetime; the CTA holds its registers the whole
-// time, so too few loads are in flight.  Here one CTA per SM keeps a ring of
+// time, so too few loads are in flight.  Here one CTA per SM keeps rings of
 // shared-memory stages filled by TMA and takes the look-back off the critical
 // path:
 //
-//   producer warp    tile ids from the atomic counter (requested several
-//                    tiles ahead) -> 2-D TMA loads (128-byte swizzle) into the
-//                    stage ring;
-//   look-back warps  start the look-back of a tile as soon as its id is
-//                    known (tiles round-robin over the warps), then publish
-//                    the tile's inclusive prefix and hand the exclusive prefix
+//   producer A       chunk ids (kChunk tiles each) from the atomic counter,
+//                    requested one chunk ahead -> 2-D TMA loads (128-byte
+//                    swizzle, L2 evict-last) of fresh tiles into ring A;
+//   compute warps    pass 1 of fresh tile k: each warp's total of its part,
+//                    the stage freed at once;
+//                    pass 2 of tile j = k - kLag, re-loaded from L2 into ring
+//                    B: serial register scan, warp shuffle scan, combine with
+//                    the earlier warps' totals and the tile's prefix, results
+//                    written back to the stage; both passes in one
+//                    instruction stream;
+//   bookkeeping      per tile: its total and its offset in the chunk; per
+//                    chunk: the aggregate, published for later look-backs;
+//   look-back warps  once a chunk's aggregate is published, its decoupled
+//                    look-back (chunks round-robin over the warps); publishes
+//                    the chunk's inclusive prefix and hands the exclusive one
 //                    to the compute warps;
-//   compute warps    pass 1 of tile k: serial register scan, warp shuffle
-//                    scan, block combine, tile-local results written back to
-//                    the stage, tile aggregate published at once;
-//                    pass 2 of tile k - kLag: prefix (+) local result, then a
-//                    TMA store of the stage.
+//   producer B       the pass-2 re-loads (L2 evict-first);
+//   store warps      TMA store of each finished stage (evict-first), then
+//                    the stage is freed.
 //
-// Each element is read from HBM once and written once.  Scan definitions as in
-// "Lecture 7: Parallel pattern -- prefix sum / scan" (UIUC ECE408 notes),
-// section 1; the single-kernel look-back is the alternative that section 6
-// of the same notes names for the hierarchical design.
+// Each element is read from HBM once (and once more from L2) and written once.
+// Scan definitions as in "Lecture 7: Parallel pattern -- prefix sum / scan"
+// (UIUC ECE408 notes), section 1; the single-kernel look-back is the
+// alternative that section 6 of the same notes names for the hierarchical
+// design.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
