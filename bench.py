@@ -252,8 +252,20 @@ def suite_lines(args, dev, sc, synth):
     y = torch.empty_like(x)
     n = x.numel()
     for ex, fn in ((0, sc.sc_scan_inclusive), (1, sc.sc_scan_exclusive)):
-        ms, b = timed(lambda: fn(sc.SC_I32, sc.SC_SUM, x.data_ptr(), y.data_ptr(), n, sp), 8 * n)
-        emit("int32_sum_n1048593_%s" % ("exclusive" if ex else "inclusive"), n, ms, b, {"l2": "flushed"})
+        call = lambda: fn(sc.SC_I32, sc.SC_SUM, x.data_ptr(), y.data_ptr(), n, sp)
+        name = "int32_sum_n1048593_%s" % ("exclusive" if ex else "inclusive")
+        ms, b = timed(call, 8 * n)
+        emit(name, n, ms, b, {"l2": "flushed, one launch between events (includes the launch latency)"})
+        # L2-warm: 200 launches back to back between two events
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(200):
+            call()
+        e1.record(s)
+        e1.synchronize()
+        emit(name, n, e0.elapsed_time(e1) / 200, 8 * n, {"l2": "warm, 200 launches back to back"})
     x = synth.make_torch(W["float32_exsum_n2^26"], device=dev)
     y = torch.empty_like(x)
     n = x.numel()

@@ -184,9 +184,10 @@ uint64_t sc_launch_count(void);
 /* ---- tuning and test hooks (process-wide; affect later launches) ---- */
 
 /* Select the kernel of the uint32/int32 sum.  0 (default): the persistent
- * TMA-pipelined kernel wherever it applies (16-byte aligned arrays of at least
- * one 16 KiB tile), else the one-tile-per-CTA kernel; v >= 1: one of the
- * precompiled one-tile-per-CTA shapes (see sc_scan_variant_info), kept for
+ * TMA-pipelined kernel wherever it applies (16-byte aligned arrays of more
+ * than 2^21 elements), else the one-tile-per-CTA kernel (for n <= 2^21 its
+ * shape of 16384-element tiles with 128-tile look-back windows, variant 10);
+ * v >= 1: one of the precompiled shapes (see sc_scan_variant_info), kept for
  * on-GPU comparison.  Returns SC_ERR_INVALID for an unknown variant. */
 sc_status sc_set_scan_variant(int variant);
 /* Select the fused-compaction kernel: 0 (default) the persistent TMA kernel

@@ -35,6 +35,13 @@ constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 // 1 .. N the one-tile-per-CTA shapes (shape v - 1), N + 1 the instrumented TMA
 // kernel, N + 1 + c (c >= 1) the persistent kernel in shape c.
 constexpr int kTmaStatsVariant = scg::kNumSumU32Variants + 1;
+// Up to this many elements the default path is the one-tile-per-CTA kernel:
+// measured on GB300, the persistent kernel's pipeline start-up (about 9 us)
+// costs more than a short scan, and the one-tile kernel with 128-tile look-back
+// windows (uint32-sum shape kSmallShape) finishes n = 2^20 in about 2/3 of the
+// persistent kernel's time; the two are level near 2^22.
+constexpr int64_t kSmallScanMax = int64_t(1) << 21;
+constexpr int kSmallShape = 9;  // 16384-element tiles, 512 threads, 128-tile windows
 int max_variant() { return kTmaStatsVariant + scg::tma_num_cfgs() - 1; }
 // Persistent-kernel shape of a public variant, or -1 for the one-tile-per-CTA kernel.
 int tma_cfg_of(int v) {
@@ -209,9 +216,10 @@ cudaError_t dispatch_scan_tma(int oid, const ScanParams& p, bool excl, unsigned 
 
 // One single-pass scan launch (plain or segmented), with optional carries.
 // Public variant 0 is the persistent TMA kernel where it applies (16-byte
-// aligned, unsegmented, at least one full tile); every other case, and public
-// variants v >= 1 of the uint32 sum, use the one-tile-per-CTA kernel (shape
-// v - 1; shape 0 by default).
+// aligned, unsegmented, more than kSmallScanMax elements); every other case,
+// and public variants v >= 1 of the uint32 sum, use the one-tile-per-CTA
+// kernel (shape v - 1; by default shape 0, or kSmallShape for short uint32
+// sums).
 sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_len, bool excl,
                    const void* carry_in, void* carry_out, cudaStream_t s) {
     const int api_variant = (oid == 0 && seg_len == 0) ? g_variant.load() : 0;
@@ -222,9 +230,11 @@ sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_le
     if (cfg >= 0) scg::tma_shape(cfg, &sh);
     const int64_t tma_tile = cfg >= 0 ? sh.tile_bytes / eb : 0;
     const bool tma_stats = api_variant == kTmaStatsVariant;
-    const bool use_tma = cfg >= 0 && seg_len == 0 && vec_ok && n >= tma_tile &&
+    const bool small = api_variant == 0 && n <= kSmallScanMax;
+    const bool use_tma = cfg >= 0 && !small && seg_len == 0 && vec_ok && n >= tma_tile &&
                          n / tma_tile * (sh.tile_bytes / 128) < (int64_t)INT_MAX && num_sms() > 0;
-    const int legacy_variant = (cfg >= 0 || api_variant == 0) ? 0 : api_variant - 1;
+    const int legacy_variant = (small && oid == 0 && seg_len == 0) ? kSmallShape
+                               : (cfg >= 0 || api_variant == 0) ? 0 : api_variant - 1;
     // units of the look-back: chunks of the persistent kernel, tiles otherwise
     const int64_t tile = use_tma ? tma_tile * sh.chunk_tiles : scg::scan_tile_elems(oid, legacy_variant);
     const unsigned ntiles = (unsigned)ceil_div(n, tile);
