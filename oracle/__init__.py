@@ -30,6 +30,23 @@ _lib = None
 
 PRED = {"gt": 0, "ge": 1, "lt": 2, "le": 3, "eq": 4, "ne": 5}
 
+# (op, numpy dtype) -> (C function, dtype the bits are passed as): the
+# operators whose result has the input's type.
+_U32, _U64 = np.dtype(np.uint32), np.dtype(np.uint64)
+_GENERIC = {}
+for _op in ("prod", "and", "or", "xor"):
+    for _dt in (np.int32, np.uint32):
+        _GENERIC[(_op, np.dtype(_dt))] = "oracle_scan_%s_u32" % _op
+    for _dt in (np.int64, np.uint64):
+        _GENERIC[(_op, np.dtype(_dt))] = "oracle_scan_%s_u64" % _op
+for _dt in (np.int64, np.uint64):
+    _GENERIC[("sum", np.dtype(_dt))] = "oracle_scan_sum_u64"
+for _op in ("max", "min"):
+    for _dt, _sfx in ((np.uint32, "u32"), (np.int64, "i64"), (np.uint64, "u64"),
+                      (np.float32, "f32"), (np.float64, "f64")):
+        _GENERIC[(_op, np.dtype(_dt))] = "oracle_scan_%s_%s" % (_op, _sfx)
+_GENERIC[("min", np.dtype(np.int32))] = "oracle_scan_min_i32"
+
 
 def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
     """Compile oracle.c into a shared library with gcc (-O2, no fast-math)."""
@@ -55,12 +72,22 @@ def load_library(path: str) -> ctypes.CDLL:
         f = getattr(lib, name)
         f.argtypes = [P, P, I64, I64, INT]
         f.restype = None
+    for name in _GENERIC.values():
+        f = getattr(lib, name)
+        f.argtypes = [P, P, I64, INT]
+        f.restype = None
+    for name in ("oracle_scan_sum_f64", "oracle_scan_maxcount_i32"):
+        f = getattr(lib, name)
+        f.argtypes = [P, P, I64, INT]
+        f.restype = None
     for name in ("oracle_compact_i32", "oracle_compact_u32", "oracle_compact_f32"):
         f = getattr(lib, name)
         f.argtypes = [P, I64, INT, D, P]
         f.restype = I64
-    lib.oracle_abs_prefix_f32.argtypes = [P, P, I64]
-    lib.oracle_abs_prefix_f32.restype = None
+    for name in ("oracle_abs_prefix_f32", "oracle_abs_prefix_f64"):
+        f = getattr(lib, name)
+        f.argtypes = [P, P, I64]
+        f.restype = None
     return lib
 
 
@@ -86,8 +113,12 @@ class Oracle:
     def scan(self, x: np.ndarray, op: str, exclusive: bool) -> np.ndarray:
         """Inclusive or exclusive scan of a 1-D array.
 
-        op: "sum" (int32/uint32 -> same dtype, wraps mod 2^32; float32 -> float64),
-            "max" (int32), "affine" (uint32 array of shape (n, 2): rows (a, b)).
+        op: "sum" (int32/uint32/int64/uint64 -> same dtype, wrapping; float32 ->
+            float64; float64 -> float64, compensated), "max" / "min" (int32,
+            uint32, int64, uint64, float32, float64; floats propagate NaN),
+            "prod" / "and" / "or" / "xor" (the four integer dtypes, wrapping),
+            "affine" (uint32 array of shape (n, 2): rows (a, b)), "maxcount"
+            (int32/uint32 array of shape (n, 2): rows (value, count)).
         """
         ex = 1 if exclusive else 0
         if op == "sum" and x.dtype in (np.int32, np.uint32):
@@ -109,6 +140,22 @@ class Oracle:
             xs = np.ascontiguousarray(x)
             y = np.empty_like(xs)
             self.c.oracle_scan_affine_u32(_ptr(xs), _ptr(y), xs.shape[0], ex)
+            return y
+        if op == "sum" and x.dtype == np.float64:
+            xs = np.ascontiguousarray(x)
+            y = np.empty_like(xs)
+            self.c.oracle_scan_sum_f64(_ptr(xs), _ptr(y), xs.size, ex)
+            return y
+        if op == "maxcount" and x.dtype in (np.int32, np.uint32) and x.ndim == 2 and x.shape[1] == 2:
+            xs = np.ascontiguousarray(x).view(np.uint32)
+            y = np.empty_like(xs)
+            self.c.oracle_scan_maxcount_i32(_ptr(xs), _ptr(y), xs.shape[0], ex)
+            return y.view(x.dtype)
+        name = _GENERIC.get((op, x.dtype))
+        if name is not None and x.ndim == 1:
+            xs = np.ascontiguousarray(x)
+            y = np.empty_like(xs)
+            getattr(self.c, name)(_ptr(xs), _ptr(y), xs.size, ex)
             return y
         raise ValueError("unsupported oracle scan: op=%s dtype=%s shape=%s" % (op, x.dtype, x.shape))
 
@@ -136,7 +183,12 @@ class Oracle:
             y = np.empty_like(xs)
             self.c.oracle_scan_batched_affine_u32(_ptr(xs), _ptr(y), rows, cols, ex)
             return y
-        raise ValueError("unsupported oracle batched scan: op=%s dtype=%s" % (op, x.dtype))
+        # every other operator (its result has the input's type): the 1-D
+        # oracle on each row
+        xs = np.ascontiguousarray(x)
+        if rows == 0:
+            return np.empty_like(xs)
+        return np.stack([self.scan(xs[r], op, exclusive) for r in range(rows)])
 
     # -- compaction ----------------------------------------------------------
     def compact(self, x: np.ndarray, pred: str, threshold: float):
@@ -152,7 +204,12 @@ class Oracle:
         return out[:cnt].copy(), int(cnt)
 
     def abs_prefix(self, x: np.ndarray) -> np.ndarray:
-        """s[i] = |x[0]| + ... + |x[i]| in fp64 (scale of the float32 tolerance)."""
+        """s[i] = |x[0]| + ... + |x[i]| in fp64 (scale of the float tolerances)."""
+        if x.dtype == np.float64:
+            xs = np.ascontiguousarray(x)
+            s = np.empty(xs.size, dtype=np.float64)
+            self.c.oracle_abs_prefix_f64(_ptr(xs), _ptr(s), xs.size)
+            return s
         xs = np.ascontiguousarray(x, dtype=np.float32)
         s = np.empty(xs.size, dtype=np.float64)
         self.c.oracle_abs_prefix_f32(_ptr(xs), _ptr(s), xs.size)

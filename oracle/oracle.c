@@ -22,6 +22,11 @@
  *  [PMPP] "Chapter 9 Parallel Patterns: Prefix Sum - Scan Algorithms"
  *        (bittern.cn), section 9.1 (definition, identity table) and section
  *        9.6 "Applications of Scan" (filtering).
+ *  [L7] section 1 also lists the operators a scan accepts besides addition:
+ *        multiplication, min, max, bitwise and/or, and a user-defined
+ *        (maximum, number of occurrences) compound operator; [PMPP] 9.1's
+ *        identity table gives 1 for multiplication, -infinity for max and
+ *        +infinity for min.
  *
  * Readings where the pages leave a step open:
  *  - integer sums wrap modulo 2^32 (both int32 and uint32 are summed as
@@ -34,7 +39,22 @@
  *  - float32 inputs are accumulated in fp64 (the CPU references in [L7]'s
  *    programs accumulate in double);
  *  - the compaction predicate is "x <op> threshold" evaluated in double
- *    ([PMPP] 4.2 marks input[i] > threshold; [L7] section 2 keeps x > 0).
+ *    ([PMPP] 4.2 marks input[i] > threshold; [L7] section 2 keeps x > 0);
+ *  - integer products, and, or, xor and the 64-bit sums are taken on the
+ *    unsigned bits (wraparound modulo 2^32 or 2^64, identical bits for the
+ *    signed types); xor (identity 0) is added to the listed and/or;
+ *  - the infinities of the identity table are the extreme values of the
+ *    integer type (max: its minimum, min: its maximum), and -inf / +inf for
+ *    floats; float max and min propagate NaN (once a NaN has been seen the
+ *    running value is NaN, as numpy's maximum/minimum do; this keeps -inf and
+ *    +inf two-sided identities) and keep the earlier of two equal values (so
+ *    -0.0 and +0.0 stay as they came);
+ *  - float64 sums are accumulated with a running compensation term
+ *    (Neumaier's variant of Kahan summation), so the oracle is more accurate
+ *    than any fp64 scan it checks;
+ *  - the (maximum, count) element is the pair (v, c) of an int32 value and a
+ *    uint32 count; (v1,c1) (+) (v2,c2) is the pair with the larger value, the
+ *    counts added when the values are equal; identity (INT32_MIN, 0).
  */
 #include <stdint.h>
 #include <math.h>
@@ -114,6 +134,129 @@ void oracle_scan_affine_u32(const uint32_t *x, uint32_t *y, int64_t n, int exclu
             y[2 * i] = acc_a;
             y[2 * i + 1] = acc_b;
         }
+    }
+}
+
+/* ---- more operators and element types ([L7] s.1 operator list; [PMPP] 9.1
+ *      identity table).  One left-to-right loop each, as above. ---- */
+
+static uint32_t prod_u32(uint32_t acc, uint32_t x) { return acc * x; }
+static uint32_t and_u32(uint32_t acc, uint32_t x) { return acc & x; }
+static uint32_t or_u32(uint32_t acc, uint32_t x) { return acc | x; }
+static uint32_t xor_u32(uint32_t acc, uint32_t x) { return acc ^ x; }
+static int32_t min_i32(int32_t acc, int32_t x) { return x < acc ? x : acc; }
+static uint32_t max_u32(uint32_t acc, uint32_t x) { return x > acc ? x : acc; }
+static uint32_t min_u32(uint32_t acc, uint32_t x) { return x < acc ? x : acc; }
+
+static uint64_t sum_u64(uint64_t acc, uint64_t x) { return acc + x; }
+static uint64_t prod_u64(uint64_t acc, uint64_t x) { return acc * x; }
+static uint64_t and_u64(uint64_t acc, uint64_t x) { return acc & x; }
+static uint64_t or_u64(uint64_t acc, uint64_t x) { return acc | x; }
+static uint64_t xor_u64(uint64_t acc, uint64_t x) { return acc ^ x; }
+static int64_t max_i64(int64_t acc, int64_t x) { return x > acc ? x : acc; }
+static int64_t min_i64(int64_t acc, int64_t x) { return x < acc ? x : acc; }
+static uint64_t max_u64(uint64_t acc, uint64_t x) { return x > acc ? x : acc; }
+static uint64_t min_u64(uint64_t acc, uint64_t x) { return x < acc ? x : acc; }
+
+/* A NaN operand gives NaN (the earlier NaN if both are); of two equal values
+ * the earlier (acc) is kept. */
+static float max_f32(float acc, float x) { if (isnan(acc)) return acc; if (isnan(x)) return x; return x > acc ? x : acc; }
+static float min_f32(float acc, float x) { if (isnan(acc)) return acc; if (isnan(x)) return x; return x < acc ? x : acc; }
+static double max_f64(double acc, double x) { if (isnan(acc)) return acc; if (isnan(x)) return x; return x > acc ? x : acc; }
+static double min_f64(double acc, double x) { if (isnan(acc)) return acc; if (isnan(x)) return x; return x < acc ? x : acc; }
+
+/* The loop of every scan above, for one (name, type, identity, operator). */
+#define ORACLE_SCAN(NAME, T, IDENT, OP)                                    \
+    void oracle_scan_##NAME(const T *x, T *y, int64_t n, int exclusive)    \
+    {                                                                      \
+        T acc = (IDENT);                                                   \
+        for (int64_t i = 0; i < n; ++i) {                                  \
+            if (exclusive) {                                               \
+                y[i] = acc;                                                \
+                acc = OP(acc, x[i]);                                       \
+            } else {                                                       \
+                acc = OP(acc, x[i]);                                       \
+                y[i] = acc;                                                \
+            }                                                              \
+        }                                                                  \
+    }
+
+ORACLE_SCAN(prod_u32, uint32_t, 1u, prod_u32)
+ORACLE_SCAN(and_u32, uint32_t, 0xFFFFFFFFu, and_u32)
+ORACLE_SCAN(or_u32, uint32_t, 0u, or_u32)
+ORACLE_SCAN(xor_u32, uint32_t, 0u, xor_u32)
+ORACLE_SCAN(min_i32, int32_t, INT32_MAX, min_i32)
+ORACLE_SCAN(max_u32, uint32_t, 0u, max_u32)
+ORACLE_SCAN(min_u32, uint32_t, 0xFFFFFFFFu, min_u32)
+ORACLE_SCAN(sum_u64, uint64_t, 0u, sum_u64)
+ORACLE_SCAN(prod_u64, uint64_t, 1u, prod_u64)
+ORACLE_SCAN(and_u64, uint64_t, 0xFFFFFFFFFFFFFFFFull, and_u64)
+ORACLE_SCAN(or_u64, uint64_t, 0u, or_u64)
+ORACLE_SCAN(xor_u64, uint64_t, 0u, xor_u64)
+ORACLE_SCAN(max_i64, int64_t, INT64_MIN, max_i64)
+ORACLE_SCAN(min_i64, int64_t, INT64_MAX, min_i64)
+ORACLE_SCAN(max_u64, uint64_t, 0u, max_u64)
+ORACLE_SCAN(min_u64, uint64_t, 0xFFFFFFFFFFFFFFFFull, min_u64)
+ORACLE_SCAN(max_f32, float, -INFINITY, max_f32)
+ORACLE_SCAN(min_f32, float, INFINITY, min_f32)
+ORACLE_SCAN(max_f64, double, -INFINITY, max_f64)
+ORACLE_SCAN(min_f64, double, INFINITY, min_f64)
+
+/* float64 sum: the running sum s and a compensation c holding the low-order
+ * part that s lost; the prefix reported is s + c. */
+void oracle_scan_sum_f64(const double *x, double *y, int64_t n, int exclusive)
+{
+    double s = 0.0, c = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        if (exclusive)
+            y[i] = s + c;
+        const double t = s + x[i];
+        if (fabs(s) >= fabs(x[i]))
+            c += (s - t) + x[i];
+        else
+            c += (x[i] - t) + s;
+        s = t;
+        if (!exclusive)
+            y[i] = s + c;
+    }
+}
+
+/* (maximum, count): x and y hold n interleaved pairs, x[2i] = value (int32
+ * bits), x[2i+1] = count. */
+static void maxcount(int32_t *acc_v, uint32_t *acc_c, int32_t v, uint32_t c)
+{
+    if (v > *acc_v) {
+        *acc_v = v;
+        *acc_c = c;
+    } else if (v == *acc_v) {
+        *acc_c = *acc_c + c;
+    }
+}
+
+void oracle_scan_maxcount_i32(const uint32_t *x, uint32_t *y, int64_t n, int exclusive)
+{
+    int32_t acc_v = INT32_MIN;
+    uint32_t acc_c = 0u;
+    for (int64_t i = 0; i < n; ++i) {
+        if (exclusive) {
+            y[2 * i] = (uint32_t)acc_v;
+            y[2 * i + 1] = acc_c;
+            maxcount(&acc_v, &acc_c, (int32_t)x[2 * i], x[2 * i + 1]);
+        } else {
+            maxcount(&acc_v, &acc_c, (int32_t)x[2 * i], x[2 * i + 1]);
+            y[2 * i] = (uint32_t)acc_v;
+            y[2 * i + 1] = acc_c;
+        }
+    }
+}
+
+/* the float64 tolerance's scale: s[i] = |x[0]| + ... + |x[i]| */
+void oracle_abs_prefix_f64(const double *x, double *s, int64_t n)
+{
+    double acc = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        acc = acc + fabs(x[i]);
+        s[i] = acc;
     }
 }
 

@@ -11,10 +11,12 @@ AssertionError if it disagrees with:
   * library routines that compute the same thing a different way
     (numpy.cumsum with uint32 wraparound, numpy.maximum.accumulate, boolean
     mask selection, math.fsum);
-  * brute force over every input of length <= 8 on small alphabets, against a
-    divide-and-conquer fold (a different association order than the oracle's
-    left-to-right loop) or, for affine maps, against applying the maps one
-    after another to a point.
+  * brute force over every input of length <= 8 (<= 5 or 6 for the added
+    operators) on small alphabets, against a divide-and-conquer fold (a
+    different association order than the oracle's left-to-right loop) or, for
+    affine maps, against applying the maps one after another to a point, and
+    for (max, count) pairs against the definition (largest value, total count
+    of its occurrences).
 
 The same functions run against deliberately broken copies of the oracle
 (tests/test_oracle_mutants.py) to show that each plausible mistake is caught.
@@ -345,9 +347,224 @@ def pin_brute_force_compaction(o):
                     assert out.tolist() == want and cnt == len(want), (row.tolist(), pred, thr)
 
 
+# ------------------------------------- more operators and element types
+M64 = 1 << 64
+INT64_MIN = -(1 << 63)
+INT64_MAX = (1 << 63) - 1
+
+
+def _fmax_first(p, q):
+    """max propagating NaN, the earlier of equal values kept (vectorised)."""
+    return np.where(np.isnan(p), p, np.where(np.isnan(q), q, np.where(q > p, q, p)))
+
+
+def _fmin_first(p, q):
+    return np.where(np.isnan(p), p, np.where(np.isnan(q), q, np.where(q < p, q, p)))
+
+
+def _same_float(a, b):
+    """Equal bit for bit, or both NaN."""
+    a, b = np.asarray(a), np.asarray(b)
+    bits = np.uint32 if a.dtype == np.float32 else np.uint64
+    return bool(np.all((a.view(bits) == b.view(bits)) | (np.isnan(a) & np.isnan(b))))
+
+
+def pin_golden_identities_more(o):
+    g = load_golden("pmpp_ch9_identities.txt")
+    for dt in (np.int32, np.uint32, np.int64, np.uint64):
+        x = np.array([5, 7, 2], dtype=dt)
+        assert int(o.scan(x, "prod", True)[0]) == g["prod"][0], dt
+        assert int(o.scan(x, "or", True)[0]) == g["or"][0], dt
+        assert int(o.scan(x, "xor", True)[0]) == 0, dt
+    assert int(o.scan(np.array([5, 7], np.int32), "min", True)[0]) == g["min_i32"][0]
+    assert int(o.scan(np.array([5, 7], np.uint32), "and", True)[0]) == g["and_u32"][0]
+    assert int(o.scan(np.array([5, 7], np.uint64), "and", True)[0]) == M64 - 1
+    assert int(o.scan(np.array([5, 7], np.int32), "and", True)[0]) == -1
+    # the integer infinities are the extremes of each type
+    for dt, lo, hi in ((np.uint32, 0, M32 - 1), (np.int64, INT64_MIN, INT64_MAX), (np.uint64, 0, M64 - 1)):
+        x = np.array([5, 7], dtype=dt)
+        assert int(o.scan(x, "max", True)[0]) == lo and int(o.scan(x, "min", True)[0]) == hi, dt
+    for dt in (np.float32, np.float64):
+        x = np.array([2.5, -1.0], dtype=dt)
+        assert o.scan(x, "max", True)[0] == float(g["max_float"][0])
+        assert o.scan(x, "min", True)[0] == float(g["min_float"][0])
+    assert float(o.scan(np.array([2.5], np.float64), "sum", True)[0]) == float(g["sum"][0])
+    yv = o.scan(np.array([[5, 1], [6, 2]], dtype=np.int32), "maxcount", True)
+    assert yv[0].tolist() == [g["max_i32"][0], 0]
+    for op, x in (("prod", np.zeros(0, np.uint64)), ("min", np.zeros(0, np.float64)),
+                  ("sum", np.zeros(0, np.float64)), ("maxcount", np.zeros((0, 2), np.int32))):
+        assert o.scan(x, op, True).shape[0] == 0 and o.scan(x, op, False).shape[0] == 0
+
+
+def pin_closed_forms_more(o):
+    for n in (1, 2, 5, 33, 70, 1000):
+        i = np.arange(n, dtype=np.int64)
+        # prod of all 3s: 3^(i+1) modulo 2^32 and 2^64
+        p32 = [pow(3, k + 1, M32) for k in range(n)]
+        p64 = [pow(3, k + 1, M64) for k in range(n)]
+        assert o.scan(np.full(n, 3, np.uint32), "prod", False).tolist() == p32
+        assert o.scan(np.full(n, 3, np.uint64), "prod", False).tolist() == p64
+        # prod of 1..n: the factorials modulo 2^64
+        fact, f = [], 1
+        for k in range(1, n + 1):
+            f = f * k % M64
+            fact.append(f)
+        assert o.scan(np.arange(1, n + 1, dtype=np.uint64), "prod", False).tolist() == fact
+        # or of 1 << (i mod 32): 2^(i+1) - 1 until all 32 bits are set
+        x = (np.uint64(1) << (i % 32).astype(np.uint64)).astype(np.uint32)
+        want = [min((1 << (k + 1)) - 1, M32 - 1) for k in range(n)]
+        assert o.scan(x, "or", False).tolist() == want
+        # and of all-ones-but-bit (i mod 32): bits 0..i cleared
+        assert o.scan(~x, "and", False).tolist() == [(M32 - 1) ^ w for w in want]
+        # xor of 0..i: i, 1, i+1, 0 by i mod 4
+        xr = [(k, 1, k + 1, 0)[k % 4] for k in range(n)]
+        assert o.scan(i.astype(np.uint32), "xor", False).tolist() == xr
+        assert o.scan(i.astype(np.uint64), "xor", False).tolist() == xr
+        # 64-bit sums: x[i] = i -> i(i+1)/2; all ones-complement -> -(i+1) mod 2^64
+        assert o.scan(i.astype(np.uint64), "sum", False).tolist() == [k * (k + 1) // 2 for k in range(n)]
+        assert o.scan(np.full(n, M64 - 1, np.uint64), "sum", False).tolist() == [(M64 - k - 1) % M64
+                                                                                    for k in range(n)]
+        assert o.scan(np.full(n, -1, np.int64), "sum", True).tolist() == [-k for k in range(n)]
+        # min over descending input is the input, over ascending it is x[0]
+        for dt in (np.int32, np.uint32, np.int64, np.uint64, np.float32, np.float64):
+            asc = np.arange(n).astype(dt)
+            assert np.array_equal(o.scan(asc[::-1].copy(), "min", False), asc[::-1])
+            assert np.array_equal(o.scan(asc, "min", False), np.zeros(n, dt))
+            assert np.array_equal(o.scan(asc, "max", False), asc)
+        # float64 sum of ones: the exact integers
+        assert o.scan(np.ones(n), "sum", True).tolist() == [float(k) for k in range(n)]
+        # (max, count) of equal values counts them; of rising values keeps count 1
+        eq = np.stack([np.full(n, 7, np.int32), np.ones(n, np.int32)], axis=1)
+        assert o.scan(eq, "maxcount", False).tolist() == [[7, k + 1] for k in range(n)]
+        up = np.stack([np.arange(n, dtype=np.int32), np.ones(n, np.int32)], axis=1)
+        assert o.scan(up, "maxcount", False).tolist() == [[k, 1] for k in range(n)]
+
+
+def _more_inputs():
+    rng = np.random.default_rng(2024)
+    n = 20011
+    u32 = rng.integers(0, M32, n, dtype=np.uint64).astype(np.uint32)
+    u64 = rng.integers(0, M64, n, dtype=np.uint64)
+    f64 = rng.uniform(-1, 1, n) * 10.0 ** rng.integers(-8, 8, n)
+    return {"u32": u32, "i32": u32.view(np.int32), "u64": u64, "i64": u64.view(np.int64),
+            "f32": rng.uniform(-3, 3, n).astype(np.float32), "f64": f64}
+
+
+def pin_library_special_cases_more(o):
+    d = _more_inputs()
+    for key in ("u32", "i32", "u64", "i64"):
+        x = d[key]
+        dt = x.dtype
+        assert np.array_equal(o.scan(x, "max", False), np.maximum.accumulate(x)), key
+        assert np.array_equal(o.scan(x, "min", False), np.minimum.accumulate(x)), key
+        assert np.array_equal(o.scan(x, "and", False), np.bitwise_and.accumulate(x)), key
+        assert np.array_equal(o.scan(x, "or", False), np.bitwise_or.accumulate(x)), key
+        assert np.array_equal(o.scan(x, "xor", False), np.bitwise_xor.accumulate(x)), key
+        assert np.array_equal(o.scan(x, "prod", False), np.cumprod(x, dtype=dt)), key
+        if dt.itemsize == 8:
+            assert np.array_equal(o.scan(x, "sum", False), np.cumsum(x, dtype=dt)), key
+    for key in ("f32", "f64"):
+        x = d[key].copy()
+        x[[3, 700, 701, 9000]] = np.nan
+        lo = np.array([-np.inf], dtype=x.dtype)
+        hi = np.array([np.inf], dtype=x.dtype)
+        assert _same_float(o.scan(x, "max", False), np.maximum.accumulate(np.concatenate([lo, x]))[1:]), key
+        assert _same_float(o.scan(x, "min", False), np.minimum.accumulate(np.concatenate([hi, x]))[1:]), key
+        assert np.isnan(o.scan(x, "max", False)[3:]).all() and not np.isnan(o.scan(x, "max", False)[:3]).any()
+    # (max, count) with unit counts: the running max and how often it has occurred so far
+    v = (d["u32"] % np.uint32(50)).astype(np.int32)
+    y = o.scan(np.stack([v, np.ones_like(v)], axis=1), "maxcount", False)
+    run = np.maximum.accumulate(v)
+    assert np.array_equal(y[:, 0], run)
+    for i in range(0, v.size, 613):
+        assert int(y[i, 1]) == int(np.count_nonzero(v[:i + 1] == run[i])), i
+
+
+def pin_float64_sum(o):
+    """The float64 sum is within a few units in the last place of the exactly
+    rounded prefix sum (math.fsum), far inside the fp64 scan error bound."""
+    x = _more_inputs()["f64"][:4000]
+    xs = x.tolist()
+    y, ye = o.scan(x, "sum", False), o.scan(x, "sum", True)
+    s = o.abs_prefix(x)
+    for i in range(0, x.size, 5):
+        exact = math.fsum(xs[:i + 1])
+        assert abs(y[i] - exact) <= 4 * 2.0 ** -53 * abs(exact) + 1e-28 * s[i], i
+        assert abs(ye[i] - math.fsum(xs[:i])) <= 4 * 2.0 ** -53 * abs(math.fsum(xs[:i])) + 1e-28 * s[i], i
+        assert abs(s[i] - math.fsum(abs(v) for v in xs[:i + 1])) <= (i + 1) * 2.0 ** -53 * s[i]
+    # cancellation that a plain running fp64 sum gets wrong
+    z = o.scan(np.array([1.0, 1e100, 1.0, -1e100]), "sum", False)
+    assert z[-1] == 2.0
+
+
+def _brute_scan_bits(o, alphabet, op_name, op, identity, max_len=5, floats=False):
+    """Like _brute_scan, with outputs compared bit for bit (floats: NaN = NaN)."""
+    for length in range(0, max_len + 1):
+        seqs = _all_sequences(alphabet, length)
+        for ex in (False, True):
+            if length == 0:
+                assert o.scan(seqs[0], op_name, ex).size == 0
+                continue
+            got = o.scan_batched(seqs, op_name, ex)
+            cols = [seqs[:, j] for j in range(length)]
+            for i in range(length):
+                pre = cols[:i] if ex else cols[:i + 1]
+                want = _dc_fold(pre, op, identity)
+                want = np.broadcast_to(np.asarray(want, dtype=seqs.dtype), (seqs.shape[0],))
+                if floats:
+                    assert _same_float(got[:, i], want), (op_name, length, ex, i)
+                else:
+                    assert np.array_equal(got[:, i], want), (op_name, length, ex, i)
+
+
+def pin_brute_force_more(o):
+    with np.errstate(over="ignore"):
+        u32 = np.array([0, 1, 2, 0x80000000, 0xFFFFFFFF], dtype=np.uint32)
+        u64 = np.array([0, 1, 3, 1 << 63, M64 - 1], dtype=np.uint64)
+        for alphabet in (u32, u64):
+            dt = alphabet.dtype
+            ones = np.array(np.iinfo(dt).max, dtype=dt)
+            _brute_scan_bits(o, alphabet, "prod", lambda p, q: (p * q).astype(dt), np.array(1, dt))
+            _brute_scan_bits(o, alphabet, "and", lambda p, q: p & q, ones)
+            _brute_scan_bits(o, alphabet, "or", lambda p, q: p | q, np.array(0, dt))
+            _brute_scan_bits(o, alphabet, "xor", lambda p, q: p ^ q, np.array(0, dt))
+            _brute_scan_bits(o, alphabet, "max", np.maximum, np.array(0, dt))
+            _brute_scan_bits(o, alphabet, "min", np.minimum, ones)
+            if dt == np.uint64:
+                _brute_scan_bits(o, alphabet, "sum", lambda p, q: (p + q).astype(dt), np.array(0, dt))
+        for alphabet in (u32.view(np.int32), u64.view(np.int64)):
+            dt = alphabet.dtype
+            info = np.iinfo(dt)
+            _brute_scan_bits(o, alphabet, "max", np.maximum, np.array(info.min, dt))
+            _brute_scan_bits(o, alphabet, "min", np.minimum, np.array(info.max, dt))
+        for dt in (np.float32, np.float64):
+            fl = np.array([np.nan, -np.inf, -0.0, 0.0, 1.5, np.inf], dtype=dt)
+            _brute_scan_bits(o, fl, "max", _fmax_first, np.array(-np.inf, dt), floats=True)
+            _brute_scan_bits(o, fl, "min", _fmin_first, np.array(np.inf, dt), floats=True)
+    # (max, count) pairs: every sequence of <= 6 pairs from a 4-pair alphabet
+    alphabet = np.array([[1 << 31, 1], [0, 1], [0, 2], [5, 0xFFFFFFFF]], dtype=np.uint32)  # value bits: INT32_MIN, 0, 0, 5
+    for length in range(1, 7):
+        seqs = alphabet[_all_sequences(np.arange(4), length)]          # (k, length, 2)
+        for ex in (False, True):
+            got = o.scan_batched(seqs, "maxcount", ex)
+            v = seqs[:, :, 0].view(np.int32).astype(np.int64)
+            c = seqs[:, :, 1].astype(np.int64)
+            for i in range(length):
+                m = i if ex else i + 1
+                if m == 0:
+                    wv, wc = np.full(seqs.shape[0], INT32_MIN), np.zeros(seqs.shape[0], np.int64)
+                else:
+                    wv = v[:, :m].max(axis=1)
+                    wc = np.where(v[:, :m] == wv[:, None], c[:, :m], 0).sum(axis=1) % M32
+                assert np.array_equal(got[:, i, 0].view(np.int32).astype(np.int64), wv), (length, ex, i)
+                assert np.array_equal(got[:, i, 1].astype(np.int64), wc), (length, ex, i)
+
+
 ALL_PINS = [
     pin_golden_sum_examples, pin_golden_compaction_examples, pin_golden_identities,
     pin_closed_forms, pin_affine_special_cases, pin_invariants, pin_affine_recurrence,
     pin_library_special_cases, pin_float_fp64_accumulation, pin_batched_rows,
     pin_brute_force_sum, pin_brute_force_max, pin_brute_force_affine, pin_brute_force_compaction,
+    pin_golden_identities_more, pin_closed_forms_more, pin_library_special_cases_more, pin_float64_sum,
+    pin_brute_force_more,
 ]

@@ -36,6 +36,29 @@ MUTANTS = {
                            "        oracle_scan_sum_u32(x + r * cols, y + r * cols, cols - (cols > 1), exclusive);"),
     # abs prefix without the absolute value
     "abs_prefix_signed": ("        acc = acc + fabs((double)x[i]);", "        acc = acc + (double)x[i];"),
+    # wrong identity for int32 min
+    "min_identity_zero": ("ORACLE_SCAN(min_i32, int32_t, INT32_MAX, min_i32)", "ORACLE_SCAN(min_i32, int32_t, 0, min_i32)"),
+    # wrong identity for the 64-bit product
+    "prod_identity_zero": ("ORACLE_SCAN(prod_u64, uint64_t, 1u, prod_u64)", "ORACLE_SCAN(prod_u64, uint64_t, 0u, prod_u64)"),
+    # xor written as or
+    "xor_is_or": ("static uint32_t xor_u32(uint32_t acc, uint32_t x) { return acc ^ x; }",
+                  "static uint32_t xor_u32(uint32_t acc, uint32_t x) { return acc | x; }"),
+    # unsigned max compared as signed
+    "max_u32_signed": ("static uint32_t max_u32(uint32_t acc, uint32_t x) { return x > acc ? x : acc; }",
+                       "static uint32_t max_u32(uint32_t acc, uint32_t x) { return (int32_t)x > (int32_t)acc ? x : acc; }"),
+    # 64-bit sum truncated to 32 bits
+    "sum_u64_truncated": ("static uint64_t sum_u64(uint64_t acc, uint64_t x) { return acc + x; }",
+                          "static uint64_t sum_u64(uint64_t acc, uint64_t x) { return (uint32_t)(acc + x); }"),
+    # float64 sum without its compensation term
+    "f64_sum_uncompensated": ("        if (!exclusive)\n            y[i] = s + c;", "        if (!exclusive)\n            y[i] = s;"),
+    # float max that ignores NaN instead of propagating it
+    "fmax_ignores_nan": ("static float max_f32(float acc, float x) { if (isnan(acc)) return acc; if (isnan(x)) return x;",
+                         "static float max_f32(float acc, float x) { if (isnan(acc)) return x; if (isnan(x)) return acc;"),
+    # float min keeping the later of two equal values
+    "fmin_tie_later": ("static double min_f64(double acc, double x) { if (isnan(acc)) return acc; if (isnan(x)) return x; return x < acc ? x : acc; }",
+                       "static double min_f64(double acc, double x) { if (isnan(acc)) return acc; if (isnan(x)) return x; return x <= acc ? x : acc; }"),
+    # (max, count): equal values do not add their counts
+    "maxcount_ties_not_added": ("        *acc_c = *acc_c + c;", "        *acc_c = c;"),
 }
 
 
@@ -50,10 +73,11 @@ def test_pins_catch_mutant(name, tmp_path):
         f.write(mutated)
     so = oracle.build(force=True, src=csrc, out=os.path.join(str(tmp_path), "liboracle_mut.so"))
     mut = oracle.Oracle(oracle.load_library(so))
-    caught = []
+    caught = None
     for pin in ALL_PINS:
         try:
             pin(mut)
         except AssertionError:
-            caught.append(pin.__name__)
+            caught = pin.__name__
+            break
     assert caught, "no pin caught mutant " + name
