@@ -34,12 +34,39 @@
  *                                        (the earlier map is applied first;
  *                                        identity (1, 0)); y[i] applied to h0
  *                                        gives the recurrence h_i = a_i*h_{i-1} + b_i.
+ *   The other operators the Lecture 7 notes (section 1) list for a scan, with
+ *   the identities of the PMPP notes' table (section 9.1):
+ *   (SC_I32 | SC_U32 | SC_I64 | SC_U64, SC_PROD)   product modulo 2^32 / 2^64,
+ *                                        identity 1;
+ *   (same types, SC_AND | SC_OR | SC_XOR)  bitwise, identities all ones / 0 / 0
+ *                                        (xor is not on the list; it is added);
+ *   (SC_I64 | SC_U64, SC_SUM)           sum modulo 2^64;
+ *   (SC_I32 | SC_U32 | SC_I64 | SC_U64, SC_MAX | SC_MIN)  in the type's own
+ *                                        order, identity the type's smallest /
+ *                                        largest value;
+ *   (SC_F32 | SC_F64, SC_MAX | SC_MIN)  identity -inf / +inf; a NaN element
+ *                                        makes every later output NaN; of two
+ *                                        equal values the earlier is kept, so
+ *                                        -0.0 and +0.0 come out as they went in;
+ *                                        exact (bit for bit);
+ *   (SC_F64, SC_SUM)                    float64 sum, within
+ *                                        (16 * ceil(n/2048) + 64) * 2^-53 *
+ *                                        sum_{k<=i} |x[k]| of the exact prefix
+ *                                        (at most 16 roundings per look-back
+ *                                        hop, one hop per tile of >= 2048
+ *                                        elements, < 64 inside a tile);
+ *   (SC_MAXCOUNT_I32, SC_MAX)           element (v, c): (v1,c1) (+) (v2,c2) is
+ *                                        the pair with the larger value, the
+ *                                        counts added (mod 2^32) when the values
+ *                                        are equal; identity (INT32_MIN, 0) --
+ *                                        the notes' "(maximum, number of
+ *                                        occurrences)" compound operator.
  *
  * Conventions for every call below.
  *   - Pointers named d_* / in / out are DEVICE pointers owned by the caller
  *     (e.g. torch tensors).  Elements are contiguous.  4-byte types need
- *     4-byte alignment, affine pairs 8-byte alignment; 16-byte aligned in/out
- *     take the vectorised path.
+ *     4-byte alignment, 8-byte types and pairs 8-byte alignment; 16-byte
+ *     aligned in/out take the vectorised path.
  *   - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t;
  *     NULL is the legacy default stream).  They never synchronise the host and
  *     never allocate in steady state: the first call on a (device, stream)
@@ -67,8 +94,17 @@ extern "C" {
 /* Same type as cudaStream_t; declared here so this header needs no CUDA header. */
 typedef struct CUstream_st *sc_stream_t;
 
-typedef enum { SC_I32 = 0, SC_U32 = 1, SC_F32 = 2, SC_AFFINE_U32 = 3 } sc_dtype;
-typedef enum { SC_SUM = 0, SC_MAX = 1, SC_COMPOSE = 2 } sc_op;
+typedef enum {
+    SC_I32 = 0, SC_U32 = 1, SC_F32 = 2,
+    SC_AFFINE_U32 = 3,   /* uint32 pairs (a, b), 8 bytes: the map h -> a*h + b */
+    SC_I64 = 4, SC_U64 = 5, SC_F64 = 6,
+    SC_MAXCOUNT_I32 = 7  /* pairs (int32 value, uint32 count), 8 bytes */
+} sc_dtype;
+typedef enum {
+    SC_SUM = 0, SC_MAX = 1,
+    SC_COMPOSE = 2,      /* SC_AFFINE_U32 only */
+    SC_MIN = 3, SC_PROD = 4, SC_AND = 5, SC_OR = 6, SC_XOR = 7
+} sc_op;
 /* Compaction predicate "x <pred> threshold", evaluated as if in double
  * precision (every int32, uint32 and float32 value is exact in double). */
 typedef enum { SC_GT = 0, SC_GE = 1, SC_LT = 2, SC_LE = 3, SC_EQ = 4, SC_NE = 5 } sc_pred;
@@ -126,7 +162,10 @@ sc_status sc_compact_if(sc_dtype dtype, const void *in, void *out, int64_t *d_co
  * total; scan the totals, recursively; add each tile's offset back), restated
  * for sm_103a.  Same results as the single-pass scan (float32: within the same
  * bound), about twice the memory traffic.  A comparison variant: it needs
- * extra workspace for the per-level totals (sc_hier_workspace_bytes). */
+ * extra workspace for the per-level totals (sc_hier_workspace_bytes), and it
+ * covers the int32/uint32 sum, float32 sum, int32 max and affine composition
+ * only (SC_ERR_UNSUPPORTED otherwise; sc_hier_workspace_bytes returns 0 for
+ * other dtypes). */
 sc_status sc_scan_hierarchical(sc_dtype dtype, sc_op op, int exclusive, const void *in, void *out,
                                int64_t n, sc_stream_t stream);
 size_t sc_hier_workspace_bytes(sc_dtype dtype, int64_t n);
@@ -145,8 +184,9 @@ sc_status sc_scan_host(sc_dtype dtype, sc_op op, int exclusive, const void *h_in
 /* ---- scan without any allocation ----
  *
  * sc_scan_noalloc computes exactly what sc_scan_inclusive (exclusive == 0) or
- * sc_scan_exclusive (exclusive != 0) compute, with the same dtypes, operators
- * and aliasing rules, but it never allocates device memory.  The pages have no
+ * sc_scan_exclusive (exclusive != 0) compute, for the int32/uint32 sum, float32
+ * sum, int32 max and affine composition (other operators: SC_ERR_UNSUPPORTED),
+ * with the same aliasing rules, but it never allocates device memory.  The pages have no
  * counterpart to this entry point; it exists for callers that cannot call
  * cudaMalloc: code running where the device allocator is unavailable or must
  * not be touched (inside another framework's memory pool, in an allocator's

@@ -23,8 +23,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libsc_gb300.so")
 
 # enums of include/sc_scan.h
-SC_I32, SC_U32, SC_F32, SC_AFFINE_U32 = 0, 1, 2, 3
-SC_SUM, SC_MAX, SC_COMPOSE = 0, 1, 2
+SC_I32, SC_U32, SC_F32, SC_AFFINE_U32, SC_I64, SC_U64, SC_F64, SC_MAXCOUNT_I32 = 0, 1, 2, 3, 4, 5, 6, 7
+SC_SUM, SC_MAX, SC_COMPOSE, SC_MIN, SC_PROD, SC_AND, SC_OR, SC_XOR = 0, 1, 2, 3, 4, 5, 6, 7
 SC_GT, SC_GE, SC_LT, SC_LE, SC_EQ, SC_NE = 0, 1, 2, 3, 4, 5
 SC_OK, SC_ERR_INVALID, SC_ERR_UNSUPPORTED, SC_ERR_WORKSPACE, SC_ERR_CUDA, SC_ERR_LOOKBACK_TIMEOUT = range(6)
 
@@ -183,19 +183,27 @@ def _stream(stream=None) -> int:
     return int(s.cuda_stream)
 
 
+_PAIR_OPS = {"affine": SC_AFFINE_U32, "maxcount": SC_MAXCOUNT_I32}
+
+
 def _dtype_code(x, op: str) -> int:
     import torch
-    if op == "affine":
+    if op in _PAIR_OPS:
         if x.dtype not in (torch.int32, torch.uint32) or x.dim() < 1 or x.shape[-1] != 2:
-            raise ValueError("affine scan expects an int32/uint32 tensor of shape (..., 2) holding (a, b)")
-        return SC_AFFINE_U32
-    m = {torch.int32: SC_I32, torch.uint32: SC_U32, torch.float32: SC_F32}
+            raise ValueError("%s scan expects an int32/uint32 tensor of shape (..., 2)" % op)
+        return _PAIR_OPS[op]
+    m = {torch.int32: SC_I32, torch.float32: SC_F32, torch.int64: SC_I64, torch.float64: SC_F64}
+    for name, code in (("uint32", SC_U32), ("uint64", SC_U64)):
+        if hasattr(torch, name):
+            m[getattr(torch, name)] = code
     if x.dtype not in m:
         raise ValueError("unsupported dtype %s" % x.dtype)
     return m[x.dtype]
 
 
-_OPS = {"sum": SC_SUM, "max": SC_MAX, "affine": SC_COMPOSE}
+# affine: (a, b) pairs composed; maxcount: (value, count) pairs (SC_MAXCOUNT_I32 with SC_MAX)
+_OPS = {"sum": SC_SUM, "max": SC_MAX, "min": SC_MIN, "prod": SC_PROD, "and": SC_AND, "or": SC_OR, "xor": SC_XOR,
+        "affine": SC_COMPOSE, "maxcount": SC_MAX}
 
 
 def _prep(x, out, op):
@@ -208,12 +216,15 @@ def _prep(x, out, op):
         out = torch.empty_like(x)
     if out.shape != x.shape or out.dtype != x.dtype or not out.is_contiguous():
         raise ValueError("out must be a contiguous tensor like x")
-    n = x.numel() // 2 if op == "affine" else x.numel()
+    n = x.numel() // 2 if op in _PAIR_OPS else x.numel()
     return out, n
 
 
 def scan_inclusive(x, op: str = "sum", out=None, stream=None):
-    """Inclusive scan of a 1-D CUDA tensor (affine: shape (n, 2))."""
+    """Inclusive scan of a 1-D CUDA tensor (affine, maxcount: shape (n, 2)).
+
+    op: sum, max, min, prod, and, or, xor, affine, maxcount (see include/sc_scan.h
+    for the dtypes each takes)."""
     out, n = _prep(x, out, op)
     _check(sc_scan_inclusive(_dtype_code(x, op), _OPS[op], x.data_ptr(), out.data_ptr(), n, _stream(stream)),
            "sc_scan_inclusive")
@@ -221,7 +232,7 @@ def scan_inclusive(x, op: str = "sum", out=None, stream=None):
 
 
 def scan_exclusive(x, op: str = "sum", out=None, stream=None):
-    """Exclusive scan of a 1-D CUDA tensor (affine: shape (n, 2))."""
+    """Exclusive scan of a 1-D CUDA tensor (affine, maxcount: shape (n, 2))."""
     out, n = _prep(x, out, op)
     _check(sc_scan_exclusive(_dtype_code(x, op), _OPS[op], x.data_ptr(), out.data_ptr(), n, _stream(stream)),
            "sc_scan_exclusive")
@@ -229,7 +240,7 @@ def scan_exclusive(x, op: str = "sum", out=None, stream=None):
 
 
 def scan_batched(x, op: str = "sum", exclusive: bool = True, out=None, stream=None):
-    """Row-wise scans of a row-major (rows, cols) CUDA tensor ((rows, cols, 2) for affine)."""
+    """Row-wise scans of a row-major (rows, cols) CUDA tensor ((rows, cols, 2) for the pair ops)."""
     out, _ = _prep(x, out, op)
     rows, cols = x.shape[0], x.shape[1]
     _check(sc_scan_batched(_dtype_code(x, op), _OPS[op], int(exclusive), x.data_ptr(), out.data_ptr(), rows, cols,
@@ -266,7 +277,7 @@ def scan_host(x, op: str = "sum", exclusive: bool = True, out=None, stream=None)
         raise ValueError("scan_host expects a contiguous CPU tensor")
     if out is None:
         out = torch.empty_like(x, pin_memory=x.is_pinned())
-    n = x.numel() // 2 if op == "affine" else x.numel()
+    n = x.numel() // 2 if op in _PAIR_OPS else x.numel()
     _check(sc_scan_host(_dtype_code(x, op), _OPS[op], int(exclusive), x.data_ptr(), out.data_ptr(), n,
                         _stream(stream)), "sc_scan_host")
     return out

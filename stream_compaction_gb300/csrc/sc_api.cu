@@ -141,21 +141,49 @@ sc_status finish_launch(Workspace& ws, unsigned num_tiles, cudaError_t e) {
 int elem_bytes(sc_dtype d) {
     switch (d) {
     case SC_I32: case SC_U32: case SC_F32: return 4;
-    case SC_AFFINE_U32: return 8;
+    case SC_AFFINE_U32: case SC_I64: case SC_U64: case SC_F64: case SC_MAXCOUNT_I32: return 8;
     default: return 0;
     }
 }
 
-bool valid_dtype(int d) { return d >= SC_I32 && d <= SC_AFFINE_U32; }
-bool valid_op(int o) { return o >= SC_SUM && o <= SC_COMPOSE; }
+bool valid_dtype(int d) { return d >= SC_I32 && d <= SC_MAXCOUNT_I32; }
+bool valid_op(int o) { return o >= SC_SUM && o <= SC_XOR; }
 
-// 0 sum u32/i32, 1 sum f32, 2 max i32, 3 affine; -1 unsupported.
+// The operator id (scg::ScanOpId) of a (dtype, op) pair; -1 unsupported.
 int op_id(sc_dtype d, sc_op o) {
-    if (o == SC_SUM && (d == SC_I32 || d == SC_U32)) return 0;
-    if (o == SC_SUM && d == SC_F32) return 1;
-    if (o == SC_MAX && d == SC_I32) return 2;
-    if (o == SC_COMPOSE && d == SC_AFFINE_U32) return 3;
-    return -1;
+    using namespace scg;
+    const bool i32 = d == SC_I32 || d == SC_U32, i64 = d == SC_I64 || d == SC_U64;
+    switch (o) {
+    case SC_SUM:
+        return i32 ? OID_SUM_U32 : i64 ? OID_SUM_U64 : d == SC_F32 ? OID_SUM_F32 : d == SC_F64 ? OID_SUM_F64 : -1;
+    case SC_PROD: return i32 ? OID_PROD_U32 : i64 ? OID_PROD_U64 : -1;
+    case SC_AND: return i32 ? OID_AND_U32 : i64 ? OID_AND_U64 : -1;
+    case SC_OR: return i32 ? OID_OR_U32 : i64 ? OID_OR_U64 : -1;
+    case SC_XOR: return i32 ? OID_XOR_U32 : i64 ? OID_XOR_U64 : -1;
+    case SC_MAX:
+        switch (d) {
+        case SC_I32: return OID_MAX_I32;
+        case SC_U32: return OID_MAX_U32;
+        case SC_I64: return OID_MAX_I64;
+        case SC_U64: return OID_MAX_U64;
+        case SC_F32: return OID_MAX_F32;
+        case SC_F64: return OID_MAX_F64;
+        case SC_MAXCOUNT_I32: return OID_MAXCOUNT_I32;
+        default: return -1;
+        }
+    case SC_MIN:
+        switch (d) {
+        case SC_I32: return OID_MIN_I32;
+        case SC_U32: return OID_MIN_U32;
+        case SC_I64: return OID_MIN_I64;
+        case SC_U64: return OID_MIN_U64;
+        case SC_F32: return OID_MIN_F32;
+        case SC_F64: return OID_MIN_F64;
+        default: return -1;
+        }
+    case SC_COMPOSE: return d == SC_AFFINE_U32 ? OID_AFFINE_U32 : -1;
+    default: return -1;
+    }
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -182,6 +210,8 @@ sc_status check_scan_args(sc_dtype dtype, sc_op op, const void* in, void* out, i
 }
 
 cudaError_t dispatch_scan(int oid, const ScanParams& p, bool excl, bool seg, int variant, cudaStream_t s) {
+    if (oid >= scg::kFirstExtraOid) return variant == 0 ? scg::launch_scan_extra(oid, p, excl, seg, 0, s)
+                                                        : cudaErrorInvalidValue;
     switch (oid) {
     case 0: return scg::launch_scan<scg::OpSumU32>(p, excl, seg, variant, s);
     case 1: return scg::launch_scan<scg::OpSumF32>(p, excl, seg, variant, s);
@@ -205,6 +235,8 @@ int num_sms() {
 
 cudaError_t dispatch_scan_tma(int oid, const ScanParams& p, bool excl, unsigned grid, cudaStream_t s, bool stats,
                               int cfg) {
+    if (oid >= scg::kFirstExtraOid) return (cfg == 0 && !stats) ? scg::launch_scan_extra(oid, p, excl, false, grid, s)
+                                                                : cudaErrorInvalidValue;
     switch (oid) {
     case 0: return scg::launch_scan_tma<scg::OpSumU32>(p, excl, grid, s, stats, cfg);
     case 1: return scg::launch_scan_tma<scg::OpSumF32>(p, excl, grid, s, false, 0);
@@ -224,7 +256,7 @@ sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_le
                    const void* carry_in, void* carry_out, cudaStream_t s) {
     const int api_variant = (oid == 0 && seg_len == 0) ? g_variant.load() : 0;
     const bool vec_ok = aligned(in, 16) && aligned(out, 16);
-    const int eb = oid == 3 ? 8 : 4;
+    const int eb = scg::oid_elem_bytes(oid);
     const int cfg = tma_cfg_of(api_variant);
     scg::TmaShape sh{0, 0, 0, 0};
     if (cfg >= 0) scg::tma_shape(cfg, &sh);
@@ -494,6 +526,7 @@ sc_status sc_compact_if(sc_dtype dtype, const void* in, void* out, int64_t* d_co
 
 size_t sc_hier_workspace_bytes(sc_dtype dtype, int64_t n) {
     if (!valid_dtype(dtype) || n <= 0) return 0;
+    if (dtype != SC_I32 && dtype != SC_U32 && dtype != SC_F32 && dtype != SC_AFFINE_U32) return 0;
     const int oid = dtype == SC_AFFINE_U32 ? 3 : 0;
     const int64_t t = scg::hier_tile_elems(oid);
     size_t total = 0;
@@ -556,7 +589,9 @@ sc_status sc_scan_hierarchical(sc_dtype dtype, sc_op op, int exclusive, const vo
                                sc_stream_t stream) {
     int oid = -1;
     sc_status st = check_scan_args(dtype, op, in, out, n, &oid);
-    if (st != SC_OK || n == 0) return st;
+    if (st != SC_OK) return st;
+    if (oid >= scg::kFirstExtraOid) return SC_ERR_UNSUPPORTED;
+    if (n == 0) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const size_t need = kStatusOffset + sc_hier_workspace_bytes(dtype, n);
     std::lock_guard<std::mutex> lk(g_ws_mu);
@@ -725,7 +760,28 @@ ScanShape scan_shape(int op_id, int variant) {
     case 1: return variant == 0 ? kShapeSumF32 : ScanShape{0, 0, 0};
     case 2: return variant == 0 ? kShapeMaxI32 : ScanShape{0, 0, 0};
     case 3: return variant == 0 ? kShapeAffine : ScanShape{0, 0, 0};
-    default: return ScanShape{0, 0, 0};
+    default:
+        if (op_id < kFirstExtraOid || op_id >= OID_COUNT || variant != 0) return ScanShape{0, 0, 0};
+        return oid_elem_bytes(op_id) == 8 ? kShapeExtra8 : kShapeExtra4;
+    }
+}
+
+cudaError_t launch_scan_extra(int oid, const ScanParams& p, bool exclusive, bool segmented, unsigned tma_grid,
+                              cudaStream_t s) {
+    switch (oid) {
+    case OID_PROD_U32: case OID_AND_U32: case OID_OR_U32: case OID_XOR_U32:
+        return launch_ops_int32_bits(oid, p, exclusive, segmented, tma_grid, s);
+    case OID_MIN_I32: case OID_MAX_U32: case OID_MIN_U32:
+        return launch_ops_int32_order(oid, p, exclusive, segmented, tma_grid, s);
+    case OID_SUM_U64: case OID_PROD_U64: case OID_AND_U64: case OID_OR_U64: case OID_XOR_U64:
+        return launch_ops_int64_bits(oid, p, exclusive, segmented, tma_grid, s);
+    case OID_MAX_I64: case OID_MIN_I64: case OID_MAX_U64: case OID_MIN_U64:
+        return launch_ops_int64_order(oid, p, exclusive, segmented, tma_grid, s);
+    case OID_MAX_F32: case OID_MIN_F32: case OID_SUM_F64:
+        return launch_ops_float_a(oid, p, exclusive, segmented, tma_grid, s);
+    case OID_MAX_F64: case OID_MIN_F64: case OID_MAXCOUNT_I32:
+        return launch_ops_float_b(oid, p, exclusive, segmented, tma_grid, s);
+    default: return cudaErrorInvalidValue;
     }
 }
 }  // namespace scg

@@ -66,6 +66,132 @@ struct OpAffineU32 {
     __device__ __forceinline__ static T lower(C c) { return c; }
 };
 
+// ---- more operators ("Lecture 7" notes, section 1, operator list; PMPP
+// notes, section 9.1, identity table).  Integer operators act on the
+// unsigned bits (wraparound); max/min compare in the value's own type.
+
+// Identity-preserving helpers for the generic operators below.
+template <class V> struct Extremes;
+template <> struct Extremes<int32_t> {
+    __device__ __forceinline__ static int32_t lowest() { return INT32_MIN; }
+    __device__ __forceinline__ static int32_t highest() { return INT32_MAX; }
+};
+template <> struct Extremes<uint32_t> {
+    __device__ __forceinline__ static uint32_t lowest() { return 0u; }
+    __device__ __forceinline__ static uint32_t highest() { return 0xffffffffu; }
+};
+template <> struct Extremes<long long> {
+    __device__ __forceinline__ static long long lowest() { return (long long)0x8000000000000000ull; }
+    __device__ __forceinline__ static long long highest() { return 0x7fffffffffffffffll; }
+};
+template <> struct Extremes<unsigned long long> {
+    __device__ __forceinline__ static unsigned long long lowest() { return 0ull; }
+    __device__ __forceinline__ static unsigned long long highest() { return ~0ull; }
+};
+template <> struct Extremes<float> {
+    __device__ __forceinline__ static float lowest() { return __int_as_float(0xff800000); }   // -inf
+    __device__ __forceinline__ static float highest() { return __int_as_float(0x7f800000); }  // +inf
+};
+template <> struct Extremes<double> {
+    __device__ __forceinline__ static double lowest() { return __longlong_as_double((long long)0xfff0000000000000ull); }
+    __device__ __forceinline__ static double highest() { return __longlong_as_double(0x7ff0000000000000ll); }
+};
+
+// An operator whose carry has the element's type.
+template <class V, class Self>
+struct SameCarry {
+    using T = V;
+    using C = V;
+    __device__ __forceinline__ static C c_identity() { return Self::identity(); }
+    __device__ __forceinline__ static C c_op(C a, C b) { return Self::op(a, b); }
+    __device__ __forceinline__ static C lift(T a) { return a; }
+    __device__ __forceinline__ static T lower(C c) { return c; }
+};
+
+template <class V>
+struct OpAddWrap : SameCarry<V, OpAddWrap<V>> {
+    __device__ __forceinline__ static V identity() { return V(0); }
+    __device__ __forceinline__ static V op(V a, V b) { return a + b; }
+};
+template <class V>
+struct OpMulWrap : SameCarry<V, OpMulWrap<V>> {
+    __device__ __forceinline__ static V identity() { return V(1); }
+    __device__ __forceinline__ static V op(V a, V b) { return a * b; }
+};
+template <class V>
+struct OpAndBits : SameCarry<V, OpAndBits<V>> {
+    __device__ __forceinline__ static V identity() { return ~V(0); }
+    __device__ __forceinline__ static V op(V a, V b) { return a & b; }
+};
+template <class V>
+struct OpOrBits : SameCarry<V, OpOrBits<V>> {
+    __device__ __forceinline__ static V identity() { return V(0); }
+    __device__ __forceinline__ static V op(V a, V b) { return a | b; }
+};
+template <class V>
+struct OpXorBits : SameCarry<V, OpXorBits<V>> {
+    __device__ __forceinline__ static V identity() { return V(0); }
+    __device__ __forceinline__ static V op(V a, V b) { return a ^ b; }
+};
+// max / min keeping the earlier of two equal values
+template <class V>
+struct OpMaxOf : SameCarry<V, OpMaxOf<V>> {
+    __device__ __forceinline__ static V identity() { return Extremes<V>::lowest(); }
+    __device__ __forceinline__ static V op(V a, V b) { return b > a ? b : a; }
+};
+template <class V>
+struct OpMinOf : SameCarry<V, OpMinOf<V>> {
+    __device__ __forceinline__ static V identity() { return Extremes<V>::highest(); }
+    __device__ __forceinline__ static V op(V a, V b) { return b < a ? b : a; }
+};
+// Float max / min: NaN propagates (the earlier NaN wins), so -inf / +inf are
+// two-sided identities; of two equal values the earlier is kept (-0.0 and
+// +0.0 stay as they came).
+template <class V>
+struct OpMaxNaN : SameCarry<V, OpMaxNaN<V>> {
+    __device__ __forceinline__ static V identity() { return Extremes<V>::lowest(); }
+    __device__ __forceinline__ static V op(V a, V b) { return (a != a) ? a : (b != b) ? b : (b > a ? b : a); }
+};
+template <class V>
+struct OpMinNaN : SameCarry<V, OpMinNaN<V>> {
+    __device__ __forceinline__ static V identity() { return Extremes<V>::highest(); }
+    __device__ __forceinline__ static V op(V a, V b) { return (a != a) ? a : (b != b) ? b : (b < a ? b : a); }
+};
+struct OpSumF64 : SameCarry<double, OpSumF64> {
+    __device__ __forceinline__ static double identity() { return 0.0; }
+    __device__ __forceinline__ static double op(double a, double b) { return __dadd_rn(a, b); }
+};
+// (maximum, count) pairs stored as uint2 {x = int32 value bits, y = count}:
+// the pair with the larger value; equal values add their counts (mod 2^32).
+struct OpMaxCount : SameCarry<uint2, OpMaxCount> {
+    __device__ __forceinline__ static uint2 identity() { return make_uint2(0x80000000u, 0u); }
+    __device__ __forceinline__ static uint2 op(uint2 a, uint2 b) {
+        const int va = (int)a.x, vb = (int)b.x;
+        return vb > va ? b : (vb == va ? make_uint2(a.x, a.y + b.y) : a);
+    }
+};
+
+using OpProdU32 = OpMulWrap<uint32_t>;
+using OpAndU32 = OpAndBits<uint32_t>;
+using OpOrU32 = OpOrBits<uint32_t>;
+using OpXorU32 = OpXorBits<uint32_t>;
+using OpMinI32 = OpMinOf<int32_t>;
+using OpMaxU32 = OpMaxOf<uint32_t>;
+using OpMinU32 = OpMinOf<uint32_t>;
+using OpSumU64 = OpAddWrap<unsigned long long>;
+using OpProdU64 = OpMulWrap<unsigned long long>;
+using OpAndU64 = OpAndBits<unsigned long long>;
+using OpOrU64 = OpOrBits<unsigned long long>;
+using OpXorU64 = OpXorBits<unsigned long long>;
+using OpMaxI64 = OpMaxOf<long long>;
+using OpMinI64 = OpMinOf<long long>;
+using OpMaxU64 = OpMaxOf<unsigned long long>;
+using OpMinU64 = OpMinOf<unsigned long long>;
+using OpMaxF32 = OpMaxNaN<float>;
+using OpMinF32 = OpMinNaN<float>;
+using OpMaxF64 = OpMaxNaN<double>;
+using OpMinF64 = OpMinNaN<double>;
+
 // Counts for the fused compaction.
 struct OpCountU32 {
     using T = uint32_t;
@@ -100,9 +226,11 @@ __device__ __forceinline__ void from_bits32(uint32_t b, float& v) { v = __uint_a
 __device__ __forceinline__ unsigned long long to_bits64(double v) { return (unsigned long long)__double_as_longlong(v); }
 __device__ __forceinline__ unsigned long long to_bits64(uint2 v) { return ((unsigned long long)v.y << 32) | v.x; }
 __device__ __forceinline__ unsigned long long to_bits64(unsigned long long v) { return v; }
+__device__ __forceinline__ unsigned long long to_bits64(long long v) { return (unsigned long long)v; }
 __device__ __forceinline__ void from_bits64(unsigned long long b, double& v) { v = __longlong_as_double((long long)b); }
 __device__ __forceinline__ void from_bits64(unsigned long long b, uint2& v) { v = make_uint2((uint32_t)b, (uint32_t)(b >> 32)); }
 __device__ __forceinline__ void from_bits64(unsigned long long b, unsigned long long& v) { v = b; }
+__device__ __forceinline__ void from_bits64(unsigned long long b, long long& v) { v = (long long)b; }
 
 // Warp shuffles for 4- and 8-byte value types.
 template <class V>
@@ -381,6 +509,15 @@ __device__ __forceinline__ void unpack(const uint4& r, float* v) {
     v[0] = __uint_as_float(r.x); v[1] = __uint_as_float(r.y); v[2] = __uint_as_float(r.z); v[3] = __uint_as_float(r.w);
 }
 __device__ __forceinline__ void unpack(const uint4& r, uint2* v) { v[0] = make_uint2(r.x, r.y); v[1] = make_uint2(r.z, r.w); }
+__device__ __forceinline__ void unpack(const uint4& r, unsigned long long* v) {
+    v[0] = ((unsigned long long)r.y << 32) | r.x; v[1] = ((unsigned long long)r.w << 32) | r.z;
+}
+__device__ __forceinline__ void unpack(const uint4& r, long long* v) {
+    v[0] = (long long)(((unsigned long long)r.y << 32) | r.x); v[1] = (long long)(((unsigned long long)r.w << 32) | r.z);
+}
+__device__ __forceinline__ void unpack(const uint4& r, double* v) {
+    v[0] = __hiloint2double((int)r.y, (int)r.x); v[1] = __hiloint2double((int)r.w, (int)r.z);
+}
 
 __device__ __forceinline__ uint4 pack(const uint32_t* v) { return make_uint4(v[0], v[1], v[2], v[3]); }
 __device__ __forceinline__ uint4 pack(const int32_t* v) { return make_uint4((uint32_t)v[0], (uint32_t)v[1], (uint32_t)v[2], (uint32_t)v[3]); }
@@ -388,6 +525,14 @@ __device__ __forceinline__ uint4 pack(const float* v) {
     return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
 }
 __device__ __forceinline__ uint4 pack(const uint2* v) { return make_uint4(v[0].x, v[0].y, v[1].x, v[1].y); }
+__device__ __forceinline__ uint4 pack(const unsigned long long* v) {
+    return make_uint4((uint32_t)v[0], (uint32_t)(v[0] >> 32), (uint32_t)v[1], (uint32_t)(v[1] >> 32));
+}
+__device__ __forceinline__ uint4 pack(const long long* v) { return pack(reinterpret_cast<const unsigned long long*>(v)); }
+__device__ __forceinline__ uint4 pack(const double* v) {
+    return make_uint4((uint32_t)__double2loint(v[0]), (uint32_t)__double2hiint(v[0]), (uint32_t)__double2loint(v[1]),
+                      (uint32_t)__double2hiint(v[1]));
+}
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
     uint4 r;

@@ -34,10 +34,43 @@ struct ScanShape {
 
 constexpr int kNumSumU32Variants = 15;
 
-// Tile size (elements) of operator `op_id` (0 sum u32, 1 sum f32, 2 max i32,
-// 3 affine) in the given variant; 0 if that variant does not exist.
+// Operator ids: one per (element type, operator) pair with distinct bits.
+// int32 and uint32 share the sum, product and bitwise operators (the same
+// bits), as do int64 and uint64.
+enum ScanOpId : int {
+    OID_SUM_U32 = 0, OID_SUM_F32 = 1, OID_MAX_I32 = 2, OID_AFFINE_U32 = 3,
+    // the rest run through launch_scan_extra
+    OID_PROD_U32 = 4, OID_AND_U32, OID_OR_U32, OID_XOR_U32, OID_MIN_I32, OID_MAX_U32, OID_MIN_U32,
+    OID_SUM_U64, OID_PROD_U64, OID_AND_U64, OID_OR_U64, OID_XOR_U64, OID_MAX_I64, OID_MIN_I64, OID_MAX_U64,
+    OID_MIN_U64, OID_MAX_F32, OID_MIN_F32, OID_SUM_F64, OID_MAX_F64, OID_MIN_F64, OID_MAXCOUNT_I32,
+    OID_COUNT
+};
+constexpr int kFirstExtraOid = OID_PROD_U32;
+
+// Element bytes of an operator id (4, or 8 for 64-bit types and pairs).
+constexpr int oid_elem_bytes(int oid) {
+    return (oid == OID_AFFINE_U32 || oid == OID_MAXCOUNT_I32 || (oid >= OID_SUM_U64 && oid <= OID_MIN_U64) ||
+            oid == OID_SUM_F64 || oid == OID_MAX_F64 || oid == OID_MIN_F64)
+               ? 8
+               : 4;
+}
+
+// Tile size (elements) of operator `op_id` in the given variant; 0 if that
+// variant does not exist.
 int scan_tile_elems(int op_id, int variant);
 ScanShape scan_shape(int op_id, int variant);
+
+// Scans of the operators from kFirstExtraOid on: the one-tile-per-CTA kernel
+// (tma_grid == 0; plain or segmented) or the persistent kernel (shape 0) on
+// tma_grid CTAs.  One translation unit per group of operators (sc_ops_*.cu).
+cudaError_t launch_scan_extra(int oid, const ScanParams& p, bool exclusive, bool segmented, unsigned tma_grid,
+                              cudaStream_t s);
+cudaError_t launch_ops_int32_bits(int oid, const ScanParams&, bool, bool, unsigned, cudaStream_t);
+cudaError_t launch_ops_int32_order(int oid, const ScanParams&, bool, bool, unsigned, cudaStream_t);
+cudaError_t launch_ops_int64_bits(int oid, const ScanParams&, bool, bool, unsigned, cudaStream_t);
+cudaError_t launch_ops_int64_order(int oid, const ScanParams&, bool, bool, unsigned, cudaStream_t);
+cudaError_t launch_ops_float_a(int oid, const ScanParams&, bool, bool, unsigned, cudaStream_t);
+cudaError_t launch_ops_float_b(int oid, const ScanParams&, bool, bool, unsigned, cudaStream_t);
 
 template <class Op>
 cudaError_t launch_scan(const ScanParams& p, bool exclusive, bool segmented, int variant, cudaStream_t s);

@@ -76,7 +76,7 @@ int op_index(sc_dtype d, sc_op o) {
 
 extern "C" sc_status sc_scan_noalloc(sc_dtype dtype, sc_op op, int exclusive, const void* in, void* out, int64_t n,
                                      sc_stream_t stream) {
-    if (dtype < SC_I32 || dtype > SC_AFFINE_U32 || op < SC_SUM || op > SC_COMPOSE || n < 0) return SC_ERR_INVALID;
+    if (dtype < SC_I32 || dtype > SC_MAXCOUNT_I32 || op < SC_SUM || op > SC_XOR || n < 0) return SC_ERR_INVALID;
     const int oid = op_index(dtype, op);
     if (oid < 0) return SC_ERR_UNSUPPORTED;
     if (n == 0) return SC_OK;

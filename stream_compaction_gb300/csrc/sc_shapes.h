@@ -28,5 +28,8 @@ constexpr ScanShape kShapeSumU32[kNumSumU32Variants] = {
 constexpr ScanShape kShapeSumF32 = {256, 16, SHAPE_LOAD_XPOSE, 1, 1, 0};
 constexpr ScanShape kShapeMaxI32 = {256, 16, SHAPE_LOAD_XPOSE, 1, 1, 0};
 constexpr ScanShape kShapeAffine = {256, 8, SHAPE_LOAD_XPOSE, 1, 1, 0};  // 8-byte elements
+// the operators run through launch_scan_extra, by element size
+constexpr ScanShape kShapeExtra4 = {256, 16, SHAPE_LOAD_XPOSE, 1, 1, 0};
+constexpr ScanShape kShapeExtra8 = {256, 8, SHAPE_LOAD_XPOSE, 1, 1, 0};
 
 }  // namespace scg

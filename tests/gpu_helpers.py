@@ -6,8 +6,10 @@ import numpy as np
 
 import stream_compaction_gb300 as sc
 
-CODE = {"i32": sc.SC_I32, "u32": sc.SC_U32, "f32": sc.SC_F32, "affine": sc.SC_AFFINE_U32}
-OPC = {"sum": sc.SC_SUM, "max": sc.SC_MAX, "affine": sc.SC_COMPOSE}
+CODE = {"i32": sc.SC_I32, "u32": sc.SC_U32, "f32": sc.SC_F32, "affine": sc.SC_AFFINE_U32, "i64": sc.SC_I64,
+        "u64": sc.SC_U64, "f64": sc.SC_F64, "maxcount": sc.SC_MAXCOUNT_I32}
+OPC = {"sum": sc.SC_SUM, "max": sc.SC_MAX, "affine": sc.SC_COMPOSE, "min": sc.SC_MIN, "prod": sc.SC_PROD,
+       "and": sc.SC_AND, "or": sc.SC_OR, "xor": sc.SC_XOR, "maxcount": sc.SC_MAX}
 
 
 def ensure_lib():
@@ -31,12 +33,16 @@ def dev_buffer(words: int, torch_dtype, offset: int = 0):
 
 
 def to_device(x: np.ndarray, offset: int = 0):
-    """Copy a numpy array (int32/uint32/float32, any shape) into a flat device view."""
+    """Copy a numpy array (4- or 8-byte elements, any shape) into a flat device view;
+    offset counts elements of that size."""
     import torch
     flat = np.ascontiguousarray(x).reshape(-1)
-    if flat.dtype == np.float32:
-        tdt = torch.float32
+    if flat.dtype in (np.float32, np.float64):
+        tdt = torch.float32 if flat.dtype == np.float32 else torch.float64
         src = torch.from_numpy(flat)
+    elif flat.dtype.itemsize == 8:
+        tdt = torch.int64
+        src = torch.from_numpy(flat.view(np.int64))
     else:
         tdt = torch.int32
         src = torch.from_numpy(flat.view(np.int32))
@@ -53,9 +59,10 @@ def to_host(view, like: np.ndarray) -> np.ndarray:
 
 
 def kind_of(x: np.ndarray, op: str) -> str:
-    if op == "affine":
-        return "affine"
-    return {np.dtype(np.int32): "i32", np.dtype(np.uint32): "u32", np.dtype(np.float32): "f32"}[x.dtype]
+    if op in ("affine", "maxcount"):
+        return op
+    return {np.dtype(np.int32): "i32", np.dtype(np.uint32): "u32", np.dtype(np.float32): "f32",
+            np.dtype(np.int64): "i64", np.dtype(np.uint64): "u64", np.dtype(np.float64): "f64"}[x.dtype]
 
 
 def gpu_scan(x: np.ndarray, op: str, exclusive: bool, offset: int = 0, inplace: bool = False,
@@ -113,3 +120,28 @@ def check_f32(y_gpu: np.ndarray, y_ref: np.ndarray, abs_prefix: np.ndarray, what
     assert bad.size == 0, "%s: %d elements outside the bound, first at %d (err %g, bound %g)" % (
         what, bad.size, bad[0], err[bad[0]], bound[bad[0]])
     return float(np.max(err / np.maximum(abs_prefix, 1e-300))) if err.size else 0.0
+
+
+def check_f64(y_gpu: np.ndarray, y_ref: np.ndarray, abs_prefix: np.ndarray, what: str = ""):
+    """Float64 sums: |y_gpu[i] - y_ref[i]| <= (16 * ceil(n/2048) + 64) * 2^-53 * sum_{k<=i} |x[k]|.
+
+    Each output is a sum of partial sums rounded along its dependency chain:
+    a tile's prefix comes from an earlier tile's prefix plus a fold of the
+    aggregates in between (at most 16 roundings deep: a 5-level warp tree, up to
+    8 serial folds per lane, 3 combines), and a chain has at most one such hop
+    per tile (tiles hold at least 2048 float64 elements); inside a tile there
+    are fewer than 64 more roundings.  Each rounding is a relative error of at
+    most 2^-53 of a partial sum no larger than sum |x|.  The oracle itself is
+    within 4 * 2^-53 of the exact prefix."""
+    n = y_ref.size
+    bound = (16 * -(-n // 2048) + 64) * 2.0 ** -53 * abs_prefix
+    err = np.abs(y_gpu - y_ref)
+    bad = np.nonzero(err > bound)[0]
+    assert bad.size == 0, "%s: %d elements outside the bound, first at %d (err %g, bound %g)" % (
+        what, bad.size, bad[0], err[bad[0]], bound[bad[0]])
+
+
+def same_float(a: np.ndarray, b: np.ndarray) -> bool:
+    """Equal bit for bit, or both NaN (the exact float max/min scans)."""
+    bits = np.uint32 if a.dtype == np.float32 else np.uint64
+    return bool(np.all((a.view(bits) == b.view(bits)) | (np.isnan(a) & np.isnan(b))))

@@ -49,11 +49,25 @@ def test_host_side_argument_checks(lib):
     import stream_compaction_gb300 as sc
     # invalid enums and negative sizes are rejected before any CUDA call
     assert sc.sc_scan_inclusive(9, sc.SC_SUM, 0, 0, 10, 0) == sc.SC_ERR_INVALID
-    assert sc.sc_scan_exclusive(sc.SC_I32, 7, 0, 0, 10, 0) == sc.SC_ERR_INVALID
+    assert sc.sc_scan_exclusive(sc.SC_I32, 8, 0, 0, 10, 0) == sc.SC_ERR_INVALID
+    assert sc.sc_scan_exclusive(8, sc.SC_SUM, 0, 0, 10, 0) == sc.SC_ERR_INVALID
     assert sc.sc_scan_exclusive(sc.SC_I32, sc.SC_SUM, 0, 0, -1, 0) == sc.SC_ERR_INVALID
     # unsupported operator/dtype pairs
-    assert sc.sc_scan_inclusive(sc.SC_F32, sc.SC_MAX, 0, 0, 0, 0) == sc.SC_ERR_UNSUPPORTED
+    assert sc.sc_scan_inclusive(sc.SC_F32, sc.SC_PROD, 0, 0, 0, 0) == sc.SC_ERR_UNSUPPORTED
+    assert sc.sc_scan_inclusive(sc.SC_F64, sc.SC_XOR, 0, 0, 0, 0) == sc.SC_ERR_UNSUPPORTED
     assert sc.sc_scan_inclusive(sc.SC_I32, sc.SC_COMPOSE, 0, 0, 0, 0) == sc.SC_ERR_UNSUPPORTED
+    assert sc.sc_scan_inclusive(sc.SC_MAXCOUNT_I32, sc.SC_MIN, 0, 0, 0, 0) == sc.SC_ERR_UNSUPPORTED
+    assert sc.sc_scan_batched(sc.SC_AFFINE_U32, sc.SC_AND, 1, 0, 0, 0, 0, 0) == sc.SC_ERR_UNSUPPORTED
+    # every listed (dtype, op) pair passes the host checks (n == 0: no launch)
+    for dt in (sc.SC_I32, sc.SC_U32, sc.SC_I64, sc.SC_U64):
+        for op in (sc.SC_SUM, sc.SC_MAX, sc.SC_MIN, sc.SC_PROD, sc.SC_AND, sc.SC_OR, sc.SC_XOR):
+            assert sc.sc_scan_inclusive(dt, op, 0, 0, 0, 0) == sc.SC_OK, (dt, op)
+    for dt in (sc.SC_F32, sc.SC_F64):
+        for op in (sc.SC_SUM, sc.SC_MAX, sc.SC_MIN):
+            assert sc.sc_scan_exclusive(dt, op, 0, 0, 0, 0) == sc.SC_OK, (dt, op)
+    assert sc.sc_scan_exclusive(sc.SC_MAXCOUNT_I32, sc.SC_MAX, 0, 0, 0, 0) == sc.SC_OK
+    # 8-byte types need 8-byte alignment
+    assert sc.sc_scan_inclusive(sc.SC_I64, sc.SC_SUM, 0x1004, 0x2000, 5, 0) == sc.SC_ERR_INVALID
     # empty input is a no-op; null pointers with n > 0 are errors
     assert sc.sc_scan_inclusive(sc.SC_U32, sc.SC_SUM, 0, 0, 0, 0) == sc.SC_OK
     assert sc.sc_scan_inclusive(sc.SC_U32, sc.SC_SUM, 0, 0, 5, 0) == sc.SC_ERR_INVALID
