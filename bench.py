@@ -297,6 +297,19 @@ def suite_lines(args, dev, sc, synth):
     ms, b = timed(lambda: sc.sc_scan_batched(sc.SC_I32, sc.SC_SUM, 1, x.data_ptr(), y.data_ptr(), 65536, 4096, sp),
                   8 * n, steps=20)
     emit("int32_rows_65536x4096", n, ms, b)
+    # one workload per family of added operators
+    for name, dtype, op, ex in (("int64_exsum_n2^27", sc.SC_I64, sc.SC_SUM, True),
+                                ("float64_exsum_n2^26", sc.SC_F64, sc.SC_SUM, True),
+                                ("int32_min_n2^27", sc.SC_I32, sc.SC_MIN, False),
+                                ("uint32_xor_n2^27", sc.SC_U32, sc.SC_XOR, False),
+                                ("float32_max_n2^26", sc.SC_F32, sc.SC_MAX, False),
+                                ("maxcount_i32_n2^26", sc.SC_MAXCOUNT_I32, sc.SC_MAX, False)):
+        x = synth.make_torch(W[name], device=dev)
+        y = torch.empty_like(x)
+        n = x.shape[0]
+        fn = sc.sc_scan_exclusive if ex else sc.sc_scan_inclusive
+        ms, b = timed(lambda: fn(dtype, op, x.data_ptr(), y.data_ptr(), n, sp), 2 * x.element_size() * x.numel())
+        emit(name, n, ms, b)
     del flush
 
 

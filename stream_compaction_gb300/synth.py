@@ -18,7 +18,10 @@ Mappings from the 64-bit draw ``r``:
   * integer uniform on the closed range [lo, hi]:  lo + (r mod (hi - lo + 1));
   * float32 uniform on [-1, 1):  (r >> 40) * 2**-23 - 1  (exact in float32);
   * full-range 32-bit words:  r >> 32;
-  * affine pairs (a, b):  a = r >> 32, b = r & 0xFFFFFFFF.
+  * affine pairs (a, b):  a = r >> 32, b = r & 0xFFFFFFFF;
+  * full-range 64-bit words:  r;
+  * float64 uniform on [-1, 1):  (r >> 11) * 2**-52 - 1  (exact in float64);
+  * (value, count) pairs:  value = r mod 1024, count = 1.
 ``offset`` selects a substream (2**40 for the second workload drawn from the
 same seed).
 """
@@ -68,6 +71,21 @@ def affine_pairs_np(n, seed, offset=0):
     out = np.empty((n, 2), dtype=np.uint32)
     out[:, 0] = (r >> np.uint64(32)).astype(np.uint32)
     out[:, 1] = (r & np.uint64(0xFFFFFFFF)).astype(np.uint32)
+    return out
+
+
+def full_u64_np(n, seed, offset=0):
+    return draws_np(n, seed, offset)
+
+
+def uniform_pm1_f64_np(n, seed, offset=0):
+    k = (draws_np(n, seed, offset) >> np.uint64(11)).astype(np.float64)
+    return k * 2.0 ** -52 - 1.0
+
+
+def maxcount_pairs_np(n, seed, offset=0):
+    out = np.ones((n, 2), dtype=np.int32)
+    out[:, 0] = (draws_np(n, seed, offset) % np.uint64(1024)).astype(np.int32)
     return out
 
 
@@ -151,8 +169,35 @@ def affine_pairs_torch(n, seed, offset=0, device="cpu"):
     return _chunked(n, f, out)
 
 
+def full_u64_torch(n, seed, offset=0, device="cpu"):
+    """Full-range 64-bit words, stored as int64 bit patterns."""
+    import torch
+    out = torch.empty(n, dtype=torch.int64, device=device)
+    return _chunked(n, lambda s, c: draws_torch(c, seed, offset, s, device), out)
+
+
+def uniform_pm1_f64_torch(n, seed, offset=0, device="cpu"):
+    import torch
+    out = torch.empty(n, dtype=torch.float64, device=device)
+    return _chunked(n, lambda s, c: _lsr(draws_torch(c, seed, offset, s, device), 11).to(torch.float64) * 2.0 ** -52
+                    - 1.0, out)
+
+
+def maxcount_pairs_torch(n, seed, offset=0, device="cpu"):
+    """(n, 2) int32 tensor of (value, 1) pairs."""
+    import torch
+    out = torch.ones((n, 2), dtype=torch.int32, device=device)
+
+    def f(s, c):
+        v = draws_torch(c, seed, offset, s, device) & 1023
+        return torch.stack([v.to(torch.int32), torch.ones_like(v, dtype=torch.int32)], dim=1)
+    return _chunked(n, f, out)
+
+
 # ------------------------------------------------------------- named workloads
-# The five benchmark workloads (sizes, distributions and seeds), as data.
+# The benchmark workloads (sizes, distributions and seeds), as data: the five
+# configurations of the headline metric, then one per family of added operators
+# (op: the operator the benchmark runs on it).
 WORKLOADS = {
     "int32_sum_n1048593": dict(kind="int", n=(1 << 20) + 17, lo=0, hi=9, seed=0, offset=0),
     "float32_exsum_n2^26": dict(kind="pm1", n=1 << 26, seed=1, offset=0),
@@ -161,6 +206,12 @@ WORKLOADS = {
     "affine_u32_n2^26": dict(kind="affine", n=1 << 26, seed=3, offset=SUBSTREAM),
     "uint32_exsum_n2^30": dict(kind="u32", n=1 << 30, seed=4, offset=0),
     "int32_rows_65536x4096": dict(kind="int", n=65536 * 4096, lo=0, hi=255, seed=4, offset=SUBSTREAM),
+    "int64_exsum_n2^27": dict(kind="u64", n=1 << 27, seed=5, offset=0, op="sum"),
+    "float64_exsum_n2^26": dict(kind="pm1_f64", n=1 << 26, seed=6, offset=0, op="sum"),
+    "int32_min_n2^27": dict(kind="u32", n=1 << 27, seed=5, offset=SUBSTREAM, op="min"),
+    "uint32_xor_n2^27": dict(kind="u32", n=1 << 27, seed=7, offset=0, op="xor"),
+    "float32_max_n2^26": dict(kind="pm1", n=1 << 26, seed=7, offset=SUBSTREAM, op="max"),
+    "maxcount_i32_n2^26": dict(kind="maxcount", n=1 << 26, seed=8, offset=0, op="maxcount"),
 }
 
 
@@ -175,6 +226,12 @@ def make_np(spec: dict, n: int | None = None):
         return full_u32_np(n, spec["seed"], spec["offset"])
     if k == "affine":
         return affine_pairs_np(n, spec["seed"], spec["offset"])
+    if k == "u64":
+        return full_u64_np(n, spec["seed"], spec["offset"])
+    if k == "pm1_f64":
+        return uniform_pm1_f64_np(n, spec["seed"], spec["offset"])
+    if k == "maxcount":
+        return maxcount_pairs_np(n, spec["seed"], spec["offset"])
     raise ValueError(k)
 
 
@@ -189,4 +246,10 @@ def make_torch(spec: dict, n: int | None = None, device="cpu"):
         return full_u32_torch(n, spec["seed"], spec["offset"], device)
     if k == "affine":
         return affine_pairs_torch(n, spec["seed"], spec["offset"], device)
+    if k == "u64":
+        return full_u64_torch(n, spec["seed"], spec["offset"], device)
+    if k == "pm1_f64":
+        return uniform_pm1_f64_torch(n, spec["seed"], spec["offset"], device)
+    if k == "maxcount":
+        return maxcount_pairs_torch(n, spec["seed"], spec["offset"], device)
     raise ValueError(k)

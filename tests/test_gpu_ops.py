@@ -167,3 +167,23 @@ def test_unsupported_pairs_and_entry_points():
     # the compaction keeps its three dtypes
     cnt = to_device(np.zeros(1, dtype=np.int64))[1]
     assert sc.sc_compact_if(sc.SC_I64, p, q, cnt.data_ptr(), 10, sc.SC_GT, 0.0, s) == sc.SC_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("name", ["int64_exsum_n2^27", "float64_exsum_n2^26", "int32_min_n2^27", "uint32_xor_n2^27",
+                                  "float32_max_n2^26", "maxcount_i32_n2^26"])
+def test_added_operator_workloads(name):
+    """The benchmark workloads of the added operators, at full size, against the oracle."""
+    import torch
+    from stream_compaction_gb300 import synth
+    spec = synth.WORKLOADS[name]
+    xt = synth.make_torch(spec, device="cuda")
+    torch.cuda.synchronize()
+    x = xt.cpu().numpy()
+    kind = {"u64": "i64", "pm1_f64": "f64", "u32": "u32", "pm1": "f32", "maxcount": "maxcount"}[spec["kind"]]
+    if kind == "u32" and spec["op"] == "min":
+        x = x.view(np.int32)
+    elif kind == "u32":
+        x = x.view(np.uint32)
+    ex = spec["op"] == "sum"
+    y = gpu_scan(x, spec["op"], ex)
+    check("f64" if kind == "f64" else kind, spec["op"], x, y, oracle.scan(x, spec["op"], ex))

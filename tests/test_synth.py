@@ -18,8 +18,8 @@ def test_numpy_and_torch_agree(name):
     n = 100003
     a = synth.make_np(spec, n)
     b = synth.make_torch(spec, n, device="cpu").numpy()
-    if a.dtype == np.uint32:
-        b = b.view(np.uint32)
+    if a.dtype in (np.uint32, np.uint64):
+        b = b.view(a.dtype)
     assert a.shape == b.shape and np.array_equal(a, b)
 
 
@@ -33,3 +33,10 @@ def test_distributions():
     assert abs((c > 0).mean() - 0.5) < 0.01
     t = synth.uniform_pm1_f32_torch(17, seed=1).numpy()
     assert np.array_equal(t, synth.uniform_pm1_f32_np(17, seed=1))
+    d = synth.uniform_pm1_f64_np(n, seed=6)
+    assert d.min() >= -1.0 and d.max() < 1.0 and abs(d.mean()) < 0.01
+    assert len(np.unique(d)) == n                     # 53 random bits: no repeats expected
+    w = synth.full_u64_np(n, seed=5)
+    assert w.max() > np.uint64(1 << 63) and w.min() < np.uint64(1 << 60)
+    m = synth.maxcount_pairs_np(n, seed=8)
+    assert m[:, 0].min() == 0 and m[:, 0].max() == 1023 and np.all(m[:, 1] == 1)
