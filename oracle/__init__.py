@@ -47,6 +47,14 @@ for _op in ("max", "min"):
         _GENERIC[(_op, np.dtype(_dt))] = "oracle_scan_%s_%s" % (_op, _sfx)
 _GENERIC[("min", np.dtype(np.int32))] = "oracle_scan_min_i32"
 
+# (op, numpy dtype) -> the segmented scan (head flags) of the same operator
+_SEGMENTED = {k: v.replace("oracle_scan_", "oracle_segscan_") for k, v in _GENERIC.items()}
+for _dt in (np.int32, np.uint32):
+    _SEGMENTED[("sum", np.dtype(_dt))] = "oracle_segscan_sum_u32"
+_SEGMENTED[("max", np.dtype(np.int32))] = "oracle_segscan_max_i32"
+_SEGMENTED[("sum", np.dtype(np.float32))] = "oracle_segscan_sum_f32"
+_SEGMENTED[("sum", np.dtype(np.float64))] = "oracle_segscan_sum_f64"
+
 
 def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
     """Compile oracle.c into a shared library with gcc (-O2, no fast-math)."""
@@ -79,6 +87,10 @@ def load_library(path: str) -> ctypes.CDLL:
     for name in ("oracle_scan_sum_f64", "oracle_scan_maxcount_i32"):
         f = getattr(lib, name)
         f.argtypes = [P, P, I64, INT]
+        f.restype = None
+    for name in set(_SEGMENTED.values()):
+        f = getattr(lib, name)
+        f.argtypes = [P, P, P, I64, INT]
         f.restype = None
     for name in ("oracle_compact_i32", "oracle_compact_u32", "oracle_compact_f32"):
         f = getattr(lib, name)
@@ -190,6 +202,32 @@ class Oracle:
             return np.empty_like(xs)
         return np.stack([self.scan(xs[r], op, exclusive) for r in range(rows)])
 
+    def scan_segmented(self, x: np.ndarray, heads: np.ndarray, op: str, exclusive: bool) -> np.ndarray:
+        """Segmented scan: heads[i] != 0 starts a new segment at i (element 0
+        always starts one); the same operators and dtypes as scan()."""
+        ex = 1 if exclusive else 0
+        h = np.ascontiguousarray(heads, dtype=np.uint8)
+        n = x.shape[0]
+        if h.shape != (n,):
+            raise ValueError("heads must hold one flag per element")
+        if op in ("affine", "maxcount") and x.ndim == 2 and x.shape[1] == 2 and x.dtype in (np.int32, np.uint32):
+            xs = np.ascontiguousarray(x).view(np.uint32)
+            y = np.empty_like(xs)
+            getattr(self.c, "oracle_segscan_%s_i32" % op if op == "maxcount" else "oracle_segscan_affine_u32")(
+                _ptr(xs), _ptr(h), _ptr(y), n, ex)
+            return y.view(x.dtype)
+        name = _SEGMENTED.get((op, x.dtype))
+        if name is None or x.ndim != 1:
+            raise ValueError("unsupported oracle segmented scan: op=%s dtype=%s" % (op, x.dtype))
+        xs = np.ascontiguousarray(x)
+        if x.dtype in (np.int32, np.uint32) and "u32" in name:
+            xs = xs.view(np.uint32)
+        elif x.dtype in (np.int64, np.uint64) and "u64" in name:
+            xs = xs.view(np.uint64)
+        y = np.empty(n, dtype=np.float64) if x.dtype == np.float32 and op == "sum" else np.empty_like(xs)
+        getattr(self.c, name)(_ptr(xs), _ptr(h), _ptr(y), n, ex)
+        return y if y.dtype == np.float64 and x.dtype == np.float32 else y.view(x.dtype)
+
     # -- compaction ----------------------------------------------------------
     def compact(self, x: np.ndarray, pred: str, threshold: float):
         """Order-preserving compaction; returns (kept values, count)."""
@@ -232,6 +270,10 @@ def scan(x, op, exclusive):
 
 def scan_batched(x, op, exclusive):
     return default().scan_batched(x, op, exclusive)
+
+
+def scan_segmented(x, heads, op, exclusive):
+    return default().scan_segmented(x, heads, op, exclusive)
 
 
 def compact(x, pred, threshold):

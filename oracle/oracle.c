@@ -260,6 +260,135 @@ void oracle_abs_prefix_f64(const double *x, double *s, int64_t n)
     }
 }
 
+/* ---- segmented scans: head flags h[i] != 0 start a new segment (element 0
+ *      always starts one); the running value restarts from the identity at
+ *      each head, so y[i] is the scan of x[s..i] (inclusive) or x[s..i-1]
+ *      (exclusive, the identity at s), s the last head at or before i.
+ *      ([L7] section 2: each digit pass of a radix sort places its elements
+ *      with a segmented scan; section 1: max/min scans answer "is this the
+ *      first element of its segment that satisfies the condition") ---- */
+
+#define ORACLE_SEGSCAN(NAME, T, IDENT, OP)                                               \
+    void oracle_segscan_##NAME(const T *x, const uint8_t *h, T *y, int64_t n, int exclusive) \
+    {                                                                                    \
+        T acc = (IDENT);                                                                 \
+        for (int64_t i = 0; i < n; ++i) {                                                \
+            if (h[i])                                                                    \
+                acc = (IDENT);                                                           \
+            if (exclusive) {                                                             \
+                y[i] = acc;                                                              \
+                acc = OP(acc, x[i]);                                                     \
+            } else {                                                                     \
+                acc = OP(acc, x[i]);                                                     \
+                y[i] = acc;                                                              \
+            }                                                                            \
+        }                                                                                \
+    }
+
+ORACLE_SEGSCAN(sum_u32, uint32_t, 0u, sum_u32)
+ORACLE_SEGSCAN(max_i32, int32_t, INT32_MIN, max_i32)
+ORACLE_SEGSCAN(prod_u32, uint32_t, 1u, prod_u32)
+ORACLE_SEGSCAN(and_u32, uint32_t, 0xFFFFFFFFu, and_u32)
+ORACLE_SEGSCAN(or_u32, uint32_t, 0u, or_u32)
+ORACLE_SEGSCAN(xor_u32, uint32_t, 0u, xor_u32)
+ORACLE_SEGSCAN(min_i32, int32_t, INT32_MAX, min_i32)
+ORACLE_SEGSCAN(max_u32, uint32_t, 0u, max_u32)
+ORACLE_SEGSCAN(min_u32, uint32_t, 0xFFFFFFFFu, min_u32)
+ORACLE_SEGSCAN(sum_u64, uint64_t, 0u, sum_u64)
+ORACLE_SEGSCAN(prod_u64, uint64_t, 1u, prod_u64)
+ORACLE_SEGSCAN(and_u64, uint64_t, 0xFFFFFFFFFFFFFFFFull, and_u64)
+ORACLE_SEGSCAN(or_u64, uint64_t, 0u, or_u64)
+ORACLE_SEGSCAN(xor_u64, uint64_t, 0u, xor_u64)
+ORACLE_SEGSCAN(max_i64, int64_t, INT64_MIN, max_i64)
+ORACLE_SEGSCAN(min_i64, int64_t, INT64_MAX, min_i64)
+ORACLE_SEGSCAN(max_u64, uint64_t, 0u, max_u64)
+ORACLE_SEGSCAN(min_u64, uint64_t, 0xFFFFFFFFFFFFFFFFull, min_u64)
+ORACLE_SEGSCAN(max_f32, float, -INFINITY, max_f32)
+ORACLE_SEGSCAN(min_f32, float, INFINITY, min_f32)
+ORACLE_SEGSCAN(max_f64, double, -INFINITY, max_f64)
+ORACLE_SEGSCAN(min_f64, double, INFINITY, min_f64)
+
+/* float32 sum: accumulated in fp64, as oracle_scan_sum_f32 */
+void oracle_segscan_sum_f32(const float *x, const uint8_t *h, double *y, int64_t n, int exclusive)
+{
+    double acc = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        if (h[i])
+            acc = 0.0;
+        if (exclusive) {
+            y[i] = acc;
+            acc = acc + (double)x[i];
+        } else {
+            acc = acc + (double)x[i];
+            y[i] = acc;
+        }
+    }
+}
+
+/* float64 sum: compensated, as oracle_scan_sum_f64 */
+void oracle_segscan_sum_f64(const double *x, const uint8_t *h, double *y, int64_t n, int exclusive)
+{
+    double s = 0.0, c = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        if (h[i]) {
+            s = 0.0;
+            c = 0.0;
+        }
+        if (exclusive)
+            y[i] = s + c;
+        const double t = s + x[i];
+        if (fabs(s) >= fabs(x[i]))
+            c += (s - t) + x[i];
+        else
+            c += (x[i] - t) + s;
+        s = t;
+        if (!exclusive)
+            y[i] = s + c;
+    }
+}
+
+/* pairs: affine maps and (max, count), interleaved as in the plain scans */
+void oracle_segscan_affine_u32(const uint32_t *x, const uint8_t *h, uint32_t *y, int64_t n, int exclusive)
+{
+    uint32_t acc_a = 1u, acc_b = 0u;
+    for (int64_t i = 0; i < n; ++i) {
+        if (h[i]) {
+            acc_a = 1u;
+            acc_b = 0u;
+        }
+        if (exclusive) {
+            y[2 * i] = acc_a;
+            y[2 * i + 1] = acc_b;
+            compose_affine(&acc_a, &acc_b, x[2 * i], x[2 * i + 1]);
+        } else {
+            compose_affine(&acc_a, &acc_b, x[2 * i], x[2 * i + 1]);
+            y[2 * i] = acc_a;
+            y[2 * i + 1] = acc_b;
+        }
+    }
+}
+
+void oracle_segscan_maxcount_i32(const uint32_t *x, const uint8_t *h, uint32_t *y, int64_t n, int exclusive)
+{
+    int32_t acc_v = INT32_MIN;
+    uint32_t acc_c = 0u;
+    for (int64_t i = 0; i < n; ++i) {
+        if (h[i]) {
+            acc_v = INT32_MIN;
+            acc_c = 0u;
+        }
+        if (exclusive) {
+            y[2 * i] = (uint32_t)acc_v;
+            y[2 * i + 1] = acc_c;
+            maxcount(&acc_v, &acc_c, (int32_t)x[2 * i], x[2 * i + 1]);
+        } else {
+            maxcount(&acc_v, &acc_c, (int32_t)x[2 * i], x[2 * i + 1]);
+            y[2 * i] = (uint32_t)acc_v;
+            y[2 * i + 1] = acc_c;
+        }
+    }
+}
+
 /* ---- batched rows: the same scan on each row of a row-major rows x cols
  *      matrix, the accumulator starting again from the identity at each row
  *      (no passage on the pages; the plain reading of "independent scans") ---- */

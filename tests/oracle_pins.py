@@ -560,11 +560,127 @@ def pin_brute_force_more(o):
                 assert np.array_equal(got[:, i, 1].astype(np.int64), wc), (length, ex, i)
 
 
+# ------------------------------------------------------------ segmented scans
+_SEG_CASES = [("i32", "sum"), ("u32", "sum"), ("i32", "max"), ("f32", "sum"), ("u32", "prod"), ("i32", "and"),
+              ("u32", "or"), ("u32", "xor"), ("i32", "min"), ("u32", "max"), ("u32", "min"), ("u64", "sum"),
+              ("i64", "prod"), ("u64", "and"), ("i64", "or"), ("u64", "xor"), ("i64", "max"), ("i64", "min"),
+              ("u64", "max"), ("u64", "min"), ("f32", "max"), ("f32", "min"), ("f64", "sum"), ("f64", "max"),
+              ("f64", "min"), ("affine", "affine"), ("maxcount", "maxcount")]
+
+
+def _seg_input(kind, n, rng):
+    if kind in ("affine", "maxcount"):
+        v = rng.integers(0, 1 << 32, (n, 2), dtype=np.uint64).astype(np.uint32)
+        if kind == "maxcount":
+            v[:, 0] = rng.integers(-3, 3, n).astype(np.int32).view(np.uint32)
+            v[:, 1] = rng.integers(0, 3, n)
+        return v
+    if kind in ("f32", "f64"):
+        x = rng.uniform(-5, 5, n).astype(np.float32 if kind == "f32" else np.float64)
+        x[rng.integers(0, n, max(1, n // 50))] = np.nan
+        return x
+    dt = {"i32": np.int32, "u32": np.uint32, "i64": np.int64, "u64": np.uint64}[kind]
+    return rng.integers(0, 1 << 62, n, dtype=np.int64).astype(np.uint64).astype(np.dtype(dt).str.replace("i", "u"))\
+        .view(dt) | np.array(1, dt)
+
+
+def _seg_equal(a, b):
+    if a.dtype.kind == "f":
+        return _same_float(a, b) if a.dtype == b.dtype else np.array_equal(a, b)
+    return np.array_equal(a, b)
+
+
+def pin_segmented_is_scan_per_segment(o):
+    """The segmented scan equals the plain scan of each segment on its own."""
+    rng = np.random.default_rng(31)
+    n = 3001
+    for kind, op in _SEG_CASES:
+        x = _seg_input(kind, n, rng)
+        for density in (0.0, 0.003, 0.05, 0.5):
+            h = (rng.random(n) < density).astype(np.uint8)
+            starts = [0] + [i for i in range(1, n) if h[i]]
+            ends = starts[1:] + [n]
+            for ex in (False, True):
+                y = o.scan_segmented(x, h, op, ex)
+                want = np.concatenate([o.scan(x[a:b].copy(), op, ex) for a, b in zip(starts, ends)])
+                assert _seg_equal(y, want), (kind, op, density, ex)
+
+
+def pin_segmented_special_cases(o):
+    rng = np.random.default_rng(32)
+    n = 2000
+    for kind, op in _SEG_CASES:
+        x = _seg_input(kind, n, rng)
+        none = np.zeros(n, np.uint8)
+        allh = np.ones(n, np.uint8)
+        for ex in (False, True):
+            assert _seg_equal(o.scan_segmented(x, none, op, ex), o.scan(x, op, ex)), (kind, op, ex)
+        # every element its own segment: inclusive gives x, exclusive the identity everywhere
+        inc = o.scan_segmented(x, allh, op, False)
+        exc = o.scan_segmented(x, allh, op, True)
+        if op == "sum" and kind == "f32":
+            assert np.array_equal(inc, x.astype(np.float64), equal_nan=True)
+        else:
+            assert _seg_equal(inc, x), (kind, op)
+        first = o.scan(x[:1].copy(), op, True)
+        assert _seg_equal(exc, np.repeat(first, n, axis=0)), (kind, op)
+    # heads at multiples of cols: the batched row scans
+    d = _random_inputs()
+    x = d["sum_i32"][:30000]
+    h = np.zeros(30000, np.uint8)
+    h[::250] = 1
+    for ex in (False, True):
+        assert np.array_equal(o.scan_segmented(x, h, "sum", ex), o.scan_batched(x.reshape(120, 250), "sum", ex).ravel())
+
+
+def pin_segmented_brute_force(o):
+    """Every head pattern of every input of length <= 6 on a small alphabet."""
+    for length in range(1, 7):
+        seqs = _all_sequences(np.array([0, 1, 5], dtype=np.uint32), length)
+        for mask in range(1 << length):
+            h = np.array([(mask >> j) & 1 for j in range(length)], dtype=np.uint8)
+            for r in range(0, seqs.shape[0], 7):
+                row = seqs[r]
+                for ex in (False, True):
+                    got = o.scan_segmented(row, h, "sum", ex).tolist()
+                    want, acc = [], 0
+                    for j in range(length):
+                        if h[j]:
+                            acc = 0
+                        if ex:
+                            want.append(acc)
+                            acc = acc + int(row[j])
+                        else:
+                            acc = acc + int(row[j])
+                            want.append(acc)
+                    assert got == want, (row.tolist(), h.tolist(), ex)
+
+
+def pin_segmented_first_satisfying(o):
+    """The pages' use of a max scan: the first element of each segment that
+    satisfies a predicate is where the predicate holds and the exclusive
+    segmented max of the predicate is still 0."""
+    rng = np.random.default_rng(33)
+    n = 5000
+    p = (rng.random(n) < 0.2).astype(np.int32)
+    h = (rng.random(n) < 0.01).astype(np.uint8)
+    seen = o.scan_segmented(p, h, "max", True)
+    first = (p == 1) & (seen <= 0)
+    want, found = [], False
+    for i in range(n):
+        if i == 0 or h[i]:
+            found = False
+        want.append(bool(p[i]) and not found)
+        found = found or bool(p[i])
+    assert first.tolist() == want
+
+
 ALL_PINS = [
     pin_golden_sum_examples, pin_golden_compaction_examples, pin_golden_identities,
     pin_closed_forms, pin_affine_special_cases, pin_invariants, pin_affine_recurrence,
     pin_library_special_cases, pin_float_fp64_accumulation, pin_batched_rows,
     pin_brute_force_sum, pin_brute_force_max, pin_brute_force_affine, pin_brute_force_compaction,
     pin_golden_identities_more, pin_closed_forms_more, pin_library_special_cases_more, pin_float64_sum,
-    pin_brute_force_more,
+    pin_brute_force_more, pin_segmented_is_scan_per_segment, pin_segmented_special_cases,
+    pin_segmented_brute_force, pin_segmented_first_satisfying,
 ]

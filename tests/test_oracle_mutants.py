@@ -59,6 +59,12 @@ MUTANTS = {
                        "static double min_f64(double acc, double x) { if (isnan(acc)) return acc; if (isnan(x)) return x; return x <= acc ? x : acc; }"),
     # (max, count): equal values do not add their counts
     "maxcount_ties_not_added": ("        *acc_c = *acc_c + c;", "        *acc_c = c;"),
+    # segmented scan that ignores the head flags
+    "segscan_no_reset": ("            if (h[i])                                                                    \\\n                acc = (IDENT);",
+                         "            if (0)                                                                       \\\n                acc = (IDENT);"),
+    # segmented float64 sum that keeps the compensation across a head
+    "segscan_f64_keeps_compensation": ("        if (h[i]) {\n            s = 0.0;\n            c = 0.0;\n        }",
+                                       "        if (h[i]) {\n            s = 0.0;\n        }"),
 }
 
 
