@@ -310,6 +310,15 @@ def suite_lines(args, dev, sc, synth):
         fn = sc.sc_scan_exclusive if ex else sc.sc_scan_inclusive
         ms, b = timed(lambda: fn(dtype, op, x.data_ptr(), y.data_ptr(), n, sp), 2 * x.element_size() * x.numel())
         emit(name, n, ms, b)
+    # segmented sum with head flags (algorithmic bytes: values in and out + one flag byte per element)
+    spec = W["int32_segsum_n2^27"]
+    x = synth.make_torch(spec, device=dev)
+    h = synth.make_heads_torch(spec, device=dev)
+    y = torch.empty_like(x)
+    n = x.numel()
+    ms, b = timed(lambda: sc.sc_scan_segmented(sc.SC_I32, sc.SC_SUM, 1, x.data_ptr(), h.data_ptr(), y.data_ptr(), n,
+                                               sp), 9 * n)
+    emit("int32_segsum_n2^27", n, ms, b, {"segments": int(h.sum().item())})
     del flush
 
 

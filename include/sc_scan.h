@@ -151,6 +151,21 @@ sc_status sc_scan_exclusive(sc_dtype dtype, sc_op op, const void *in, void *out,
 sc_status sc_scan_batched(sc_dtype dtype, sc_op op, int exclusive, const void *in, void *out,
                           int64_t rows, int64_t cols, sc_stream_t stream);
 
+/* Segmented scan with head flags: d_heads[i] != 0 (one byte per element,
+ * device memory, n bytes) starts a new segment at i; element 0 always starts
+ * one.  The running value restarts from the identity at every head, so y[i]
+ * is the scan of x[s..i] (inclusive) or x[s..i-1] (exclusive: the identity at
+ * s itself), s the last head at or before i.  The Lecture 7 notes (section 2)
+ * name the segmented scan as the placement step of each radix-sort digit
+ * pass, and (section 1) max/min scans for "predicate prefix" questions such as
+ * "is this the first element of its segment that satisfies the condition";
+ * the head-flag form is the plain reading of a segment boundary.  Every
+ * (dtype, op) pair of the plain scans; in == out is allowed; d_heads must not
+ * overlap out.  One launch of the one-tile-per-CTA kernel (a tile that holds a
+ * head publishes its complete prefix at once). */
+sc_status sc_scan_segmented(sc_dtype dtype, sc_op op, int exclusive, const void *in, const uint8_t *d_heads,
+                            void *out, int64_t n, sc_stream_t stream);
+
 /* Fused, order-preserving stream compaction (one kernel launch): out[0..count)
  * receives, in input order, every in[i] with (in[i] <pred> threshold); the
  * number kept is written to *d_count (device int64).  out[count..n) is left

@@ -88,7 +88,7 @@ def load_library(path: str) -> ctypes.CDLL:
         f = getattr(lib, name)
         f.argtypes = [P, P, I64, INT]
         f.restype = None
-    for name in set(_SEGMENTED.values()):
+    for name in set(_SEGMENTED.values()) | {"oracle_segscan_affine_u32", "oracle_segscan_maxcount_i32"}:
         f = getattr(lib, name)
         f.argtypes = [P, P, P, I64, INT]
         f.restype = None

@@ -46,6 +46,7 @@ SIGNATURES = {
     "sc_hier_workspace_bytes": ([_INT, _I64], _SZ),
     "sc_scan_host": ([_INT, _INT, _INT, _P, _P, _I64, _P], _INT),
     "sc_scan_noalloc": ([_INT, _INT, _INT, _P, _P, _I64, _P], _INT),
+    "sc_scan_segmented": ([_INT, _INT, _INT, _P, _P, _P, _I64, _P], _INT),
     "sc_get_device_error": ([_P], _INT),
     "sc_launch_count": ([], _U64),
     "sc_set_scan_variant": ([_INT], _INT),
@@ -139,6 +140,11 @@ def sc_scan_host(dtype: int, op: int, exclusive: int, h_in: int, h_out: int, n: 
 
 def sc_scan_noalloc(dtype: int, op: int, exclusive: int, d_in: int, d_out: int, n: int, stream: int) -> int:
     return load().sc_scan_noalloc(dtype, op, exclusive, d_in, d_out, n, stream)
+
+
+def sc_scan_segmented(dtype: int, op: int, exclusive: int, d_in: int, d_heads: int, d_out: int, n: int,
+                      stream: int) -> int:
+    return load().sc_scan_segmented(dtype, op, exclusive, d_in, d_heads, d_out, n, stream)
 
 
 SC_NOALLOC_MAX_N = 1 << 27
@@ -245,6 +251,20 @@ def scan_batched(x, op: str = "sum", exclusive: bool = True, out=None, stream=No
     rows, cols = x.shape[0], x.shape[1]
     _check(sc_scan_batched(_dtype_code(x, op), _OPS[op], int(exclusive), x.data_ptr(), out.data_ptr(), rows, cols,
                            _stream(stream)), "sc_scan_batched")
+    return out
+
+
+def scan_segmented(x, heads, op: str = "sum", exclusive: bool = True, out=None, stream=None):
+    """Segmented scan of a 1-D CUDA tensor (pair ops: shape (n, 2)); heads is a
+    CUDA uint8/bool tensor of n flags, nonzero where a segment starts."""
+    import torch
+    out, n = _prep(x, out, op)
+    if not heads.is_cuda or heads.numel() != n or heads.dtype not in (torch.uint8, torch.bool, torch.int8):
+        raise ValueError("heads must be a CUDA uint8/bool tensor with one flag per element")
+    if not heads.is_contiguous():
+        raise ValueError("heads must be contiguous")
+    _check(sc_scan_segmented(_dtype_code(x, op), _OPS[op], int(exclusive), x.data_ptr(), heads.data_ptr(),
+                             out.data_ptr(), n, _stream(stream)), "sc_scan_segmented")
     return out
 
 

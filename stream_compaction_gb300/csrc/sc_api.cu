@@ -253,8 +253,9 @@ cudaError_t dispatch_scan_tma(int oid, const ScanParams& p, bool excl, unsigned 
 // kernel (shape v - 1; by default shape 0, or kSmallShape for short uint32
 // sums).
 sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_len, bool excl,
-                   const void* carry_in, void* carry_out, cudaStream_t s) {
-    const int api_variant = (oid == 0 && seg_len == 0) ? g_variant.load() : 0;
+                   const void* carry_in, void* carry_out, cudaStream_t s, const unsigned char* heads = nullptr) {
+    const bool segmented = seg_len > 0 || heads != nullptr;
+    const int api_variant = (oid == 0 && !segmented) ? g_variant.load() : 0;
     const bool vec_ok = aligned(in, 16) && aligned(out, 16);
     const int eb = scg::oid_elem_bytes(oid);
     const int cfg = tma_cfg_of(api_variant);
@@ -263,9 +264,9 @@ sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_le
     const int64_t tma_tile = cfg >= 0 ? sh.tile_bytes / eb : 0;
     const bool tma_stats = api_variant == kTmaStatsVariant;
     const bool small = api_variant == 0 && n <= kSmallScanMax;
-    const bool use_tma = cfg >= 0 && !small && seg_len == 0 && vec_ok && n >= tma_tile &&
+    const bool use_tma = cfg >= 0 && !small && !segmented && vec_ok && n >= tma_tile &&
                          n / tma_tile * (sh.tile_bytes / 128) < (int64_t)INT_MAX && num_sms() > 0;
-    const int legacy_variant = (small && oid == 0 && seg_len == 0) ? kSmallShape
+    const int legacy_variant = (small && oid == 0 && !segmented) ? kSmallShape
                                : (cfg >= 0 || api_variant == 0) ? 0 : api_variant - 1;
     // units of the look-back: chunks of the persistent kernel, tiles otherwise
     const int64_t tile = use_tma ? tma_tile * sh.chunk_tiles : scg::scan_tile_elems(oid, legacy_variant);
@@ -279,6 +280,7 @@ sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_le
     p.out = out;
     p.n = n;
     p.seg_len = seg_len;
+    p.heads = heads;
     p.vec_ok = vec_ok;
     p.carry_in = carry_in;
     p.carry_out = carry_out;
@@ -288,7 +290,7 @@ sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_le
         const cudaError_t e = dispatch_scan_tma(oid, p, excl, grid, s, tma_stats, cfg);
         return finish_launch(*ws, ntiles + grid * (unsigned)scg::tma_ids_per_cta(), e);
     }
-    return finish_launch(*ws, ntiles, dispatch_scan(oid, p, excl, seg_len > 0, legacy_variant, s));
+    return finish_launch(*ws, ntiles, dispatch_scan(oid, p, excl, segmented, legacy_variant, s));
 }
 
 // ------------------------------------------------------ compaction predicate
@@ -458,6 +460,19 @@ sc_status sc_scan_inclusive(sc_dtype dtype, sc_op op, const void* in, void* out,
 
 sc_status sc_scan_exclusive(sc_dtype dtype, sc_op op, const void* in, void* out, int64_t n, sc_stream_t stream) {
     return scan_common(dtype, op, in, out, n, stream, true);
+}
+
+sc_status sc_scan_segmented(sc_dtype dtype, sc_op op, int exclusive, const void* in, const uint8_t* d_heads,
+                            void* out, int64_t n, sc_stream_t stream) {
+    int oid = -1;
+    sc_status st = check_scan_args(dtype, op, in, out, n, &oid);
+    if (st != SC_OK || n == 0) return st;
+    if (!d_heads) return SC_ERR_INVALID;
+    const uintptr_t h = reinterpret_cast<uintptr_t>(d_heads), o = reinterpret_cast<uintptr_t>(out);
+    const size_t out_bytes = (size_t)n * elem_bytes(dtype);
+    if (h < o + out_bytes && o < h + (size_t)n) return SC_ERR_INVALID;  // the flags must not be overwritten
+    return run_scan(oid, in, out, n, 0, exclusive != 0, nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream),
+                    d_heads);
 }
 
 sc_status sc_scan_batched(sc_dtype dtype, sc_op op, int exclusive, const void* in, void* out, int64_t rows,

@@ -113,6 +113,7 @@ extern "C" sc_status sc_scan_noalloc(sc_dtype dtype, sc_op op, int exclusive, co
     p.out = out;
     p.n = n;
     p.seg_len = 0;
+    p.heads = nullptr;
     p.vec_ok = (a % 16 == 0) && (b % 16 == 0);
     p.carry_in = nullptr;
     p.carry_out = nullptr;

@@ -30,6 +30,7 @@ struct ScanParams {
     void* out;
     long long n;                    // elements
     long long seg_len;              // > 0: independent segments of this length (batched rows)
+    const unsigned char* heads;     // non-null: heads[i] != 0 starts a segment at i (seg_len unused)
     int vec_ok;                     // in and out are 16-byte aligned
     const void* carry_in;           // optional carry folded in front of element 0 (device)
     void* carry_out;                // optional inclusive total, written by the last tile (device)

@@ -29,6 +29,37 @@ __device__ __forceinline__ uint32_t head_bits(long long first_index, long long s
     return hm;
 }
 
+// Segment heads inside the thread's IPT items from a head-flag array (one
+// byte per element, nonzero = head); one vector load when the flags are full
+// and aligned, else byte loads up to n.
+template <int IPT>
+__device__ __forceinline__ uint32_t head_bits_flags(const unsigned char* heads, long long first, long long n) {
+    uint32_t hm = 0;
+    const unsigned char* f = heads + first;
+    if constexpr (IPT == 16 || IPT == 8) {
+        if (first + IPT <= n && (reinterpret_cast<uintptr_t>(f) % IPT) == 0) {
+            uint32_t w[IPT / 4];
+            if constexpr (IPT == 16) {
+                const uint4 q = __ldg(reinterpret_cast<const uint4*>(f));
+                w[0] = q.x; w[1] = q.y; w[2] = q.z; w[3] = q.w;
+            } else {
+                const uint2 q = __ldg(reinterpret_cast<const uint2*>(f));
+                w[0] = q.x; w[1] = q.y;
+            }
+#pragma unroll
+            for (int j = 0; j < IPT / 4; ++j)
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+                    if ((w[j] >> (8 * b)) & 0xffu) hm |= 1u << (4 * j + b);
+            return hm;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < IPT; ++k)
+        if (first + k < n && f[k]) hm |= 1u << k;
+    return hm;
+}
+
 // Sleep for the test hook that slows one tile down (bounded by ns itself).
 __device__ __forceinline__ void hook_delay(unsigned ns) {
     const unsigned long long t0 = global_ns();
@@ -79,7 +110,10 @@ __global__ void __launch_bounds__(NT, kMinB) scan_kernel(const ScanParams p) {
     else load_partial_tile<T, IPT>(tin, v, valid, Op::identity());
 
     uint32_t hm = 0;
-    if constexpr (kSeg) hm = head_bits<IPT>(tile_start + (long long)tid * IPT, p.seg_len);
+    if constexpr (kSeg) {
+        const long long first = tile_start + (long long)tid * IPT;
+        hm = p.heads ? head_bits_flags<IPT>(p.heads, first, p.n) : head_bits<IPT>(first, p.seg_len);
+    }
 
     // thread-serial inclusive scan (restarting at segment heads)
 #pragma unroll
@@ -135,7 +169,8 @@ __global__ void __launch_bounds__(NT, kMinB) scan_kernel(const ScanParams p) {
         } else {
             if (tile == p.lb.delay_tile && lane == 0) hook_delay(p.lb.delay_ns);
             __syncwarp();
-            const bool first_is_head = kSeg && (tile_start % p.seg_len == 0);
+            const bool first_is_head =
+                kSeg && (p.heads ? (p.heads[tile_start] != 0) : (tile_start % p.seg_len == 0));
             if (tile == 0 || first_is_head) {
                 if (!kSeg && p.carry_in) prefix = *static_cast<const C*>(p.carry_in);
                 if (lane == 0) StatusIO<C>::publish(p.lb, tile, ST_PREFIX, kSeg ? agg : Op::c_op(prefix, agg));

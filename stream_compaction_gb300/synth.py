@@ -21,7 +21,8 @@ Mappings from the 64-bit draw ``r``:
   * affine pairs (a, b):  a = r >> 32, b = r & 0xFFFFFFFF;
   * full-range 64-bit words:  r;
   * float64 uniform on [-1, 1):  (r >> 11) * 2**-52 - 1  (exact in float64);
-  * (value, count) pairs:  value = r mod 1024, count = 1.
+  * (value, count) pairs:  value = r mod 1024, count = 1;
+  * segment head flags with mean segment length L:  1 if r mod L == 0, else 0.
 ``offset`` selects a substream (2**40 for the second workload drawn from the
 same seed).
 """
@@ -87,6 +88,10 @@ def maxcount_pairs_np(n, seed, offset=0):
     out = np.ones((n, 2), dtype=np.int32)
     out[:, 0] = (draws_np(n, seed, offset) % np.uint64(1024)).astype(np.int32)
     return out
+
+
+def head_flags_np(n, seed, offset=0, period=1024):
+    return (draws_np(n, seed, offset) % np.uint64(period) == 0).astype(np.uint8)
 
 
 # --------------------------------------------------------------- torch (device)
@@ -194,6 +199,19 @@ def maxcount_pairs_torch(n, seed, offset=0, device="cpu"):
     return _chunked(n, f, out)
 
 
+def head_flags_torch(n, seed, offset=0, period=1024, device="cpu"):
+    """uint8 flags: 1 where a segment starts."""
+    import torch
+    out = torch.empty(n, dtype=torch.uint8, device=device)
+
+    def f(s, c):
+        r = draws_torch(c, seed, offset, s, device)
+        # unsigned r mod period from the two 32-bit halves, as in uniform_int_torch
+        v = ((_lsr(r, 32) % period) * ((1 << 32) % period) + (r & 0xFFFFFFFF)) % period
+        return (v == 0).to(torch.uint8)
+    return _chunked(n, f, out)
+
+
 # ------------------------------------------------------------- named workloads
 # The benchmark workloads (sizes, distributions and seeds), as data: the five
 # configurations of the headline metric, then one per family of added operators
@@ -212,7 +230,20 @@ WORKLOADS = {
     "uint32_xor_n2^27": dict(kind="u32", n=1 << 27, seed=7, offset=0, op="xor"),
     "float32_max_n2^26": dict(kind="pm1", n=1 << 26, seed=7, offset=SUBSTREAM, op="max"),
     "maxcount_i32_n2^26": dict(kind="maxcount", n=1 << 26, seed=8, offset=0, op="maxcount"),
+    # segmented sum: values as the batched rows, heads with mean segment length 1024
+    "int32_segsum_n2^27": dict(kind="int", n=1 << 27, lo=0, hi=255, seed=9, offset=0, op="sum",
+                               heads=dict(seed=9, offset=SUBSTREAM, period=1024)),
 }
+
+
+def make_heads_np(spec: dict, n: int | None = None):
+    h = spec["heads"]
+    return head_flags_np(spec["n"] if n is None else n, h["seed"], h["offset"], h["period"])
+
+
+def make_heads_torch(spec: dict, n: int | None = None, device="cpu"):
+    h = spec["heads"]
+    return head_flags_torch(spec["n"] if n is None else n, h["seed"], h["offset"], h["period"], device)
 
 
 def make_np(spec: dict, n: int | None = None):

@@ -80,6 +80,11 @@ def test_host_side_argument_checks(lib):
     assert sc.sc_compact_if(sc.SC_I32, 0x1000, 0x9000, 0x8000, 16, 11, 0.0, 0) == sc.SC_ERR_INVALID
     assert sc.sc_compact_if(sc.SC_AFFINE_U32, 0x1000, 0x9000, 0x8000, 16, sc.SC_GT, 0.0, 0) == sc.SC_ERR_UNSUPPORTED
     assert sc.sc_compact_if(sc.SC_I32, 0x1000, 0x9000, 0, 16, sc.SC_GT, 0.0, 0) == sc.SC_ERR_INVALID
+    # segmented scan: flags are required and must not overlap the output
+    assert sc.sc_scan_segmented(sc.SC_I32, sc.SC_SUM, 1, 0x1000, 0, 0x9000, 16, 0) == sc.SC_ERR_INVALID
+    assert sc.sc_scan_segmented(sc.SC_I32, sc.SC_SUM, 1, 0x1000, 0x9004, 0x9000, 16, 0) == sc.SC_ERR_INVALID
+    assert sc.sc_scan_segmented(sc.SC_I32, sc.SC_COMPOSE, 1, 0x1000, 0x20000, 0x9000, 16, 0) == sc.SC_ERR_UNSUPPORTED
+    assert sc.sc_scan_segmented(sc.SC_I64, sc.SC_XOR, 0, 0, 0, 0, 0, 0) == sc.SC_OK
     # tuning and test hooks
     assert sc.sc_set_scan_variant(99) == sc.SC_ERR_INVALID
     st, t, i, l = sc.sc_scan_variant_info(0)

@@ -40,3 +40,11 @@ def test_distributions():
     assert w.max() > np.uint64(1 << 63) and w.min() < np.uint64(1 << 60)
     m = synth.maxcount_pairs_np(n, seed=8)
     assert m[:, 0].min() == 0 and m[:, 0].max() == 1023 and np.all(m[:, 1] == 1)
+
+
+def test_head_flags_agree_and_density():
+    spec = synth.WORKLOADS["int32_segsum_n2^27"]
+    a = synth.make_heads_np(spec, 300007)
+    b = synth.make_heads_torch(spec, 300007).numpy()
+    assert a.dtype == np.uint8 and np.array_equal(a, b)
+    assert abs(a.mean() * 1024 - 1) < 0.1
