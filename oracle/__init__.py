@@ -100,6 +100,10 @@ def load_library(path: str) -> ctypes.CDLL:
         f = getattr(lib, name)
         f.argtypes = [P, P, I64]
         f.restype = None
+    lib.oracle_histogram.argtypes = [P, I64, I64, P]
+    lib.oracle_histogram.restype = I64
+    lib.oracle_bin_offsets.argtypes = [P, I64, I64, P, P]
+    lib.oracle_bin_offsets.restype = I64
     return lib
 
 
@@ -228,6 +232,24 @@ class Oracle:
         getattr(self.c, name)(_ptr(xs), _ptr(h), _ptr(y), n, ex)
         return y if y.dtype == np.float64 and x.dtype == np.float32 else y.view(x.dtype)
 
+    # -- histogram and bin offsets ------------------------------------------
+    def histogram(self, bins: np.ndarray, nbins: int):
+        """(counts int64[nbins], entries outside [0, nbins))."""
+        b = np.ascontiguousarray(bins, dtype=np.int32)
+        counts = np.empty(max(nbins, 0), dtype=np.int64)
+        outside = self.c.oracle_histogram(_ptr(b), b.size, nbins, _ptr(counts))
+        return counts, int(outside)
+
+    def bin_offsets(self, bins: np.ndarray, nbins: int):
+        """(offsets int64[nbins + 1], entries outside [0, nbins)): the exclusive
+        scan of the histogram, the number of counted entries last (COO row
+        indices -> CSR row offsets)."""
+        b = np.ascontiguousarray(bins, dtype=np.int32)
+        counts = np.empty(max(nbins, 0), dtype=np.int64)
+        offsets = np.empty(nbins + 1, dtype=np.int64)
+        outside = self.c.oracle_bin_offsets(_ptr(b), b.size, nbins, _ptr(counts), _ptr(offsets))
+        return offsets, int(outside)
+
     # -- compaction ----------------------------------------------------------
     def compact(self, x: np.ndarray, pred: str, threshold: float):
         """Order-preserving compaction; returns (kept values, count)."""
@@ -278,6 +300,14 @@ def scan_segmented(x, heads, op, exclusive):
 
 def compact(x, pred, threshold):
     return default().compact(x, pred, threshold)
+
+
+def histogram(bins, nbins):
+    return default().histogram(bins, nbins)
+
+
+def bin_offsets(bins, nbins):
+    return default().bin_offsets(bins, nbins)
 
 
 def abs_prefix(x):

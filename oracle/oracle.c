@@ -389,6 +389,41 @@ void oracle_segscan_maxcount_i32(const uint32_t *x, const uint8_t *h, uint32_t *
     }
 }
 
+/* ---- histogram and bin offsets ([PMPP] section 4.2 lists, among the uses of
+ *      scan: a radix sort's digit pass scans the digit histogram to find where
+ *      each bucket starts, and converting a sparse matrix from COO to CSR scans
+ *      the per-row entry counts to get the row offsets).
+ *      counts[b] = number of i with bins[i] == b, for 0 <= b < nbins; entries
+ *      outside [0, nbins) are not counted (the return value says how many).
+ *      offsets[b] = counts[0] + ... + counts[b-1] (exclusive scan), with
+ *      offsets[nbins] = the number of counted entries. ---- */
+
+int64_t oracle_histogram(const int32_t *bins, int64_t n, int64_t nbins, int64_t *counts)
+{
+    int64_t outside = 0;
+    for (int64_t b = 0; b < nbins; ++b)
+        counts[b] = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        if (bins[i] >= 0 && bins[i] < nbins)
+            counts[bins[i]] += 1;
+        else
+            outside += 1;
+    }
+    return outside;
+}
+
+int64_t oracle_bin_offsets(const int32_t *bins, int64_t n, int64_t nbins, int64_t *counts, int64_t *offsets)
+{
+    const int64_t outside = oracle_histogram(bins, n, nbins, counts);
+    int64_t acc = 0;
+    for (int64_t b = 0; b < nbins; ++b) {
+        offsets[b] = acc;
+        acc += counts[b];
+    }
+    offsets[nbins] = acc;
+    return outside;
+}
+
 /* ---- batched rows: the same scan on each row of a row-major rows x cols
  *      matrix, the accumulator starting again from the identity at each row
  *      (no passage on the pages; the plain reading of "independent scans") ---- */

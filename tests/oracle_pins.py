@@ -675,6 +675,38 @@ def pin_segmented_first_satisfying(o):
     assert first.tolist() == want
 
 
+# ------------------------------------------------- histogram and bin offsets
+def pin_histogram_and_bin_offsets(o):
+    rng = np.random.default_rng(41)
+    for n, nbins in ((0, 5), (1, 1), (1000, 7), (50000, 256), (30011, 100000)):
+        bins = rng.integers(-3, nbins + 3, n).astype(np.int32)
+        counts, outside = o.histogram(bins, nbins)
+        inside = bins[(bins >= 0) & (bins < nbins)]
+        # numpy's bincount is the same histogram computed another way
+        assert np.array_equal(counts, np.bincount(inside, minlength=nbins).astype(np.int64))
+        assert outside == n - inside.size
+        offsets, outside2 = o.bin_offsets(bins, nbins)
+        assert outside2 == outside and offsets.size == nbins + 1
+        assert offsets[0] == 0 and offsets[-1] == inside.size
+        assert np.array_equal(np.diff(offsets), counts)
+        # for sorted bins the offsets are where each bin starts (searchsorted), the CSR row pointers
+        srt = np.sort(inside)
+        assert np.array_equal(offsets, np.searchsorted(srt, np.arange(nbins + 1), side="left"))
+    # the pages' radix-sort use: bucket starts are the exclusive scan of the digit histogram
+    keys = rng.integers(0, 1 << 32, 20000, dtype=np.uint64).astype(np.uint32)
+    digit = (keys >> np.uint32(8)) & np.uint32(255)
+    starts, _ = o.bin_offsets(digit.astype(np.int32), 256)
+    order = np.argsort(digit, kind="stable")
+    sd = digit[order]
+    for d in (0, 17, 255):
+        hit = np.flatnonzero(sd == d)
+        if hit.size:
+            assert hit[0] == starts[d] and hit[-1] == starts[d + 1] - 1
+    # COO -> CSR on a small matrix written out by hand: rows of the entries, 4 rows
+    rows = np.array([0, 0, 1, 3, 3, 3], dtype=np.int32)
+    assert o.bin_offsets(rows, 4)[0].tolist() == [0, 2, 3, 3, 6]
+
+
 ALL_PINS = [
     pin_golden_sum_examples, pin_golden_compaction_examples, pin_golden_identities,
     pin_closed_forms, pin_affine_special_cases, pin_invariants, pin_affine_recurrence,
@@ -682,5 +714,5 @@ ALL_PINS = [
     pin_brute_force_sum, pin_brute_force_max, pin_brute_force_affine, pin_brute_force_compaction,
     pin_golden_identities_more, pin_closed_forms_more, pin_library_special_cases_more, pin_float64_sum,
     pin_brute_force_more, pin_segmented_is_scan_per_segment, pin_segmented_special_cases,
-    pin_segmented_brute_force, pin_segmented_first_satisfying,
+    pin_segmented_brute_force, pin_segmented_first_satisfying, pin_histogram_and_bin_offsets,
 ]

@@ -59,6 +59,10 @@ MUTANTS = {
                        "static double min_f64(double acc, double x) { if (isnan(acc)) return acc; if (isnan(x)) return x; return x <= acc ? x : acc; }"),
     # (max, count): equal values do not add their counts
     "maxcount_ties_not_added": ("        *acc_c = *acc_c + c;", "        *acc_c = c;"),
+    # bin offsets that include the bin's own count (inclusive instead of exclusive)
+    "bin_offsets_inclusive": ("        offsets[b] = acc;\n        acc += counts[b];", "        acc += counts[b];\n        offsets[b] = acc;"),
+    # histogram that drops bin 0
+    "histogram_drops_bin0": ("        if (bins[i] >= 0 && bins[i] < nbins)", "        if (bins[i] > 0 && bins[i] < nbins)"),
     # segmented scan that ignores the head flags
     "segscan_no_reset": ("            if (h[i])                                                                    \\\n                acc = (IDENT);",
                          "            if (0)                                                                       \\\n                acc = (IDENT);"),
