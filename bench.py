@@ -319,6 +319,13 @@ def suite_lines(args, dev, sc, synth):
     ms, b = timed(lambda: sc.sc_scan_segmented(sc.SC_I32, sc.SC_SUM, 1, x.data_ptr(), h.data_ptr(), y.data_ptr(), n,
                                                sp), 9 * n)
     emit("int32_segsum_n2^27", n, ms, b, {"segments": int(h.sum().item())})
+    # bin offsets (histogram + exclusive scan): CSR row offsets of a COO matrix, radix digit bucket starts
+    for name, nbins in (("csr_rows_2^22", W["csr_rows_2^22"]["nrows"]), ("digit_bins_n2^27", 256)):
+        bins = synth.make_torch(W[name], device=dev)
+        offs = torch.empty(nbins + 1, dtype=torch.int64, device=dev)
+        n = bins.numel()
+        ms, b = timed(lambda: sc.sc_bin_offsets(bins.data_ptr(), n, nbins, offs.data_ptr(), sp), 4 * n + 8 * (nbins + 1))
+        emit(name, n, ms, b, {"nbins": nbins, "note": "bytes: bins read once, offsets written once"})
     del flush
 
 

@@ -166,6 +166,23 @@ sc_status sc_scan_batched(sc_dtype dtype, sc_op op, int exclusive, const void *i
 sc_status sc_scan_segmented(sc_dtype dtype, sc_op op, int exclusive, const void *in, const uint8_t *d_heads,
                             void *out, int64_t n, sc_stream_t stream);
 
+/* Histogram of int32 bin indices: d_counts[b] (int64, nbins entries) = the
+ * number of i with d_bins[i] == b, 0 <= b < nbins; entries outside [0, nbins)
+ * are skipped.  1 <= nbins < 2^31; d_counts must not overlap d_bins.  One
+ * memset and one kernel launch (equal bins of a warp share one atomic; up to
+ * 32768 bins each CTA counts in shared memory first). */
+sc_status sc_histogram(const int32_t *d_bins, int64_t n, int64_t nbins, int64_t *d_counts, sc_stream_t stream);
+
+/* Bin offsets: d_offsets[b] (int64, nbins + 1 entries) = the number of i with
+ * 0 <= d_bins[i] < b, i.e. the exclusive scan of the histogram, and
+ * d_offsets[nbins] = the number of entries inside [0, nbins).  With d_bins =
+ * the row indices of a COO sparse matrix and nbins = its row count these are
+ * the CSR row offsets; with d_bins = a radix digit of each key, the start of
+ * each bucket ("Chapter 9 Parallel Patterns: Prefix Sum - Scan Algorithms",
+ * PMPP notes, section 4.2).  The histogram above, then the int64 exclusive
+ * scan in place. */
+sc_status sc_bin_offsets(const int32_t *d_bins, int64_t n, int64_t nbins, int64_t *d_offsets, sc_stream_t stream);
+
 /* Fused, order-preserving stream compaction (one kernel launch): out[0..count)
  * receives, in input order, every in[i] with (in[i] <pred> threshold); the
  * number kept is written to *d_count (device int64).  out[count..n) is left

@@ -47,6 +47,8 @@ SIGNATURES = {
     "sc_scan_host": ([_INT, _INT, _INT, _P, _P, _I64, _P], _INT),
     "sc_scan_noalloc": ([_INT, _INT, _INT, _P, _P, _I64, _P], _INT),
     "sc_scan_segmented": ([_INT, _INT, _INT, _P, _P, _P, _I64, _P], _INT),
+    "sc_histogram": ([_P, _I64, _I64, _P, _P], _INT),
+    "sc_bin_offsets": ([_P, _I64, _I64, _P, _P], _INT),
     "sc_get_device_error": ([_P], _INT),
     "sc_launch_count": ([], _U64),
     "sc_set_scan_variant": ([_INT], _INT),
@@ -265,6 +267,42 @@ def scan_segmented(x, heads, op: str = "sum", exclusive: bool = True, out=None, 
         raise ValueError("heads must be contiguous")
     _check(sc_scan_segmented(_dtype_code(x, op), _OPS[op], int(exclusive), x.data_ptr(), heads.data_ptr(),
                              out.data_ptr(), n, _stream(stream)), "sc_scan_segmented")
+    return out
+
+
+def sc_histogram(d_bins: int, n: int, nbins: int, d_counts: int, stream: int) -> int:
+    return load().sc_histogram(d_bins, n, nbins, d_counts, stream)
+
+
+def sc_bin_offsets(d_bins: int, n: int, nbins: int, d_offsets: int, stream: int) -> int:
+    return load().sc_bin_offsets(d_bins, n, nbins, d_offsets, stream)
+
+
+def _bins_tensor(bins):
+    import torch
+    if not bins.is_cuda or bins.dtype != torch.int32 or not bins.is_contiguous():
+        raise ValueError("bins must be a contiguous CUDA int32 tensor")
+    return bins
+
+
+def histogram(bins, nbins: int, out=None, stream=None):
+    """int64 counts of each bin 0 .. nbins-1 in a CUDA int32 tensor (others skipped)."""
+    import torch
+    _bins_tensor(bins)
+    if out is None:
+        out = torch.empty(nbins, dtype=torch.int64, device=bins.device)
+    _check(sc_histogram(bins.data_ptr(), bins.numel(), nbins, out.data_ptr(), _stream(stream)), "sc_histogram")
+    return out
+
+
+def bin_offsets(bins, nbins: int, out=None, stream=None):
+    """int64 offsets (nbins + 1): exclusive scan of the histogram, total last
+    (COO row indices -> CSR row pointers)."""
+    import torch
+    _bins_tensor(bins)
+    if out is None:
+        out = torch.empty(nbins + 1, dtype=torch.int64, device=bins.device)
+    _check(sc_bin_offsets(bins.data_ptr(), bins.numel(), nbins, out.data_ptr(), _stream(stream)), "sc_bin_offsets")
     return out
 
 

@@ -462,6 +462,47 @@ sc_status sc_scan_exclusive(sc_dtype dtype, sc_op op, const void* in, void* out,
     return scan_common(dtype, op, in, out, n, stream, true);
 }
 
+// ---------------------------------------------------- histogram, bin offsets
+static sc_status check_hist_args(const int32_t* bins, int64_t n, int64_t nbins, const int64_t* out, int64_t out_len) {
+    if (n < 0 || nbins < 1 || nbins > (int64_t)INT32_MAX - 1) return SC_ERR_INVALID;
+    if (!out || !aligned(out, 8)) return SC_ERR_INVALID;
+    if (n == 0) return SC_OK;
+    if (!bins || !aligned(bins, 4)) return SC_ERR_INVALID;
+    const uintptr_t b = reinterpret_cast<uintptr_t>(bins), o = reinterpret_cast<uintptr_t>(out);
+    if (b < o + (size_t)out_len * 8 && o < b + (size_t)n * 4) return SC_ERR_INVALID;  // the output must not overlap the bins
+    return SC_OK;
+}
+
+// counts[0..zero_len) = 0, then counts[b] += occurrences of b in bins, 0 <= b < nbins.
+static sc_status count_bins(const int32_t* bins, int64_t n, int64_t nbins, int64_t* counts, int64_t zero_len,
+                            cudaStream_t s) {
+    if (cudaMemsetAsync(counts, 0, (size_t)zero_len * 8, s) != cudaSuccess) return SC_ERR_CUDA;
+    if (n == 0) return SC_OK;
+    const int sms = num_sms();
+    if (sms <= 0) return SC_ERR_CUDA;
+    const cudaError_t e =
+        scg::launch_histogram(bins, n, (int)nbins, reinterpret_cast<unsigned long long*>(counts), sms, s);
+    g_launches.fetch_add(1);
+    return e == cudaSuccess ? SC_OK : SC_ERR_CUDA;
+}
+
+sc_status sc_histogram(const int32_t* d_bins, int64_t n, int64_t nbins, int64_t* d_counts, sc_stream_t stream) {
+    const sc_status st = check_hist_args(d_bins, n, nbins, d_counts, nbins);
+    if (st != SC_OK) return st;
+    return count_bins(d_bins, n, nbins, d_counts, nbins, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sc_status sc_bin_offsets(const int32_t* d_bins, int64_t n, int64_t nbins, int64_t* d_offsets, sc_stream_t stream) {
+    const sc_status st = check_hist_args(d_bins, n, nbins, d_offsets, nbins + 1);
+    if (st != SC_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // counts in offsets[0..nbins), 0 in offsets[nbins]; the exclusive scan in
+    // place then leaves the total in offsets[nbins]
+    const sc_status r = count_bins(d_bins, n, nbins, d_offsets, nbins + 1, s);
+    if (r != SC_OK) return r;
+    return run_scan(scg::OID_SUM_U64, d_offsets, d_offsets, nbins + 1, 0, true, nullptr, nullptr, s);
+}
+
 sc_status sc_scan_segmented(sc_dtype dtype, sc_op op, int exclusive, const void* in, const uint8_t* d_heads,
                             void* out, int64_t n, sc_stream_t stream) {
     int oid = -1;

@@ -109,6 +109,11 @@ int compact_tma_chunk_tiles();
 template <class T>
 cudaError_t launch_compact_tma(const CompactParams& p, bool wide_count, unsigned grid, cudaStream_t s, int shape);
 
+// Histogram of int32 bins into uint64 counts (which the caller has zeroed);
+// entries outside [0, nbins) are skipped.
+cudaError_t launch_histogram(const int32_t* bins, long long n, int nbins, unsigned long long* counts, int num_sms,
+                             cudaStream_t s);
+
 // Hierarchical (scan-then-propagate) comparison variant.
 constexpr int kHierNT = 256;
 int hier_tile_elems(int op_id);

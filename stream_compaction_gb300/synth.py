@@ -22,7 +22,9 @@ Mappings from the 64-bit draw ``r``:
   * full-range 64-bit words:  r;
   * float64 uniform on [-1, 1):  (r >> 11) * 2**-52 - 1  (exact in float64);
   * (value, count) pairs:  value = r mod 1024, count = 1;
-  * segment head flags with mean segment length L:  1 if r mod L == 0, else 0.
+  * segment head flags with mean segment length L:  1 if r mod L == 0, else 0;
+  * COO row indices of a sparse matrix with rows sorted: row r holds
+    1 + (r_r mod 63) entries (r_r the draw of row r), so 32 on average.
 ``offset`` selects a substream (2**40 for the second workload drawn from the
 same seed).
 """
@@ -92,6 +94,11 @@ def maxcount_pairs_np(n, seed, offset=0):
 
 def head_flags_np(n, seed, offset=0, period=1024):
     return (draws_np(n, seed, offset) % np.uint64(period) == 0).astype(np.uint8)
+
+
+def coo_rows_np(nrows, seed, offset=0):
+    lengths = (draws_np(nrows, seed, offset) % np.uint64(63)).astype(np.int64) + 1
+    return np.repeat(np.arange(nrows, dtype=np.int32), lengths)
 
 
 # --------------------------------------------------------------- torch (device)
@@ -212,6 +219,13 @@ def head_flags_torch(n, seed, offset=0, period=1024, device="cpu"):
     return _chunked(n, f, out)
 
 
+def coo_rows_torch(nrows, seed, offset=0, device="cpu"):
+    import torch
+    r = draws_torch(nrows, seed, offset, 0, device)
+    lengths = ((_lsr(r, 32) % 63) * ((1 << 32) % 63) + (r & 0xFFFFFFFF)) % 63 + 1
+    return torch.repeat_interleave(torch.arange(nrows, dtype=torch.int32, device=device), lengths)
+
+
 # ------------------------------------------------------------- named workloads
 # The benchmark workloads (sizes, distributions and seeds), as data: the five
 # configurations of the headline metric, then one per family of added operators
@@ -233,6 +247,10 @@ WORKLOADS = {
     # segmented sum: values as the batched rows, heads with mean segment length 1024
     "int32_segsum_n2^27": dict(kind="int", n=1 << 27, lo=0, hi=255, seed=9, offset=0, op="sum",
                                heads=dict(seed=9, offset=SUBSTREAM, period=1024)),
+    # bin offsets: the CSR row offsets of a COO matrix with 2^22 sorted rows
+    # (about 2^27 entries), and the start of each bucket of an 8-bit radix digit
+    "csr_rows_2^22": dict(kind="coo_rows", nrows=1 << 22, seed=10, offset=0),
+    "digit_bins_n2^27": dict(kind="int", n=1 << 27, lo=0, hi=255, seed=11, offset=0, nbins=256),
 }
 
 
@@ -247,7 +265,7 @@ def make_heads_torch(spec: dict, n: int | None = None, device="cpu"):
 
 
 def make_np(spec: dict, n: int | None = None):
-    n = spec["n"] if n is None else n
+    n = spec.get("n") if n is None else n
     k = spec["kind"]
     if k == "int":
         return uniform_int_np(n, spec["lo"], spec["hi"], spec["seed"], spec["offset"])
@@ -263,11 +281,13 @@ def make_np(spec: dict, n: int | None = None):
         return uniform_pm1_f64_np(n, spec["seed"], spec["offset"])
     if k == "maxcount":
         return maxcount_pairs_np(n, spec["seed"], spec["offset"])
+    if k == "coo_rows":
+        return coo_rows_np(spec["nrows"], spec["seed"], spec["offset"])
     raise ValueError(k)
 
 
 def make_torch(spec: dict, n: int | None = None, device="cpu"):
-    n = spec["n"] if n is None else n
+    n = spec.get("n") if n is None else n
     k = spec["kind"]
     if k == "int":
         return uniform_int_torch(n, spec["lo"], spec["hi"], spec["seed"], spec["offset"], device)
@@ -283,4 +303,6 @@ def make_torch(spec: dict, n: int | None = None, device="cpu"):
         return uniform_pm1_f64_torch(n, spec["seed"], spec["offset"], device)
     if k == "maxcount":
         return maxcount_pairs_torch(n, spec["seed"], spec["offset"], device)
+    if k == "coo_rows":
+        return coo_rows_torch(spec["nrows"], spec["seed"], spec["offset"], device)
     raise ValueError(k)

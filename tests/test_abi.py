@@ -85,6 +85,12 @@ def test_host_side_argument_checks(lib):
     assert sc.sc_scan_segmented(sc.SC_I32, sc.SC_SUM, 1, 0x1000, 0x9004, 0x9000, 16, 0) == sc.SC_ERR_INVALID
     assert sc.sc_scan_segmented(sc.SC_I32, sc.SC_COMPOSE, 1, 0x1000, 0x20000, 0x9000, 16, 0) == sc.SC_ERR_UNSUPPORTED
     assert sc.sc_scan_segmented(sc.SC_I64, sc.SC_XOR, 0, 0, 0, 0, 0, 0) == sc.SC_OK
+    # histogram / bin offsets
+    assert sc.sc_histogram(0x1000, 10, 0, 0x8000, 0) == sc.SC_ERR_INVALID            # no bins
+    assert sc.sc_histogram(0x1000, -1, 5, 0x8000, 0) == sc.SC_ERR_INVALID
+    assert sc.sc_histogram(0x1000, 10, 5, 0x8004, 0) == sc.SC_ERR_INVALID            # misaligned counts
+    assert sc.sc_bin_offsets(0x1000, 10, 5, 0x1008, 0) == sc.SC_ERR_INVALID          # overlaps the bins
+    assert sc.sc_bin_offsets(0x1002, 10, 5, 0x8000, 0) == sc.SC_ERR_INVALID          # misaligned bins
     # tuning and test hooks
     assert sc.sc_set_scan_variant(99) == sc.SC_ERR_INVALID
     st, t, i, l = sc.sc_scan_variant_info(0)

@@ -16,6 +16,8 @@ def test_splitmix64_reference_values():
 def test_numpy_and_torch_agree(name):
     spec = synth.WORKLOADS[name]
     n = 100003
+    if spec["kind"] == "coo_rows":
+        spec = dict(spec, nrows=5000)
     a = synth.make_np(spec, n)
     b = synth.make_torch(spec, n, device="cpu").numpy()
     if a.dtype in (np.uint32, np.uint64):
@@ -48,3 +50,10 @@ def test_head_flags_agree_and_density():
     b = synth.make_heads_torch(spec, 300007).numpy()
     assert a.dtype == np.uint8 and np.array_equal(a, b)
     assert abs(a.mean() * 1024 - 1) < 0.1
+
+
+def test_coo_rows():
+    rows = synth.coo_rows_np(10000, seed=10)
+    assert rows.dtype == np.int32 and np.all(np.diff(rows) >= 0)
+    lengths = np.bincount(rows, minlength=10000)
+    assert lengths.min() >= 1 and lengths.max() <= 63 and abs(lengths.mean() - 32) < 1
