@@ -100,6 +100,10 @@ def load_library(path: str) -> ctypes.CDLL:
         f = getattr(lib, name)
         f.argtypes = [P, P, I64]
         f.restype = None
+    lib.oracle_radix_pass_u32.argtypes = [P, P, I64, INT, INT]
+    lib.oracle_radix_pass_u32.restype = None
+    lib.oracle_radix_sort_u32.argtypes = [P, P, P, I64]
+    lib.oracle_radix_sort_u32.restype = None
     lib.oracle_histogram.argtypes = [P, I64, I64, P]
     lib.oracle_histogram.restype = I64
     lib.oracle_bin_offsets.argtypes = [P, I64, I64, P, P]
@@ -250,6 +254,24 @@ class Oracle:
         outside = self.c.oracle_bin_offsets(_ptr(b), b.size, nbins, _ptr(counts), _ptr(offsets))
         return offsets, int(outside)
 
+    # -- radix sort ------------------------------------------------------------
+    def radix_pass(self, keys: np.ndarray, shift: int, bits: int) -> np.ndarray:
+        """One stable counting-sort pass of uint32 keys by (k >> shift) & (2^bits - 1), 1 <= bits <= 8."""
+        if not (1 <= bits <= 8 and 0 <= shift <= 31):
+            raise ValueError("bits in [1, 8], shift in [0, 31]")
+        k = np.ascontiguousarray(keys, dtype=np.uint32)
+        out = np.empty_like(k)
+        self.c.oracle_radix_pass_u32(_ptr(k), _ptr(out), k.size, shift, bits)
+        return out
+
+    def radix_sort(self, keys: np.ndarray) -> np.ndarray:
+        """uint32 keys sorted ascending by four 8-bit passes."""
+        k = np.ascontiguousarray(keys, dtype=np.uint32)
+        out = np.empty_like(k)
+        tmp = np.empty_like(k)
+        self.c.oracle_radix_sort_u32(_ptr(k), _ptr(out), _ptr(tmp), k.size)
+        return out
+
     # -- compaction ----------------------------------------------------------
     def compact(self, x: np.ndarray, pred: str, threshold: float):
         """Order-preserving compaction; returns (kept values, count)."""
@@ -304,6 +326,14 @@ def compact(x, pred, threshold):
 
 def histogram(bins, nbins):
     return default().histogram(bins, nbins)
+
+
+def radix_pass(keys, shift, bits):
+    return default().radix_pass(keys, shift, bits)
+
+
+def radix_sort(keys):
+    return default().radix_sort(keys)
 
 
 def bin_offsets(bins, nbins):

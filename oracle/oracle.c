@@ -424,6 +424,43 @@ int64_t oracle_bin_offsets(const int32_t *bins, int64_t n, int64_t nbins, int64_
     return outside;
 }
 
+/* ---- radix sort ([L7] section 2: a radix sort makes one pass per digit, a
+ *      split by the digit whose placement is a scan; [PMPP] section 4.2: the
+ *      scan of the digit histogram gives where each bucket starts).  One pass:
+ *      a stable counting sort of the keys by d(k) = (k >> shift) & (2^bits - 1):
+ *      count each digit, exclusive-scan the counts into bucket starts, then
+ *      place the keys in input order, each at the next free slot of its bucket.
+ *      A full sort of 32-bit keys is four 8-bit passes, least significant first. ---- */
+
+void oracle_radix_pass_u32(const uint32_t *in, uint32_t *out, int64_t n, int shift, int bits)
+{
+    const uint32_t mask = (bits >= 32) ? 0xFFFFFFFFu : ((1u << bits) - 1u);
+    const int64_t nb = (int64_t)1 << bits;
+    int64_t count[256] = {0};
+    int64_t start[256];
+    for (int64_t i = 0; i < n; ++i)
+        count[(in[i] >> shift) & mask] += 1;
+    int64_t acc = 0;
+    for (int64_t d = 0; d < nb; ++d) {
+        start[d] = acc;
+        acc += count[d];
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        const uint32_t d = (in[i] >> shift) & mask;
+        out[start[d]] = in[i];
+        start[d] += 1;
+    }
+}
+
+/* keys sorted ascending; tmp has room for n keys */
+void oracle_radix_sort_u32(const uint32_t *in, uint32_t *out, uint32_t *tmp, int64_t n)
+{
+    oracle_radix_pass_u32(in, tmp, n, 0, 8);
+    oracle_radix_pass_u32(tmp, out, n, 8, 8);
+    oracle_radix_pass_u32(out, tmp, n, 16, 8);
+    oracle_radix_pass_u32(tmp, out, n, 24, 8);
+}
+
 /* ---- batched rows: the same scan on each row of a row-major rows x cols
  *      matrix, the accumulator starting again from the identity at each row
  *      (no passage on the pages; the plain reading of "independent scans") ---- */

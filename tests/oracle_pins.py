@@ -707,6 +707,25 @@ def pin_histogram_and_bin_offsets(o):
     assert o.bin_offsets(rows, 4)[0].tolist() == [0, 2, 3, 3, 6]
 
 
+# ----------------------------------------------------------------- radix sort
+def pin_radix_pass_and_sort(o):
+    rng = np.random.default_rng(51)
+    for n in (0, 1, 2, 17, 1000, 65537):
+        keys = rng.integers(0, 1 << 32, n, dtype=np.uint64).astype(np.uint32)
+        keys[: n // 3] &= np.uint32(0x00FF00FF)          # repeated digits
+        for shift, bits in ((0, 8), (8, 8), (24, 8), (3, 5), (31, 1), (28, 4)):
+            got = o.radix_pass(keys, shift, bits)
+            digit = (keys >> np.uint32(shift)) & np.uint32((1 << bits) - 1)
+            # a stable partition by the digit is numpy's stable argsort of the digits
+            assert np.array_equal(got, keys[np.argsort(digit, kind="stable")]), (n, shift, bits)
+        # four 8-bit passes sort the keys
+        assert np.array_equal(o.radix_sort(keys), np.sort(keys)), n
+    # stability, by hand: equal digits keep their input order
+    keys = np.array([0x102, 0x001, 0x201, 0x002, 0x101], dtype=np.uint32)
+    assert o.radix_pass(keys, 0, 8).tolist() == [0x001, 0x201, 0x101, 0x102, 0x002]
+    assert o.radix_pass(keys, 8, 8).tolist() == [0x001, 0x002, 0x102, 0x101, 0x201]
+
+
 ALL_PINS = [
     pin_golden_sum_examples, pin_golden_compaction_examples, pin_golden_identities,
     pin_closed_forms, pin_affine_special_cases, pin_invariants, pin_affine_recurrence,
@@ -715,4 +734,5 @@ ALL_PINS = [
     pin_golden_identities_more, pin_closed_forms_more, pin_library_special_cases_more, pin_float64_sum,
     pin_brute_force_more, pin_segmented_is_scan_per_segment, pin_segmented_special_cases,
     pin_segmented_brute_force, pin_segmented_first_satisfying, pin_histogram_and_bin_offsets,
+    pin_radix_pass_and_sort,
 ]

@@ -63,6 +63,12 @@ MUTANTS = {
     "bin_offsets_inclusive": ("        offsets[b] = acc;\n        acc += counts[b];", "        acc += counts[b];\n        offsets[b] = acc;"),
     # histogram that drops bin 0
     "histogram_drops_bin0": ("        if (bins[i] >= 0 && bins[i] < nbins)", "        if (bins[i] > 0 && bins[i] < nbins)"),
+    # radix pass that places keys in reverse input order inside a bucket (not stable)
+    "radix_not_stable": ("        out[start[d]] = in[i];\n        start[d] += 1;",
+                         "        out[start[d] + count[d] - 1] = in[i];\n        count[d] -= 1;"),
+    # radix sort whose passes run most significant digit first
+    "radix_msd_first": ("    oracle_radix_pass_u32(in, tmp, n, 0, 8);\n    oracle_radix_pass_u32(tmp, out, n, 8, 8);",
+                        "    oracle_radix_pass_u32(in, tmp, n, 24, 8);\n    oracle_radix_pass_u32(tmp, out, n, 8, 8);"),
     # segmented scan that ignores the head flags
     "segscan_no_reset": ("            if (h[i])                                                                    \\\n                acc = (IDENT);",
                          "            if (0)                                                                       \\\n                acc = (IDENT);"),
