@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--suite", action="store_true")
     ap.add_argument("--profile-case", type=int, default=0, metavar="N",
                     help="no timing: run the headline scan on the first N elements --steps times (for ncu)")
-    ap.add_argument("--profile-op", default="scan", choices=["scan", "compact", "rows", "hier"],
+    ap.add_argument("--profile-op", default="scan", choices=["scan", "compact", "rows", "hier", "radix", "sort"],
                     help="which kernel --profile-case runs")
     ap.add_argument("--compact-variant", type=int, default=0,
                     help="compaction kernel for --profile-op compact (sc_set_compact_variant)")
@@ -326,6 +326,15 @@ def suite_lines(args, dev, sc, synth):
         n = bins.numel()
         ms, b = timed(lambda: sc.sc_bin_offsets(bins.data_ptr(), n, nbins, offs.data_ptr(), sp), 4 * n + 8 * (nbins + 1))
         emit(name, n, ms, b, {"nbins": nbins, "note": "bytes: bins read once, offsets written once"})
+    # radix sort of 32-bit keys: four passes of (count read, place read + write)
+    k = synth.make_torch(W["uint32_sort_n2^27"], device=dev)
+    ko = torch.empty_like(k)
+    kt = torch.empty_like(k)
+    n = k.numel()
+    ms, b = timed(lambda: sc.sc_radix_sort_u32(k.data_ptr(), ko.data_ptr(), kt.data_ptr(), n, sp), 48 * n, steps=10)
+    emit("uint32_sort_n2^27", n, ms, b, {"passes": 4, "note": "bytes: 4 x (count read + place read + write)"})
+    ms, b = timed(lambda: sc.sc_radix_pass_u32(k.data_ptr(), ko.data_ptr(), n, 8, 8, sp), 12 * n, steps=10)
+    emit("uint32_radix_pass_n2^27", n, ms, b, {"note": "bytes: count read + place read + write"})
     del flush
 
 
@@ -504,6 +513,13 @@ def profile_case(args):
         x = synth.make_torch(synth.WORKLOADS["int32_rows_65536x4096"], n=n, device="cuda")
         y = torch.empty_like(x)
         run = lambda: sc.sc_scan_batched(sc.SC_I32, sc.SC_SUM, 1, x.data_ptr(), y.data_ptr(), n // cols, cols, sp)
+    elif args.profile_op in ("radix", "sort"):
+        k = synth.make_torch(synth.WORKLOADS["uint32_sort_n2^27"], n=n, device="cuda")
+        ko, kt = torch.empty_like(k), torch.empty_like(k)
+        if args.profile_op == "radix":
+            run = lambda: sc.sc_radix_pass_u32(k.data_ptr(), ko.data_ptr(), n, 8, 8, sp)
+        else:
+            run = lambda: sc.sc_radix_sort_u32(k.data_ptr(), ko.data_ptr(), kt.data_ptr(), n, sp)
     else:
         x = synth.make_torch(synth.WORKLOADS[WORKLOAD], n=n, device="cuda")
         y = torch.empty_like(x)

@@ -114,7 +114,8 @@ typedef enum {
     SC_ERR_UNSUPPORTED = 2,      /* valid enums, but this (dtype, op) is not provided */
     SC_ERR_WORKSPACE = 3,        /* caller-bound workspace too small, or allocation failed */
     SC_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed */
-    SC_ERR_LOOKBACK_TIMEOUT = 5  /* a kernel gave up waiting on a predecessor tile */
+    SC_ERR_LOOKBACK_TIMEOUT = 5, /* a kernel gave up waiting on a predecessor tile */
+    SC_ERR_INTERNAL = 6          /* a kernel's bounds check caught an out-of-range position (nothing written there) */
 } sc_status;
 
 /* Library version string. */
@@ -182,6 +183,25 @@ sc_status sc_histogram(const int32_t *d_bins, int64_t n, int64_t nbins, int64_t 
  * PMPP notes, section 4.2).  The histogram above, then the int64 exclusive
  * scan in place. */
 sc_status sc_bin_offsets(const int32_t *d_bins, int64_t n, int64_t nbins, int64_t *d_offsets, sc_stream_t stream);
+
+/* Radix sort ("Lecture 7" notes, section 2: one pass per digit, a split whose
+ * placement is a scan; PMPP notes, section 4.2: the scan of the digit
+ * histogram gives each bucket's start).
+ *
+ * sc_radix_pass_u32: one stable counting-sort pass: d_out receives the keys of
+ * d_in ordered by the digit (key >> shift) & (2^bits - 1), keys with equal
+ * digits in their input order.  1 <= bits <= 8, 0 <= shift <= 31,
+ * n < 2^32; d_in and d_out must not overlap.  Three launches over
+ * 4096-key tiles: each tile's digit counts (workspace: 1 KiB per tile, digit
+ * major), their exclusive scan in place (which gives every tile the start of
+ * its run of each digit), the placement.
+ *
+ * sc_radix_sort_u32: d_out = the keys of d_in in ascending order, by four 8-bit
+ * passes (least significant digit first) ping-ponging through d_tmp (n keys);
+ * d_in may equal d_out; d_tmp must overlap neither. */
+sc_status sc_radix_pass_u32(const uint32_t *d_in, uint32_t *d_out, int64_t n, int shift, int bits,
+                            sc_stream_t stream);
+sc_status sc_radix_sort_u32(const uint32_t *d_in, uint32_t *d_out, uint32_t *d_tmp, int64_t n, sc_stream_t stream);
 
 /* Fused, order-preserving stream compaction (one kernel launch): out[0..count)
  * receives, in input order, every in[i] with (in[i] <pred> threshold); the

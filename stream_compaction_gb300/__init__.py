@@ -26,7 +26,8 @@ LIB_PATH = os.path.join(_HERE, "libsc_gb300.so")
 SC_I32, SC_U32, SC_F32, SC_AFFINE_U32, SC_I64, SC_U64, SC_F64, SC_MAXCOUNT_I32 = 0, 1, 2, 3, 4, 5, 6, 7
 SC_SUM, SC_MAX, SC_COMPOSE, SC_MIN, SC_PROD, SC_AND, SC_OR, SC_XOR = 0, 1, 2, 3, 4, 5, 6, 7
 SC_GT, SC_GE, SC_LT, SC_LE, SC_EQ, SC_NE = 0, 1, 2, 3, 4, 5
-SC_OK, SC_ERR_INVALID, SC_ERR_UNSUPPORTED, SC_ERR_WORKSPACE, SC_ERR_CUDA, SC_ERR_LOOKBACK_TIMEOUT = range(6)
+SC_OK, SC_ERR_INVALID, SC_ERR_UNSUPPORTED, SC_ERR_WORKSPACE, SC_ERR_CUDA, SC_ERR_LOOKBACK_TIMEOUT, SC_ERR_INTERNAL = \
+    range(7)
 
 PRED = {"gt": SC_GT, "ge": SC_GE, "lt": SC_LT, "le": SC_LE, "eq": SC_EQ, "ne": SC_NE}
 
@@ -48,6 +49,8 @@ SIGNATURES = {
     "sc_scan_noalloc": ([_INT, _INT, _INT, _P, _P, _I64, _P], _INT),
     "sc_scan_segmented": ([_INT, _INT, _INT, _P, _P, _P, _I64, _P], _INT),
     "sc_histogram": ([_P, _I64, _I64, _P, _P], _INT),
+    "sc_radix_pass_u32": ([_P, _P, _I64, _INT, _INT, _P], _INT),
+    "sc_radix_sort_u32": ([_P, _P, _P, _I64, _P], _INT),
     "sc_bin_offsets": ([_P, _I64, _I64, _P, _P], _INT),
     "sc_get_device_error": ([_P], _INT),
     "sc_launch_count": ([], _U64),
@@ -276,6 +279,26 @@ def sc_histogram(d_bins: int, n: int, nbins: int, d_counts: int, stream: int) ->
 
 def sc_bin_offsets(d_bins: int, n: int, nbins: int, d_offsets: int, stream: int) -> int:
     return load().sc_bin_offsets(d_bins, n, nbins, d_offsets, stream)
+
+
+def sc_radix_pass_u32(d_in: int, d_out: int, n: int, shift: int, bits: int, stream: int) -> int:
+    return load().sc_radix_pass_u32(d_in, d_out, n, shift, bits, stream)
+
+
+def sc_radix_sort_u32(d_in: int, d_out: int, d_tmp: int, n: int, stream: int) -> int:
+    return load().sc_radix_sort_u32(d_in, d_out, d_tmp, n, stream)
+
+
+def radix_sort(keys, out=None, tmp=None, stream=None):
+    """Ascending sort of a CUDA uint32 (or int32 holding uint32 bits) tensor."""
+    import torch
+    if not keys.is_cuda or keys.element_size() != 4 or not keys.is_contiguous():
+        raise ValueError("keys must be a contiguous CUDA tensor of 4-byte unsigned keys")
+    out = torch.empty_like(keys) if out is None else out
+    tmp = torch.empty_like(keys) if tmp is None else tmp
+    _check(sc_radix_sort_u32(keys.data_ptr(), out.data_ptr(), tmp.data_ptr(), keys.numel(), _stream(stream)),
+           "sc_radix_sort_u32")
+    return out
 
 
 def _bins_tensor(bins):

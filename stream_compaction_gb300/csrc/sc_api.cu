@@ -420,6 +420,7 @@ const char* sc_status_string(sc_status s) {
     case SC_ERR_WORKSPACE: return "SC_ERR_WORKSPACE: workspace too small or allocation failed";
     case SC_ERR_CUDA: return "SC_ERR_CUDA: CUDA runtime error";
     case SC_ERR_LOOKBACK_TIMEOUT: return "SC_ERR_LOOKBACK_TIMEOUT: a tile gave up waiting on its predecessors";
+    case SC_ERR_INTERNAL: return "SC_ERR_INTERNAL: a kernel's bounds check caught an out-of-range position";
     default: return "unknown sc_status";
     }
 }
@@ -501,6 +502,69 @@ sc_status sc_bin_offsets(const int32_t* d_bins, int64_t n, int64_t nbins, int64_
     const sc_status r = count_bins(d_bins, n, nbins, d_offsets, nbins + 1, s);
     if (r != SC_OK) return r;
     return run_scan(scg::OID_SUM_U64, d_offsets, d_offsets, nbins + 1, 0, true, nullptr, nullptr, s);
+}
+
+// ------------------------------------------------------------- radix sort
+static bool overlaps(const void* a, size_t abytes, const void* b, size_t bbytes) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + bbytes && y < x + abytes;
+}
+
+// One pass: counts of each tile's digits (digit-major), their exclusive scan in
+// place (bucket start + the earlier tiles' keys of the digit, in one value),
+// then the placement.  The counts live in the stream's workspace after the
+// scan's own status words.
+static sc_status radix_one_pass(const uint32_t* in, uint32_t* out, int64_t n, int shift, uint32_t mask,
+                                cudaStream_t s) {
+    const int64_t ntiles = ceil_div(n, scg::radix_tile_keys());
+    const int64_t m = 256 * ntiles;
+    const size_t counts_off = (lookback_bytes(m) + 255) / 256 * 256;
+    unsigned char* base = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_ws_mu);
+        Workspace* ws = nullptr;
+        const sc_status st = acquire_ws(s, counts_off + (size_t)m * 4, &ws);
+        if (st != SC_OK) return st;
+        base = ws->base;
+    }
+    uint32_t* counts = reinterpret_cast<uint32_t*>(base + counts_off);
+    cudaError_t e = scg::launch_radix_count(in, n, shift, mask, counts, ntiles, s);
+    g_launches.fetch_add(1);
+    if (e != cudaSuccess) return SC_ERR_CUDA;
+    // the scan needs fewer workspace bytes than acquired above: no reallocation
+    sc_status st = run_scan(scg::OID_SUM_U32, counts, counts, m, 0, true, nullptr, nullptr, s);
+    if (st != SC_OK) return st;
+    e = scg::launch_radix_place(in, out, n, shift, mask, counts, ntiles, reinterpret_cast<unsigned int*>(base + 8), s);
+    g_launches.fetch_add(1);
+    return e == cudaSuccess ? SC_OK : SC_ERR_CUDA;
+}
+
+sc_status sc_radix_pass_u32(const uint32_t* d_in, uint32_t* d_out, int64_t n, int shift, int bits,
+                            sc_stream_t stream) {
+    if (n < 0 || n > (int64_t)UINT32_MAX || bits < 1 || bits > 8 || shift < 0 || shift > 31) return SC_ERR_INVALID;
+    if (n == 0) return SC_OK;
+    if (!d_in || !d_out || !aligned(d_in, 4) || !aligned(d_out, 4)) return SC_ERR_INVALID;
+    if (overlaps(d_in, (size_t)n * 4, d_out, (size_t)n * 4)) return SC_ERR_INVALID;
+    return radix_one_pass(d_in, d_out, n, shift, (1u << bits) - 1u, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sc_status sc_radix_sort_u32(const uint32_t* d_in, uint32_t* d_out, uint32_t* d_tmp, int64_t n, sc_stream_t stream) {
+    if (n < 0 || n > (int64_t)UINT32_MAX) return SC_ERR_INVALID;
+    if (n == 0) return SC_OK;
+    if (!d_in || !d_out || !d_tmp || !aligned(d_in, 4) || !aligned(d_out, 4) || !aligned(d_tmp, 4))
+        return SC_ERR_INVALID;
+    const size_t bytes = (size_t)n * 4;
+    if (overlaps(d_tmp, bytes, d_in, bytes) || overlaps(d_tmp, bytes, d_out, bytes)) return SC_ERR_INVALID;
+    if (d_in != d_out && overlaps(d_in, bytes, d_out, bytes)) return SC_ERR_INVALID;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // least significant digit first: in -> tmp -> out -> tmp -> out
+    const uint32_t* src[4] = {d_in, d_tmp, d_out, d_tmp};
+    uint32_t* dst[4] = {d_tmp, d_out, d_tmp, d_out};
+    for (int k = 0; k < 4; ++k) {
+        const sc_status st = radix_one_pass(src[k], dst[k], n, 8 * k, 0xffu, s);
+        if (st != SC_OK) return st;
+    }
+    return SC_OK;
 }
 
 sc_status sc_scan_segmented(sc_dtype dtype, sc_op op, int exclusive, const void* in, const uint8_t* d_heads,

@@ -114,6 +114,15 @@ cudaError_t launch_compact_tma(const CompactParams& p, bool wide_count, unsigned
 cudaError_t launch_histogram(const int32_t* bins, long long n, int nbins, unsigned long long* counts, int num_sms,
                              cudaStream_t s);
 
+// One radix-sort pass of uint32 keys by (k >> shift) & mask over tiles of
+// radix_tile_keys() keys: the tiles' digit counts into counts[d * ntiles + t],
+// then (after an exclusive scan of the counts in place) the placement.
+int radix_tile_keys();
+cudaError_t launch_radix_count(const uint32_t* keys, long long n, int shift, uint32_t mask, uint32_t* counts,
+                               long long ntiles, cudaStream_t s);
+cudaError_t launch_radix_place(const uint32_t* in, uint32_t* out, long long n, int shift, uint32_t mask,
+                               const uint32_t* offsets, long long ntiles, unsigned int* error, cudaStream_t s);
+
 // Hierarchical (scan-then-propagate) comparison variant.
 constexpr int kHierNT = 256;
 int hier_tile_elems(int op_id);

@@ -9,7 +9,7 @@ namespace scg {
 enum : unsigned { ST_INVALID = 0u, ST_AGGREGATE = 1u, ST_PREFIX = 2u, ST_POISON = 3u };
 
 // Device error word values (mirrors sc_status codes of the public header).
-enum : unsigned { DEV_OK = 0u, DEV_LOOKBACK_TIMEOUT = 5u };
+enum : unsigned { DEV_OK = 0u, DEV_LOOKBACK_TIMEOUT = 5u, DEV_INTERNAL = 6u };
 
 struct LookbackCtl {
     unsigned long long* status;     // one (or two) 64-bit words per tile

@@ -251,6 +251,8 @@ WORKLOADS = {
     # (about 2^27 entries), and the start of each bucket of an 8-bit radix digit
     "csr_rows_2^22": dict(kind="coo_rows", nrows=1 << 22, seed=10, offset=0),
     "digit_bins_n2^27": dict(kind="int", n=1 << 27, lo=0, hi=255, seed=11, offset=0, nbins=256),
+    # radix sort: full-range 32-bit keys
+    "uint32_sort_n2^27": dict(kind="u32", n=1 << 27, seed=12, offset=0),
 }
 
 
