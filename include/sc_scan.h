@@ -287,6 +287,11 @@ sc_status sc_set_scan_variant(int variant);
  * one-tile-per-CTA kernel (inputs that are not 16-byte aligned, or smaller than
  * one 32 KiB tile, always use the latter).  SC_ERR_INVALID otherwise. */
 sc_status sc_set_compact_variant(int variant);
+/* Select how the radix pass ranks a warp step's keys by digit: 0 (default)
+ * __match_any_sync on the digit's top 3 bits and one ballot per lower bit;
+ * v = 1..5: v - 1 bits by __match_any_sync, the other 8 - (v - 1) by ballots.
+ * Every variant gives the same (stable) result.  SC_ERR_INVALID otherwise. */
+sc_status sc_set_radix_variant(int variant);
 /* Threads per CTA, items per thread and loader kind (0 direct loads,
  * 1 coalesced loads + shared-memory transpose, 2 persistent TMA pipeline;
  * for 2, threads are the CTA's compute threads) of a uint32-sum variant;

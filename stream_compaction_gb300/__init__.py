@@ -56,6 +56,7 @@ SIGNATURES = {
     "sc_launch_count": ([], _U64),
     "sc_set_scan_variant": ([_INT], _INT),
     "sc_set_compact_variant": ([_INT], _INT),
+    "sc_set_radix_variant": ([_INT], _INT),
     "sc_scan_variant_info": ([_INT, ctypes.POINTER(_INT), ctypes.POINTER(_INT), ctypes.POINTER(_INT)], _INT),
     "sc_debug_set_lookback": ([_I64, _I64, _U32, _U64], _INT),
     "sc_debug_lookback_stats": ([_P, ctypes.POINTER(_U64)], _INT),
@@ -169,6 +170,10 @@ def sc_set_scan_variant(variant: int) -> int:
 
 def sc_set_compact_variant(variant: int) -> int:
     return load().sc_set_compact_variant(variant)
+
+
+def sc_set_radix_variant(variant: int) -> int:
+    return load().sc_set_radix_variant(variant)
 
 
 def sc_scan_variant_info(variant: int):

@@ -52,6 +52,7 @@ int tma_cfg_of(int v) {
 
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_variant{0};
+std::atomic<int> g_radix_variant{0};    // placement ranking of the radix pass (scg::launch_radix_place)
 std::atomic<int> g_compact_variant{0};  // 0, 1: persistent kernel shapes; 2: one tile per CTA
 std::atomic<long long> g_stall_tile{-1};
 std::atomic<long long> g_delay_tile{-1};
@@ -534,7 +535,8 @@ static sc_status radix_one_pass(const uint32_t* in, uint32_t* out, int64_t n, in
     // the scan needs fewer workspace bytes than acquired above: no reallocation
     sc_status st = run_scan(scg::OID_SUM_U32, counts, counts, m, 0, true, nullptr, nullptr, s);
     if (st != SC_OK) return st;
-    e = scg::launch_radix_place(in, out, n, shift, mask, counts, ntiles, reinterpret_cast<unsigned int*>(base + 8), s);
+    e = scg::launch_radix_place(in, out, n, shift, mask, counts, ntiles, reinterpret_cast<unsigned int*>(base + 8),
+                                g_radix_variant.load(), s);
     g_launches.fetch_add(1);
     return e == cudaSuccess ? SC_OK : SC_ERR_CUDA;
 }
@@ -835,6 +837,12 @@ sc_status sc_set_scan_variant(int variant) {
 sc_status sc_set_compact_variant(int variant) {
     if (variant < 0 || variant > 2) return SC_ERR_INVALID;
     g_compact_variant.store(variant);
+    return SC_OK;
+}
+
+sc_status sc_set_radix_variant(int variant) {
+    if (variant < 0 || variant >= scg::radix_num_variants()) return SC_ERR_INVALID;
+    g_radix_variant.store(variant);
     return SC_OK;
 }
 

@@ -120,8 +120,12 @@ cudaError_t launch_histogram(const int32_t* bins, long long n, int nbins, unsign
 int radix_tile_keys();
 cudaError_t launch_radix_count(const uint32_t* keys, long long n, int shift, uint32_t mask, uint32_t* counts,
                                long long ntiles, cudaStream_t s);
+// variant: 0 the default ranking, 1..radix_num_variants()-1 the ranking with
+// variant - 1 digit bits matched by __match_any_sync (the rest by ballots).
+int radix_num_variants();
 cudaError_t launch_radix_place(const uint32_t* in, uint32_t* out, long long n, int shift, uint32_t mask,
-                               const uint32_t* offsets, long long ntiles, unsigned int* error, cudaStream_t s);
+                               const uint32_t* offsets, long long ntiles, unsigned int* error, int variant,
+                               cudaStream_t s);
 
 // Hierarchical (scan-then-propagate) comparison variant.
 constexpr int kHierNT = 256;

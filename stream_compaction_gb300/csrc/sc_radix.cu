@@ -16,8 +16,9 @@
 //                       histograms);
 //   the library's scan  exclusive uint32 sum over the counts, in place;
 //   radix_place_kernel  each tile ranks its keys (in element order: the lanes
-//                       of a warp step with the same digit, found by one ballot
-//                       per digit bit, plus per-warp running counts per digit),
+//                       of a warp step with the same digit, found by a match on
+//                       the top digit bits and one ballot per lower bit, plus
+//                       per-warp running counts per digit),
 //                       reorders them by digit in shared memory and writes
 //                       each digit's run at the scanned offset.
 //
@@ -95,14 +96,17 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t x, uint32_t* s
     return before + incl - x;
 }
 
-// Lanes of the warp whose 8-bit digit equals this lane's: one ballot per bit.
-// (__match_any_sync gives the same mask, but its cost grows with the number of
-// distinct values; with random digits it took about 60 cycles of the SM's
-// address-divergence unit per call and bounded the whole kernel.)
+// Lanes of the warp whose 8-bit digit equals this lane's: __match_any_sync on
+// the top kMatchBits bits, one ballot for each lower bit.  The match runs on the
+// SM's address-divergence unit and its cost grows with the number of distinct
+// values (about 60 cycles a call for 8 random bits, which bounded the whole
+// kernel); the ballots cost integer-pipe instructions.  Splitting the bits puts
+// part of the work on each.
+template <int kMatchBits>
 __device__ __forceinline__ uint32_t same_digit_lanes(uint32_t d) {
-    uint32_t m = 0xffffffffu;
+    uint32_t m = kMatchBits > 0 ? __match_any_sync(0xffffffffu, d >> (8 - kMatchBits)) : 0xffffffffu;
 #pragma unroll
-    for (int b = 0; b < 8; ++b) {
+    for (int b = 0; b < 8 - kMatchBits; ++b) {
         const uint32_t bit = (d >> b) & 1u;
         const uint32_t on = __ballot_sync(0xffffffffu, bit);
         m &= on ^ (bit - 1u);                 // lanes whose bit b equals mine
@@ -113,7 +117,7 @@ __device__ __forceinline__ uint32_t same_digit_lanes(uint32_t d) {
 // Load the warp's 512 keys of the tile (slot j of lane l is element
 // wbase + 32 j + l) and rank each among the warp's earlier keys of its digit:
 // rank = this warp's running count of the digit + same-digit lanes below.
-template <bool kFull>
+template <bool kFull, int kMatchBits>
 __device__ __forceinline__ void load_and_rank(const uint32_t* __restrict__ src, int wbase, int nvalid, int shift,
                                               uint32_t mask, uint32_t* cnt /* this warp's 256 counts */,
                                               uint32_t (&key)[kKPT], uint32_t (&rank)[kKPT]) {
@@ -128,7 +132,7 @@ __device__ __forceinline__ void load_and_rank(const uint32_t* __restrict__ src, 
     for (int j = 0; j < kKPT; ++j) {
         const bool valid = kFull || wbase + j * 32 + lane < nvalid;
         const uint32_t d = (key[j] >> shift) & mask;
-        uint32_t m = same_digit_lanes(d);
+        uint32_t m = same_digit_lanes<kMatchBits>(d);
         if (!kFull) m &= __ballot_sync(0xffffffffu, valid);
         const uint32_t c = cnt[d];
         rank[j] = c + __popc(m & below);
@@ -142,6 +146,7 @@ __device__ __forceinline__ void load_and_rank(const uint32_t* __restrict__ src, 
 
 // Place the keys of tile blockIdx.x: offsets[d * ntiles + tile] is where its
 // first key with digit d goes (the scanned counts).
+template <int kMatchBits>
 __global__ void __launch_bounds__(kNT, 4) radix_place_kernel(const uint32_t* __restrict__ in, uint32_t* __restrict__ out,
                                                              long long n, int shift, uint32_t mask,
                                                              const uint32_t* __restrict__ offsets, long long ntiles,
@@ -164,8 +169,8 @@ __global__ void __launch_bounds__(kNT, 4) radix_place_kernel(const uint32_t* __r
     uint32_t key[kKPT], rank[kKPT];
     const int wbase = warp * 32 * kKPT;
     const uint32_t* src = in + t0 + wbase + (tid & 31);
-    if (nvalid == kTileKeys) load_and_rank<true>(src, wbase, nvalid, shift, mask, s_cnt[warp], key, rank);
-    else load_and_rank<false>(src, wbase, nvalid, shift, mask, s_cnt[warp], key, rank);
+    if (nvalid == kTileKeys) load_and_rank<true, kMatchBits>(src, wbase, nvalid, shift, mask, s_cnt[warp], key, rank);
+    else load_and_rank<false, kMatchBits>(src, wbase, nvalid, shift, mask, s_cnt[warp], key, rank);
     __syncthreads();
 
     // per digit d = tid: the tile's count, its first slot in the reordered tile,
@@ -199,7 +204,7 @@ __global__ void __launch_bounds__(kNT, 4) radix_place_kernel(const uint32_t* __r
     for (int i = tid; i < nvalid; i += kNT) {
         const uint32_t k = s_keys[i];
         const uint32_t pos = s_gdelta[(k >> shift) & mask] + (uint32_t)i;
-        if (pos < (unsigned long long)n) out[pos] = k;
+        if (pos < (uint32_t)n) out[pos] = k;  // n < 2^32
         else raise_error(error, DEV_INTERNAL);  // counts and placement disagree: never expected
     }
 }
@@ -212,10 +217,24 @@ cudaError_t launch_radix_count(const uint32_t* keys, long long n, int shift, uin
     return cudaGetLastError();
 }
 
+int radix_num_variants() { return 6; }
+
 cudaError_t launch_radix_place(const uint32_t* in, uint32_t* out, long long n, int shift, uint32_t mask,
-                               const uint32_t* offsets, long long ntiles, unsigned int* error, cudaStream_t s) {
-    radix_place_kernel<<<(unsigned)ntiles, kNT, 0, s>>>(in, out, n, shift, mask, offsets, ntiles, error);
-    return cudaGetLastError();
+                               const uint32_t* offsets, long long ntiles, unsigned int* error, int variant,
+                               cudaStream_t s) {
+    auto go = [&](auto kernel) {
+        kernel<<<(unsigned)ntiles, kNT, 0, s>>>(in, out, n, shift, mask, offsets, ntiles, error);
+        return cudaGetLastError();
+    };
+    switch (variant) {  // 1 + the number of digit bits matched by __match_any_sync; 0 the default
+        case 1: return go(radix_place_kernel<0>);
+        case 2: return go(radix_place_kernel<1>);
+        case 3: return go(radix_place_kernel<2>);
+        case 0:
+        case 4: return go(radix_place_kernel<3>);
+        case 5: return go(radix_place_kernel<4>);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace scg

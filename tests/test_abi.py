@@ -93,6 +93,8 @@ def test_host_side_argument_checks(lib):
     assert sc.sc_bin_offsets(0x1002, 10, 5, 0x8000, 0) == sc.SC_ERR_INVALID          # misaligned bins
     # tuning and test hooks
     assert sc.sc_set_scan_variant(99) == sc.SC_ERR_INVALID
+    assert sc.sc_set_radix_variant(-1) == sc.SC_ERR_INVALID
+    assert sc.sc_set_radix_variant(6) == sc.SC_ERR_INVALID
     st, t, i, l = sc.sc_scan_variant_info(0)
     assert st == sc.SC_OK and l == 2 and t * i * 4 >= 16384  # persistent TMA kernel, >= 16 KiB tiles
     assert sc.sc_debug_set_lookback(-5, -1, 0, 0) == sc.SC_ERR_INVALID

@@ -78,6 +78,21 @@ def test_radix_sort(kind, n):
     _same(got, np.sort(k))
 
 
+@pytest.mark.parametrize("variant", range(6))
+def test_radix_ranking_variants(variant):
+    """Every ranking split (digit bits by match vs by ballots) gives the same stable pass."""
+    import stream_compaction_gb300 as sc
+    assert sc.sc_set_radix_variant(variant) == sc.SC_OK
+    try:
+        for n, kind in ((3 * 4096 + 5, "uniform"), (100003, "few"), ((1 << 20) + 17, "uniform")):
+            k = _keys(n, kind, seed=variant * 11 + n)
+            for shift, bits in ((0, 8), (24, 8), (3, 5), (31, 1)):
+                _same(gpu_pass(k, shift, bits), oracle.radix_pass(k, shift, bits))
+            _same(gpu_sort(k), np.sort(k))
+    finally:
+        sc.sc_set_radix_variant(0)
+
+
 def test_radix_unaligned_and_inplace():
     k = _keys(9 * 4096 + 11, "uniform", 5)
     ref = np.sort(k)
