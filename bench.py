@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--suite", action="store_true")
     ap.add_argument("--profile-case", type=int, default=0, metavar="N",
                     help="no timing: run the headline scan on the first N elements --steps times (for ncu)")
-    ap.add_argument("--profile-op", default="scan", choices=["scan", "compact", "rows", "hier", "radix", "sort"],
+    ap.add_argument("--profile-op", default="scan", choices=["scan", "scan_f32", "compact", "rows", "hier", "radix", "sort"],
                     help="which kernel --profile-case runs")
     ap.add_argument("--compact-variant", type=int, default=0,
                     help="compaction kernel for --profile-op compact (sc_set_compact_variant)")
@@ -520,6 +520,10 @@ def profile_case(args):
             run = lambda: sc.sc_radix_pass_u32(k.data_ptr(), ko.data_ptr(), n, 8, 8, sp)
         else:
             run = lambda: sc.sc_radix_sort_u32(k.data_ptr(), ko.data_ptr(), kt.data_ptr(), n, sp)
+    elif args.profile_op == "scan_f32":
+        x = synth.make_torch(synth.WORKLOADS["float32_exsum_n2^26"], n=n, device="cuda")
+        y = torch.empty_like(x)
+        run = lambda: sc.sc_scan_exclusive(sc.SC_F32, sc.SC_SUM, x.data_ptr(), y.data_ptr(), n, sp)
     else:
         x = synth.make_torch(synth.WORKLOADS[WORKLOAD], n=n, device="cuda")
         y = torch.empty_like(x)
