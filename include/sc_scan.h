@@ -280,7 +280,10 @@ uint64_t sc_launch_count(void);
  * than 2^21 elements), else the one-tile-per-CTA kernel (for n <= 2^21 its
  * shape of 16384-element tiles with 128-tile look-back windows, variant 10);
  * v >= 1: one of the precompiled shapes (see sc_scan_variant_info), kept for
- * on-GPU comparison.  Returns SC_ERR_INVALID for an unknown variant. */
+ * on-GPU comparison; for int32/uint32 sums segmented by head flags (default:
+ * the shape of variant 9) and batched rows (default: the shape of variant 1)
+ * variants 1, 6, 9, 10 and 11 select their shape, any other the default.
+ * Returns SC_ERR_INVALID for an unknown variant. */
 sc_status sc_set_scan_variant(int variant);
 /* Select the fused-compaction kernel: 0 (default) the persistent TMA kernel
  * with 8 compute warps, 1 the same with 16 compute warps, 2 the

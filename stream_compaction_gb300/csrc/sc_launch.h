@@ -58,6 +58,9 @@ constexpr int oid_elem_bytes(int oid) {
 // Tile size (elements) of operator `op_id` in the given variant; 0 if that
 // variant does not exist.
 int scan_tile_elems(int op_id, int variant);
+// Whether the uint32-sum shape `variant` has a segmented form (the others
+// fall back to shape 0 for segmented scans and batched rows).
+bool segmented_shape(int variant);
 ScanShape scan_shape(int op_id, int variant);
 
 // Scans of the operators from kFirstExtraOid on: the one-tile-per-CTA kernel

@@ -8,8 +8,14 @@ namespace scg {
 template <>
 cudaError_t launch_scan<OpSumU32>(const ScanParams& p, bool exclusive, bool segmented, int variant, cudaStream_t s) {
     if (segmented) {
-        if (variant != 0) return cudaErrorInvalidValue;
-        return launch_shape<OpSumU32, SHAPE(0)>(p, exclusive, true, s);
+        switch (variant) {
+        case 0: return launch_shape<OpSumU32, SHAPE(0)>(p, exclusive, true, s);
+        case 5: return launch_shape<OpSumU32, SHAPE(5)>(p, exclusive, true, s);
+        case 8: return launch_shape<OpSumU32, SHAPE(8)>(p, exclusive, true, s);
+        case 9: return launch_shape<OpSumU32, SHAPE(9)>(p, exclusive, true, s);
+        case 10: return launch_shape<OpSumU32, SHAPE(10)>(p, exclusive, true, s);
+        default: return cudaErrorInvalidValue;
+        }
     }
     switch (variant) {
     case 0: return launch_shape<OpSumU32, SHAPE(0)>(p, exclusive, false, s);
@@ -29,6 +35,10 @@ cudaError_t launch_scan<OpSumU32>(const ScanParams& p, bool exclusive, bool segm
     case 14: return launch_shape_plain<OpSumU32, SHAPE(14)>(p, exclusive, s);
     default: return cudaErrorInvalidValue;
     }
+}
+
+bool segmented_shape(int variant) {
+    return variant == 0 || variant == 5 || variant == 8 || variant == 9 || variant == 10;
 }
 
 #undef SHAPE

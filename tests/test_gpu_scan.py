@@ -107,6 +107,15 @@ def test_uint32_variants(variant):
             for ex in (False, True):
                 assert np.array_equal(gpu_scan(x, "sum", ex), oracle.scan(x, "sum", ex)), (variant, n, ex)
                 assert np.array_equal(gpu_scan(x, "sum", ex, offset=1), oracle.scan(x, "sum", ex))
+        # segmented scans take the variant's shape where it has a segmented form
+        from test_gpu_segmented import _heads, gpu_segmented
+        n = 77 * 4096 + 1234
+        x = _input("u32", n, seed=variant + 5)
+        for density in (1e-4, 3e-3):
+            h = _heads(n, density, seed=variant)
+            for ex in (False, True):
+                got = gpu_segmented(x, h, "sum", ex)
+                assert np.array_equal(got, oracle.scan_segmented(x, h, "sum", ex)), (variant, density, ex)
     finally:
         sc.sc_set_scan_variant(0)
 
