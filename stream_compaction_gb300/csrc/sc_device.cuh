@@ -7,6 +7,7 @@
 // Prefix Sum - Scan Algorithms" (PMPP notes), section 9.1.
 #pragma once
 #include <cstdint>
+#include <type_traits>
 #include <cuda_runtime.h>
 
 #include "sc_params.h"
@@ -97,6 +98,14 @@ template <> struct Extremes<double> {
     __device__ __forceinline__ static double highest() { return __longlong_as_double(0x7ff0000000000000ll); }
 };
 
+// Operators whose combine costs several instructions (or slow float64 units)
+// declare kHeavyCombine = true; kernels may then trade shared memory for
+// fewer combines per element.
+template <class Op, class = void>
+struct HeavyCombine { static constexpr bool value = false; };
+template <class Op>
+struct HeavyCombine<Op, std::void_t<decltype(Op::kHeavyCombine)>> { static constexpr bool value = Op::kHeavyCombine; };
+
 // An operator whose carry has the element's type.
 template <class V, class Self>
 struct SameCarry {
@@ -149,21 +158,25 @@ struct OpMinOf : SameCarry<V, OpMinOf<V>> {
 // +0.0 stay as they came).
 template <class V>
 struct OpMaxNaN : SameCarry<V, OpMaxNaN<V>> {
+    static constexpr bool kHeavyCombine = true;
     __device__ __forceinline__ static V identity() { return Extremes<V>::lowest(); }
     __device__ __forceinline__ static V op(V a, V b) { return (a != a) ? a : (b != b) ? b : (b > a ? b : a); }
 };
 template <class V>
 struct OpMinNaN : SameCarry<V, OpMinNaN<V>> {
+    static constexpr bool kHeavyCombine = true;
     __device__ __forceinline__ static V identity() { return Extremes<V>::highest(); }
     __device__ __forceinline__ static V op(V a, V b) { return (a != a) ? a : (b != b) ? b : (b < a ? b : a); }
 };
 struct OpSumF64 : SameCarry<double, OpSumF64> {
+    static constexpr bool kHeavyCombine = true;  // float64 adds are slow on this part
     __device__ __forceinline__ static double identity() { return 0.0; }
     __device__ __forceinline__ static double op(double a, double b) { return __dadd_rn(a, b); }
 };
 // (maximum, count) pairs stored as uint2 {x = int32 value bits, y = count}:
 // the pair with the larger value; equal values add their counts (mod 2^32).
 struct OpMaxCount : SameCarry<uint2, OpMaxCount> {
+    static constexpr bool kHeavyCombine = true;
     __device__ __forceinline__ static uint2 identity() { return make_uint2(0x80000000u, 0u); }
     __device__ __forceinline__ static uint2 op(uint2 a, uint2 b) {
         const int va = (int)a.x, vb = (int)b.x;

@@ -18,8 +18,10 @@
 //                    the stage freed at once;
 //                    pass 2 of tile j = k - kLag, re-loaded from L2 into ring
 //                    B: serial register scan, warp shuffle scan, combine with
-//                    the earlier warps' totals and the tile's prefix, results
-//                    written back to the stage; both passes in one
+//                    the earlier warps' totals and the tile's prefix (for
+//                    costly operators: the carry first, from thread totals
+//                    kept from pass 1, then one serial scan seeded with it),
+//                    results written back to the stage; both passes in one
 //                    instruction stream;
 //   bookkeeping      per tile: its total and its offset in the chunk; per
 //                    chunk: the aggregate, published for later look-backs;
@@ -127,6 +129,20 @@ using Cfg3 = TmaCfg<16384, 6, 6, 8, 12, 4>;
 using Cfg4 = TmaCfg<32768, 3, 3, 8, 8, 2>;
 constexpr int kNumCfgs = 5;
 
+// For operators with costly combines, pass 1 keeps each compute thread's
+// total of a tile in shared memory for pass 2 (kLag + 2 tiles deep) where the
+// shape leaves room for it; pass 2 then needs one combine per element instead
+// of two.  Measured on GB300: float64 sum 531 -> 413 us and float32 max
+// 144 -> 122 us (2^26); for cheap integer operators it cost 1-1.5 %, so they
+// keep the two-combine form.
+template <class Op, class Cfg>
+struct ThreadTotals {
+    static constexpr int kSlots = Cfg::kLag + 2;
+    static constexpr int kBytes = kSlots * Cfg::kCompute * (int)sizeof(typename Op::T);
+    static constexpr bool kKeep = HeavyCombine<Op>::value && Cfg::kSmemBytes + kBytes <= 232448;
+    static constexpr int kSmemBytes = Cfg::kSmemBytes + (kKeep ? kBytes : 0);
+};
+
 constexpr int kLbPer = 8;               // at most 8 status words per lane: 256-chunk windows
 constexpr unsigned kSentinel = 0xffffffffu;  // end of work
 constexpr unsigned kVoid = 0xfffffffeu;      // past the last tile, inside the last chunk
@@ -156,10 +172,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     constexpr int IPT = kBytesPerThread / sizeof(T);
     constexpr int TILE = kCompute * IPT;
     constexpr int NV = kBytesPerThread / 16;  // 16-byte chunks per compute thread
+    using TT = ThreadTotals<Op, Cfg>;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + (kSA + kSB) * kTileBytes);
+    // each compute thread's pass-1 total, kept for its pass 2 (TT::kSlots tiles)
+    T* ttot = reinterpret_cast<T*>(smem + (kSA + kSB) * kTileBytes + Cfg::kCtrlBytes);
     const uint32_t stageA = smem_u32(smem);
     const uint32_t stageB = stageA + kSA * kTileBytes;
     auto B = [](const unsigned long long& b) { return smem_u32(&b); };
@@ -429,6 +448,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             acc = v[0];
 #pragma unroll
             for (int w = 1; w < IPT; ++w) acc = Op::op(acc, v[w]);
+            if constexpr (TT::kKeep) ttot[(k % TT::kSlots) * kCompute + ctid] = acc;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {  // ordered reduction: lane 0 ends with lanes 0..31
                 const T y = shfl_down_v(acc, d);
@@ -463,23 +483,48 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             const C cp = Op::c_op(unpack_bits<C>(ctl->chunk_prefix[q % kChunkSlots]), unpack_bits<C>(ctl->offset[j % kRing]));
             T base = Op::lower(cp);
             if (warp > 0) base = Op::op(base, wpre);
+            if constexpr (TT::kKeep) {
+                // the thread's total from pass 1 gives its carry first; then one
+                // serial pass seeded with the carry: one combine per element
+                T x = ttot[(j % TT::kSlots) * kCompute + ctid];
 #pragma unroll
-            for (int w = 1; w < IPT; ++w) v[w] = Op::op(v[w - 1], v[w]);
-            T x = v[IPT - 1];
+                for (int d = 1; d < 32; d <<= 1) {
+                    const T y = shfl_up_v(x, d);
+                    if (lane >= d) x = Op::op(y, x);
+                }
+                T run = shfl_up_v(x, 1);
+                run = lane == 0 ? base : Op::op(base, run);
+                if constexpr (kExcl) {
 #pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const T y = shfl_up_v(x, d);
-                if (lane >= d) x = Op::op(y, x);
-            }
-            T carry = shfl_up_v(x, 1);
-            carry = lane == 0 ? base : Op::op(base, carry);
-            if constexpr (kExcl) {
+                    for (int w = 0; w < IPT; ++w) {
+                        const T xw = v[w];
+                        v[w] = run;
+                        run = Op::op(run, xw);
+                    }
+                } else {
+                    v[0] = Op::op(run, v[0]);
 #pragma unroll
-                for (int w = IPT - 1; w >= 1; --w) v[w] = Op::op(carry, v[w - 1]);
-                v[0] = carry;
+                    for (int w = 1; w < IPT; ++w) v[w] = Op::op(v[w - 1], v[w]);
+                }
             } else {
 #pragma unroll
-                for (int w = 0; w < IPT; ++w) v[w] = Op::op(carry, v[w]);
+                for (int w = 1; w < IPT; ++w) v[w] = Op::op(v[w - 1], v[w]);
+                T x = v[IPT - 1];
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const T y = shfl_up_v(x, d);
+                    if (lane >= d) x = Op::op(y, x);
+                }
+                T carry = shfl_up_v(x, 1);
+                carry = lane == 0 ? base : Op::op(base, carry);
+                if constexpr (kExcl) {
+#pragma unroll
+                    for (int w = IPT - 1; w >= 1; --w) v[w] = Op::op(carry, v[w - 1]);
+                    v[0] = carry;
+                } else {
+#pragma unroll
+                    for (int w = 0; w < IPT; ++w) v[w] = Op::op(carry, v[w]);
+                }
             }
             if (full) {
                 const uint32_t sb = stageB + s * kTileBytes;
@@ -547,9 +592,10 @@ cudaError_t launch_one(const ScanParams& p, unsigned grid, cudaStream_t s) {
     const unsigned long long rows = (unsigned long long)nfull * Cfg::kRows;
     if (!make_map(&a, p.in, rows, Cfg::kRows) || !make_map(&b, p.out, rows, Cfg::kRows)) return cudaErrorInvalidValue;
     static std::atomic<unsigned long long> done_mask{0};
-    const cudaError_t e = allow_smem(scan_tma_kernel<Op, kExcl, kStats, Cfg>, Cfg::kSmemBytes, done_mask);
+    constexpr int smem = ThreadTotals<Op, Cfg>::kSmemBytes;
+    const cudaError_t e = allow_smem(scan_tma_kernel<Op, kExcl, kStats, Cfg>, smem, done_mask);
     if (e != cudaSuccess) return e;
-    scan_tma_kernel<Op, kExcl, kStats, Cfg><<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(a, b, p, nfull);
+    scan_tma_kernel<Op, kExcl, kStats, Cfg><<<grid, Cfg::kThreads, smem, s>>>(a, b, p, nfull);
     return cudaGetLastError();
 }
 
