@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--suite", action="store_true")
     ap.add_argument("--profile-case", type=int, default=0, metavar="N",
                     help="no timing: run the headline scan on the first N elements --steps times (for ncu)")
-    ap.add_argument("--profile-op", default="scan", choices=["scan", "scan_f32", "compact", "rows", "hier", "radix", "sort"],
+    ap.add_argument("--profile-op", default="scan", choices=["scan", "scan_f32", "compact", "rows", "hier", "radix", "sort", "csr"],
                     help="which kernel --profile-case runs")
     ap.add_argument("--compact-variant", type=int, default=0,
                     help="compaction kernel for --profile-op compact (sc_set_compact_variant)")
@@ -520,6 +520,13 @@ def profile_case(args):
             run = lambda: sc.sc_radix_pass_u32(k.data_ptr(), ko.data_ptr(), n, 8, 8, sp)
         else:
             run = lambda: sc.sc_radix_sort_u32(k.data_ptr(), ko.data_ptr(), kt.data_ptr(), n, sp)
+    elif args.profile_op == "csr":
+        spec = synth.WORKLOADS["csr_rows_2^22"]
+        bins = synth.make_torch(spec, device="cuda")
+        n = bins.numel()
+        nbins = spec["nrows"]
+        offs = torch.empty(nbins + 1, dtype=torch.int64, device="cuda")
+        run = lambda: sc.sc_bin_offsets(bins.data_ptr(), n, nbins, offs.data_ptr(), sp)
     elif args.profile_op == "scan_f32":
         x = synth.make_torch(synth.WORKLOADS["float32_exsum_n2^26"], n=n, device="cuda")
         y = torch.empty_like(x)

@@ -6,9 +6,10 @@
 // int64 single-pass scan (sc_api.cu).
 //
 // counts[b] += number of i with bins[i] == b, 0 <= b < nbins (entries outside
-// are skipped).  Equal bins inside a warp are counted with one atomic
-// (__match_any_sync), so sorted input (CSR rows) costs about one atomic per row
-// per warp step.  Up to kWarpCopyBins bins each warp counts into its own
+// are skipped).  Beyond kWarpCopyBins bins, a run of equal neighbouring bins
+// in a warp step (128 consecutive entries) is counted with one atomic, so
+// sorted input (CSR rows) costs about one atomic per row per warp step.  Up to
+// kWarpCopyBins bins each warp counts into its own
 // shared-memory histogram (plain shared atomics), up to kSmemBins bins each CTA
 // into one shared histogram; the CTA adds its counts to the global ones once
 // at the end.  Beyond that the atomics go to the global counts directly.
@@ -22,9 +23,9 @@ namespace {
 
 constexpr int kHistThreads = 512;
 
-// kMode: 0 global atomics (warp-aggregated), 1 one shared histogram per CTA
-// (warp-aggregated), 2 one shared histogram per warp (plain shared atomics:
-// contention stays inside the warp; for small bin counts).
+// kMode: 0 global atomics (one per run of equal neighbours), 1 one shared
+// histogram per CTA (likewise), 2 one shared histogram per warp (plain shared
+// atomics: contention stays inside the warp; for small bin counts).
 template <int kMode>
 __global__ void __launch_bounds__(kHistThreads) histogram_kernel(const int32_t* __restrict__ bins, long long n,
                                                                  int nbins, unsigned long long* __restrict__ counts,
@@ -38,15 +39,36 @@ __global__ void __launch_bounds__(kHistThreads) histogram_kernel(const int32_t* 
         __syncthreads();
     }
     unsigned int* const mine = sh + (kMode == 2 ? (threadIdx.x >> 5) * nbins : 0);
-    auto add = [&](int b) {
-        const bool ok = b >= 0 && b < nbins;
-        if constexpr (kMode == 2) {
-            if (ok) atomicAdd(&mine[b], 1u);
-        } else {
-            const unsigned mask = __match_any_sync(0xffffffffu, ok ? b : -1);
-            if (ok && lane == __ffs(mask) - 1) {
-                if constexpr (kMode == 1) atomicAdd(&sh[b], (unsigned)__popc(mask));
-                else atomicAdd(&counts[b], (unsigned long long)__popc(mask));
+    auto add = [&](int b) {  // one shared histogram per warp: plain shared atomics
+        if (b >= 0 && b < nbins) atomicAdd(&mine[b], 1u);
+    };
+    // The warp step's 128 bins in memory order (lane l holds 4l .. 4l+3): one
+    // atomic per run of equal neighbours, its length from the next run's start
+    // (a shuffle finds the starts, a ballot and one shuffle the next start in
+    // a later lane).  No __match_any_sync: its cost grows with the number of
+    // distinct values and it bounded this kernel (address-divergence unit 90 %
+    // busy on CSR rows).
+    auto add_runs = [&](const int (&b)[4]) {
+        const int prev = __shfl_up_sync(0xffffffffu, b[3], 1);
+        bool h[4];
+        h[0] = lane == 0 || b[0] != prev;
+#pragma unroll
+        for (int k = 1; k < 4; ++k) h[k] = b[k] != b[k - 1];
+        const int fh = h[0] ? 0 : h[1] ? 1 : h[2] ? 2 : h[3] ? 3 : 4;  // first run start in this lane
+        const unsigned any = __ballot_sync(0xffffffffu, fh < 4);
+        const unsigned later = lane == 31 ? 0u : any & (0xffffffffu << (lane + 1));
+        const int nl = later ? __ffs(later) - 1 : 32;
+        const int nfh = __shfl_sync(0xffffffffu, fh, nl & 31);
+        int end = nl < 32 ? 4 * nl + nfh : 128;  // start of the run after this lane's last
+#pragma unroll
+        for (int k = 3; k >= 0; --k) {
+            if (h[k]) {
+                const int pos = 4 * lane + k;
+                if (b[k] >= 0 && b[k] < nbins) {
+                    if constexpr (kMode == 1) atomicAdd(&sh[b[k]], (unsigned)(end - pos));
+                    else atomicAdd(&counts[b[k]], (unsigned long long)(end - pos));
+                }
+                end = pos;
             }
         }
     };
@@ -54,7 +76,7 @@ __global__ void __launch_bounds__(kHistThreads) histogram_kernel(const int32_t* 
     // steps of 32 groups per loop iteration with all loads issued first; every
     // lane of a warp runs the same number of iterations, so each match sees all
     // 32 lanes
-    constexpr int kUnroll = kMode == 0 ? 1 : 4;  // measured: unrolling slows the global-atomic form
+    constexpr int kUnroll = 4;
     const long long ngroups = (n + 3) / 4;
     const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
@@ -77,9 +99,14 @@ __global__ void __launch_bounds__(kHistThreads) histogram_kernel(const int32_t* 
             }
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
+        for (int u = 0; u < kUnroll; ++u) {
+            if constexpr (kMode == 2) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) add(v[u][k]);
+                for (int k = 0; k < 4; ++k) add(v[u][k]);
+            } else {
+                add_runs(v[u]);
+            }
+        }
     }
     if constexpr (kMode != 0) {
         __syncthreads();
@@ -122,7 +149,7 @@ cudaError_t launch_histogram(const int32_t* bins, long long n, int nbins, unsign
         return launch_mode<2>(bins, n, nbins, counts, grid_of(2, 4), nbins * 4 * (kHistThreads / 32), vec, s);
     if (nbins <= kSmemBins)
         return launch_mode<1>(bins, n, nbins, counts, grid_of(nbins <= 8192 ? 2 : 1, 4), nbins * 4, vec, s);
-    return launch_mode<0>(bins, n, nbins, counts, grid_of(4, 1), 0, vec, s);
+    return launch_mode<0>(bins, n, nbins, counts, grid_of(4, 4), 0, vec, s);
 }
 
 }  // namespace scg
