@@ -122,6 +122,7 @@ LookbackCtl make_ctl(Workspace& ws, unsigned num_tiles) {
     lb.counter_base = ws.counter_base;
     lb.epoch = ++ws.epoch;
     lb.num_tiles = num_tiles;
+    lb.static_ids = 0;
     lb.stall_tile = g_stall_tile.load();
     lb.delay_tile = g_delay_tile.load();
     lb.delay_ns = g_delay_ns.load();
@@ -298,7 +299,13 @@ sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_le
         const cudaError_t e = dispatch_scan_tma(oid, p, excl, grid, s, tma_stats, cfg);
         return finish_launch(*ws, ntiles + grid * (unsigned)scg::tma_ids_per_cta(), e);
     }
-    return finish_launch(*ws, ntiles, dispatch_scan(oid, p, excl, segmented, legacy_variant, s));
+    // a grid no larger than the SM count is resident at once, so tiles may take
+    // their ids from blockIdx.x (no counter round trip): every tile a look-back
+    // waits on is already running
+    const int sms = num_sms();
+    p.lb.static_ids = sms > 0 && ntiles <= (unsigned)sms;
+    return finish_launch(*ws, p.lb.static_ids ? 0u : ntiles,
+                         dispatch_scan(oid, p, excl, segmented, legacy_variant, s));
 }
 
 // ------------------------------------------------------ compaction predicate

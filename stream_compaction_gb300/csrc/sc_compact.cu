@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(NT) compact_kernel(const CompactParams p) {
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
-        s_tile = (unsigned)(atomicAdd(p.lb.counter, 1ull) - p.lb.counter_base);
+        s_tile = p.lb.static_ids ? blockIdx.x : (unsigned)(atomicAdd(p.lb.counter, 1ull) - p.lb.counter_base);
         s_abort = 0;
     }
     __syncthreads();

@@ -123,6 +123,7 @@ extern "C" sc_status sc_scan_noalloc(sc_dtype dtype, sc_op op, int exclusive, co
     p.lb.counter_base = 0;
     p.lb.epoch = ++slot->epoch;
     p.lb.num_tiles = (unsigned)((n + tile - 1) / tile);
+    p.lb.static_ids = 0;
     p.lb.stall_tile = -1;
     p.lb.delay_tile = -1;
     p.lb.delay_ns = 0;

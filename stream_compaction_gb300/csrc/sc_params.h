@@ -18,6 +18,7 @@ struct LookbackCtl {
     unsigned long long counter_base;
     unsigned int epoch;             // 1 .. 2^30-1; words of other epochs read as "not yet"
     unsigned int num_tiles;
+    int static_ids;                 // 1: tile = blockIdx.x (the whole grid is resident at once), 0: from the counter
     long long stall_tile;           // test hook: tile that never publishes (-1: off)
     long long delay_tile;           // test hook: tile that sleeps before publishing (-1: off)
     unsigned int delay_ns;

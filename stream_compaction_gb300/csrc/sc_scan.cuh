@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(NT, kMinB) scan_kernel(const ScanParams p) {
     unsigned windows = 0, polls = 0;
     if (kStats && tid == 0) t0 = global_ns();
     if (tid == 0) {
-        s_tile = (unsigned)(atomicAdd(p.lb.counter, 1ull) - p.lb.counter_base);
+        s_tile = p.lb.static_ids ? blockIdx.x : (unsigned)(atomicAdd(p.lb.counter, 1ull) - p.lb.counter_base);
         s_abort = 0;
     }
     __syncthreads();
