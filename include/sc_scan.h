@@ -75,6 +75,10 @@
  *   - Calls on one stream must not overlap in time with calls on the same
  *     stream from another host thread; different streams have independent
  *     workspaces.
+ *   - Calls cannot be captured into a CUDA graph: each call's look-back epoch
+ *     and tile-counter base are host state that a replay would repeat.  A
+ *     call whose stream is capturing returns SC_ERR_UNSUPPORTED before any
+ *     launch.
  *   - n == 0 is a successful no-op (compaction writes *d_count = 0).
  *   - Argument errors are detected on the host before any launch and return
  *     SC_ERR_INVALID / SC_ERR_UNSUPPORTED.  A failure inside a kernel (a
@@ -170,8 +174,10 @@ sc_status sc_scan_segmented(sc_dtype dtype, sc_op op, int exclusive, const void 
 /* Histogram of int32 bin indices: d_counts[b] (int64, nbins entries) = the
  * number of i with d_bins[i] == b, 0 <= b < nbins; entries outside [0, nbins)
  * are skipped.  1 <= nbins < 2^31; d_counts must not overlap d_bins.  One
- * memset and one kernel launch (equal bins of a warp share one atomic; up to
- * 32768 bins each CTA counts in shared memory first). */
+ * memset and one kernel launch (up to 1024 bins each warp counts in shared
+ * memory, up to 32768 each CTA; beyond 1024 a run of equal neighbouring bins
+ * shares one atomic).  Keeps no host state between calls, so unlike the other
+ * calls it may be captured into a CUDA graph. */
 sc_status sc_histogram(const int32_t *d_bins, int64_t n, int64_t nbins, int64_t *d_counts, sc_stream_t stream);
 
 /* Bin offsets: d_offsets[b] (int64, nbins + 1 entries) = the number of i with

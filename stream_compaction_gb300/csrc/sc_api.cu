@@ -82,7 +82,17 @@ size_t lookback_bytes(int64_t n) { return kStatusOffset + kSlotBytes * (size_t)c
 
 // Workspace of (current device, stream) with at least `need` bytes, zeroed and
 // ready for the next epoch.  Caller holds g_ws_mu.
+// SC_OK when `s` is not capturing into a CUDA graph: the look-back epoch and
+// counter base are host state that a captured call would replay unchanged.
+sc_status refuse_capture(cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return SC_ERR_CUDA;
+    return cs == cudaStreamCaptureStatusNone ? SC_OK : SC_ERR_UNSUPPORTED;
+}
+
 sc_status acquire_ws(cudaStream_t s, size_t need, Workspace** out) {
+    const sc_status cap = refuse_capture(s);
+    if (cap != SC_OK) return cap;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SC_ERR_CUDA;
     Workspace& ws = g_ws[{dev, s}];
@@ -512,6 +522,10 @@ sc_status sc_bin_offsets(const int32_t* d_bins, int64_t n, int64_t nbins, int64_
     const sc_status st = check_hist_args(d_bins, n, nbins, d_offsets, nbins + 1);
     if (st != SC_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (n > 0 || nbins > 0) {
+        const sc_status cap = refuse_capture(s);  // before the first launch
+        if (cap != SC_OK) return cap;
+    }
     // counts in offsets[0..nbins), 0 in offsets[nbins]; the exclusive scan in
     // place then leaves the total in offsets[nbins]
     const sc_status r = count_bins(d_bins, n, nbins, d_offsets, nbins + 1, s);
@@ -747,6 +761,8 @@ sc_status sc_scan_host(sc_dtype dtype, sc_op op, int exclusive, const void* h_in
     if (!h_in || !h_out) return SC_ERR_INVALID;
     const int eb = elem_bytes(dtype);
     if (bad_overlap(h_in, h_out, (size_t)n * eb, true)) return SC_ERR_INVALID;
+    const sc_status cap = refuse_capture(reinterpret_cast<cudaStream_t>(stream));
+    if (cap != SC_OK) return cap;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SC_ERR_CUDA;
     HostPipe* hp;

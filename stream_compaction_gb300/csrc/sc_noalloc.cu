@@ -88,6 +88,9 @@ extern "C" sc_status sc_scan_noalloc(sc_dtype dtype, sc_op op, int exclusive, co
     if (a != b && a < b + bytes && b < a + bytes) return SC_ERR_INVALID;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;  // the epoch is host state: no capture
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return SC_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone) return SC_ERR_UNSUPPORTED;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SC_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);
