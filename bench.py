@@ -271,7 +271,15 @@ def suite_lines(args, dev, sc, synth):
     y = torch.empty_like(x)
     n = x.numel()
     ms, b = timed(lambda: sc.sc_scan_exclusive(sc.SC_F32, sc.SC_SUM, x.data_ptr(), y.data_ptr(), n, sp), 8 * n)
-    emit("float32_exsum_n2^26", n, ms, b)
+    # accuracy of the last run against a float64 cumulative sum of the same input:
+    # the largest |y - exact| / (1e-5 * sum_{k<=i} |x_k|) (1.0 = at the bound)
+    x64 = x.double()
+    exact = torch.cumsum(x64, 0) - x64
+    bound = 1e-5 * torch.cumsum(x64.abs(), 0)
+    ratio = float(((y.double() - exact).abs() / bound.clamp_min(1e-300)).max())
+    del x64, exact, bound
+    emit("float32_exsum_n2^26", n, ms, b, {"max_err_over_bound": ratio,
+                                           "bound": "1e-5 * sum_{k<=i} |x_k|, against a float64 cumsum"})
     x = synth.make_torch(W["int32_compact_gt0_n2^27"], device=dev)
     y = torch.empty_like(x)
     cnt = torch.empty(1, dtype=torch.int64, device=dev)

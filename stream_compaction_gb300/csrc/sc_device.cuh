@@ -17,8 +17,9 @@ namespace scg {
 // ----------------------------------------------------------------- operators
 // Each operator has an element type T (what the tile is scanned in) and a
 // carry type C (what travels between tiles through the look-back).  Only the
-// float32 sum has C != T: its inter-tile carry is fp64 so that the error of a
-// prefix stays a small multiple of eps * sum|x| however many tiles precede it.
+// float32 sum has C != T: its inter-tile carry is a float-float pair so that
+// the error of a prefix stays a small multiple of eps * sum|x| however many
+// tiles precede it.
 
 struct OpSumU32 {  // int32 and uint32 sums: two's-complement wraparound mod 2^32
     using T = uint32_t;
@@ -31,15 +32,32 @@ struct OpSumU32 {  // int32 and uint32 sums: two's-complement wraparound mod 2^3
     __device__ __forceinline__ static T lower(C c) { return c; }
 };
 
+// Sum of two float-float numbers (x = high part, y = low part, |y| <= ulp(x)/2):
+// Knuth's error-free TwoSum of the high parts, the low parts added to its
+// error, then a fast renormalisation (Dekker).  Relative error about 2^-44 of
+// |a| + |b|; float32 operations only.
+__device__ __forceinline__ float2 ff_add(float2 a, float2 b) {
+    const float s = __fadd_rn(a.x, b.x);
+    const float bv = __fsub_rn(s, a.x);
+    const float e = __fadd_rn(__fsub_rn(a.x, __fsub_rn(s, bv)), __fsub_rn(b.x, bv));  // a.x + b.x == s + e exactly
+    const float lo = __fadd_rn(e, __fadd_rn(a.y, b.y));
+    const float hi = __fadd_rn(s, lo);
+    return make_float2(hi, __fsub_rn(lo, __fsub_rn(hi, s)));
+}
+
+// float32 sums: each tile in float32; the carry between tiles as a float-float
+// pair, so that a prefix chained through many tiles keeps about 44 bits
+// (GB300's float64 units are slow enough that a float64 carry cost 7-8 % of
+// the scan's time).
 struct OpSumF32 {
     using T = float;
-    using C = double;
+    using C = float2;
     __device__ __forceinline__ static T identity() { return 0.0f; }
     __device__ __forceinline__ static T op(T a, T b) { return __fadd_rn(a, b); }
-    __device__ __forceinline__ static C c_identity() { return 0.0; }
-    __device__ __forceinline__ static C c_op(C a, C b) { return __dadd_rn(a, b); }
-    __device__ __forceinline__ static C lift(T a) { return (double)a; }
-    __device__ __forceinline__ static T lower(C c) { return __double2float_rn(c); }
+    __device__ __forceinline__ static C c_identity() { return make_float2(0.0f, 0.0f); }
+    __device__ __forceinline__ static C c_op(C a, C b) { return ff_add(a, b); }
+    __device__ __forceinline__ static C lift(T a) { return make_float2(a, 0.0f); }
+    __device__ __forceinline__ static T lower(C c) { return __fadd_rn(c.x, c.y); }
 };
 
 struct OpMaxI32 {  // identity INT32_MIN (the "-infinity" of the PMPP identity table)
@@ -240,10 +258,16 @@ __device__ __forceinline__ unsigned long long to_bits64(double v) { return (unsi
 __device__ __forceinline__ unsigned long long to_bits64(uint2 v) { return ((unsigned long long)v.y << 32) | v.x; }
 __device__ __forceinline__ unsigned long long to_bits64(unsigned long long v) { return v; }
 __device__ __forceinline__ unsigned long long to_bits64(long long v) { return (unsigned long long)v; }
+__device__ __forceinline__ unsigned long long to_bits64(float2 v) {
+    return ((unsigned long long)__float_as_uint(v.y) << 32) | __float_as_uint(v.x);
+}
 __device__ __forceinline__ void from_bits64(unsigned long long b, double& v) { v = __longlong_as_double((long long)b); }
 __device__ __forceinline__ void from_bits64(unsigned long long b, uint2& v) { v = make_uint2((uint32_t)b, (uint32_t)(b >> 32)); }
 __device__ __forceinline__ void from_bits64(unsigned long long b, unsigned long long& v) { v = b; }
 __device__ __forceinline__ void from_bits64(unsigned long long b, long long& v) { v = (long long)b; }
+__device__ __forceinline__ void from_bits64(unsigned long long b, float2& v) {
+    v = make_float2(__uint_as_float((uint32_t)b), __uint_as_float((uint32_t)(b >> 32)));
+}
 
 // Warp shuffles for 4- and 8-byte value types.
 template <class V>

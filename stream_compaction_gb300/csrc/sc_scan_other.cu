@@ -1,4 +1,4 @@
-// float32 sum (fp64 inter-tile carry), int32 max and affine-map composition scans.
+// float32 sum (float-float inter-tile carry), int32 max and affine-map composition scans.
 #include "sc_scan_launch.cuh"
 
 namespace scg {
