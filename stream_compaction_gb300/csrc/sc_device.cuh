@@ -186,6 +186,23 @@ struct OpMinNaN : SameCarry<V, OpMinNaN<V>> {
     __device__ __forceinline__ static V identity() { return Extremes<V>::highest(); }
     __device__ __forceinline__ static V op(V a, V b) { return (a != a) ? a : (b != b) ? b : (b < a ? b : a); }
 };
+// float32: one max.NaN / min.NaN instruction (NaN in, canonical NaN out; it
+// orders -0.0 below +0.0, so equal values first keep the earlier one)
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float fmin_nan(float a, float b) {
+    float r;
+    asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+template <>
+__device__ __forceinline__ float OpMaxNaN<float>::op(float a, float b) { return a == b ? a : fmax_nan(a, b); }
+template <>
+__device__ __forceinline__ float OpMinNaN<float>::op(float a, float b) { return a == b ? a : fmin_nan(a, b); }
+
 struct OpSumF64 : SameCarry<double, OpSumF64> {
     static constexpr bool kHeavyCombine = true;  // float64 adds are slow on this part
     __device__ __forceinline__ static double identity() { return 0.0; }

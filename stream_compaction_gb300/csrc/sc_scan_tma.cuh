@@ -445,9 +445,23 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     auto finish1 = [&](int k, int s, unsigned tu, T (&v)[IPT]) {
         T acc = Op::identity();
         if (tu != kVoid) {
-            acc = v[0];
+            if constexpr (TT::kKeep && IPT % 4 == 0) {
+                // costly combines: four independent in-order chains, then their
+                // totals in order (the same number of combines, a quarter of
+                // the dependency depth)
+                T part[4];
 #pragma unroll
-            for (int w = 1; w < IPT; ++w) acc = Op::op(acc, v[w]);
+                for (int g = 0; g < 4; ++g) {
+                    part[g] = v[g * (IPT / 4)];
+#pragma unroll
+                    for (int w = 1; w < IPT / 4; ++w) part[g] = Op::op(part[g], v[g * (IPT / 4) + w]);
+                }
+                acc = Op::op(Op::op(part[0], part[1]), Op::op(part[2], part[3]));
+            } else {
+                acc = v[0];
+#pragma unroll
+                for (int w = 1; w < IPT; ++w) acc = Op::op(acc, v[w]);
+            }
             if constexpr (TT::kKeep) ttot[(k % TT::kSlots) * kCompute + ctid] = acc;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {  // ordered reduction: lane 0 ends with lanes 0..31
