@@ -49,7 +49,9 @@
  *                                        makes every later output NaN; of two
  *                                        equal values the earlier is kept, so
  *                                        -0.0 and +0.0 come out as they went in;
- *                                        exact (bit for bit);
+ *                                        exact (bit for bit, except that a NaN
+ *                                        output is a NaN, not necessarily the
+ *                                        input NaN's payload);
  *   (SC_F64, SC_SUM)                    float64 sum, within
  *                                        (16 * ceil(n/2048) + 64) * 2^-53 *
  *                                        sum_{k<=i} |x[k]| of the exact prefix
