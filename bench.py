@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--suite", action="store_true")
     ap.add_argument("--profile-case", type=int, default=0, metavar="N",
                     help="no timing: run the headline scan on the first N elements --steps times (for ncu)")
-    ap.add_argument("--profile-op", default="scan", choices=["scan", "scan_f32", "compact", "rows", "hier", "radix", "sort", "csr"],
+    ap.add_argument("--profile-op", default="scan", choices=["scan", "scan_f32", "compact", "rows", "hier", "radix", "sort", "csr", "segsum"],
                     help="which kernel --profile-case runs")
     ap.add_argument("--compact-variant", type=int, default=0,
                     help="compaction kernel for --profile-op compact (sc_set_compact_variant)")
@@ -528,6 +528,12 @@ def profile_case(args):
             run = lambda: sc.sc_radix_pass_u32(k.data_ptr(), ko.data_ptr(), n, 8, 8, sp)
         else:
             run = lambda: sc.sc_radix_sort_u32(k.data_ptr(), ko.data_ptr(), kt.data_ptr(), n, sp)
+    elif args.profile_op == "segsum":
+        spec = synth.WORKLOADS["int32_segsum_n2^27"]
+        x = synth.make_torch(spec, n=n, device="cuda")
+        h = synth.make_heads_torch(spec, n=n, device="cuda")
+        y = torch.empty_like(x)
+        run = lambda: sc.sc_scan_segmented(sc.SC_I32, sc.SC_SUM, 1, x.data_ptr(), h.data_ptr(), y.data_ptr(), n, sp)
     elif args.profile_op == "csr":
         spec = synth.WORKLOADS["csr_rows_2^22"]
         bins = synth.make_torch(spec, device="cuda")

@@ -303,6 +303,17 @@ sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_le
     p.vec_ok = vec_ok;
     p.carry_in = carry_in;
     p.carry_out = carry_out;
+    // scans segmented by head flags: the persistent kernel when the operator
+    // has that form and the arrays are 16-byte aligned and hold a full tile
+    const int64_t seg_tile = scg::segscan_tma_tile_elems();
+    if (heads && api_variant == 0 && scg::segscan_tma_supported(oid) && vec_ok && aligned(heads, 16) &&
+        n >= seg_tile && !carry_in && !carry_out && n / seg_tile * 256 < (int64_t)INT_MAX && num_sms() > 0) {
+        const unsigned nchunks = (unsigned)ceil_div(n, seg_tile * scg::segscan_tma_chunk_tiles());
+        p.lb = make_ctl(*ws, nchunks);
+        const unsigned grid = (unsigned)std::min<int64_t>(num_sms(), nchunks);
+        const cudaError_t e = scg::launch_segscan_tma(oid, p, excl, grid, s);
+        return finish_launch(*ws, nchunks + grid * (unsigned)scg::tma_ids_per_cta(), e);
+    }
     p.lb = make_ctl(*ws, ntiles);
     if (use_tma) {
         const unsigned grid = (unsigned)std::min<int64_t>(num_sms(), ntiles);

@@ -58,6 +58,12 @@ constexpr int oid_elem_bytes(int oid) {
 // Tile size (elements) of operator `op_id` in the given variant; 0 if that
 // variant does not exist.
 int scan_tile_elems(int op_id, int variant);
+// Persistent scans segmented by head flags (sc_segscan_tma.cu): tile
+// elements, tiles per look-back chunk, the operators compiled, the launch.
+int segscan_tma_tile_elems();
+int segscan_tma_chunk_tiles();
+bool segscan_tma_supported(int op_id);
+cudaError_t launch_segscan_tma(int op_id, const ScanParams& p, bool exclusive, unsigned grid, cudaStream_t s);
 // Whether the uint32-sum shape `variant` has a segmented form (the others
 // fall back to shape 0 for segmented scans and batched rows).
 bool segmented_shape(int variant);

@@ -148,3 +148,35 @@ def test_segmented_workload_full_size():
     x = xt.cpu().numpy()
     h = synth.make_heads_np(spec)
     assert np.array_equal(gpu_segmented(x, h, "sum", True), oracle.scan_segmented(x, h, "sum", True))
+
+
+@pytest.mark.parametrize("op", ["sum", "max"])
+def test_segmented_persistent_tile_and_chunk_boundaries(op):
+    """int32 sums and max segmented by heads run on the persistent kernel
+    (8192-element tiles, 2-tile chunks, flags bulk-copied with each tile):
+    heads on, just before and just after tile and chunk starts, a head only
+    in the ragged last tile, heads everywhere, and sizes around tile
+    multiples; the one-tile-per-CTA kernel (scan variant 1) must agree."""
+    import stream_compaction_gb300 as sc
+    T, CH = 8192, 16384
+    for n in (T, T + 1, 2 * CH - 1, 2 * CH, 7 * CH + T + 3, 64 * CH + 5):
+        x = make_input("i32", op, n, seed=n)
+        cases = [np.zeros(n, np.uint8), np.ones(n, np.uint8)]
+        for stride, shift in ((T, 0), (T, -1), (T, 1), (CH, 0), (CH, -1), (CH, 1)):
+            h = np.zeros(n, np.uint8)
+            idx = np.arange(stride + shift, n, stride)
+            h[idx[(idx >= 0) & (idx < n)]] = 1
+            cases.append(h)
+        h = np.zeros(n, np.uint8)
+        h[n - 1] = 7                                   # any nonzero byte is a head
+        cases.append(h)
+        for h in cases:
+            for ex in (False, True):
+                ref = oracle.scan_segmented(x, h, op, ex)
+                got = gpu_segmented(x, h, op, ex)
+                assert np.array_equal(got, ref), (n, op, ex)
+        assert sc.sc_set_scan_variant(1) == sc.SC_OK
+        try:
+            assert np.array_equal(gpu_segmented(x, cases[-2], op, True), oracle.scan_segmented(x, cases[-2], op, True))
+        finally:
+            sc.sc_set_scan_variant(0)
