@@ -64,6 +64,8 @@ int segscan_tma_tile_elems();
 int segscan_tma_chunk_tiles();
 bool segscan_tma_supported(int op_id);
 cudaError_t launch_segscan_tma(int op_id, const ScanParams& p, bool exclusive, unsigned grid, cudaStream_t s);
+cudaError_t launch_segscan_tma_bits(int op_id, const ScanParams& p, bool exclusive, unsigned grid, cudaStream_t s);
+cudaError_t launch_segscan_tma_order(int op_id, const ScanParams& p, bool exclusive, unsigned grid, cudaStream_t s);
 // Whether the uint32-sum shape `variant` has a segmented form (the others
 // fall back to shape 0 for segmented scans and batched rows).
 bool segmented_shape(int variant);
