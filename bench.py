@@ -63,7 +63,8 @@ def peaks():
 
 
 # The sources the headline kernel (the persistent TMA scan) is compiled from.
-HEADLINE_SOURCES = ("sc_scan_tma.cu", "sc_scan_tma.cuh", "sc_persist.cuh", "sc_tma.cuh", "sc_device.cuh", "sc_params.h")
+HEADLINE_SOURCES = ("sc_scan_tma.cu", "sc_scan_tma.cuh", "sc_scan.cuh", "sc_persist.cuh", "sc_tma.cuh", "sc_device.cuh",
+                    "sc_params.h")
 
 
 def kernel_sources_hash() -> str:
