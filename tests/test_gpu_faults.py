@@ -127,3 +127,49 @@ def test_many_streams_are_independent():
     torch.cuda.synchronize()
     for x, o in zip(xs, outs):
         assert np.array_equal(o.cpu().numpy().view(np.uint32), oracle.scan(x, "sum", True))
+
+
+def _raw_segscan(x, heads):
+    import torch
+    _, xin = to_device(x)
+    _, xout = dev_buffer(xin.numel(), xin.dtype)
+    h = torch.from_numpy(heads).cuda()
+    st = sc.sc_scan_segmented(sc.SC_U32, sc.SC_SUM, 1, xin.data_ptr(), h.data_ptr(), xout.data_ptr(), x.size,
+                              stream())
+    return st, xout
+
+
+@pytest.mark.parametrize("density", [0.0, 1e-3])
+def test_stalled_chunk_in_segmented_scan_times_out(density):
+    """The persistent segmented scan (8192-element tiles, 2-tile chunks): a chunk
+    that never publishes makes its successor's look-back time out even when
+    later chunks hold heads and publish their own prefixes at once."""
+    n = 200 * 8192 + 77
+    rng = np.random.default_rng(3)
+    x = rng.integers(0, 100, n).astype(np.uint32)
+    h = (rng.random(n) < density).astype(np.uint8)
+    assert sc.sc_debug_set_lookback(10, -1, 0, 50_000_000) == sc.SC_OK  # chunk 5 never publishes
+    try:
+        st, _ = _raw_segscan(x, h)
+        assert st == sc.SC_OK
+        assert sc.sc_get_device_error(stream()) == sc.SC_ERR_LOOKBACK_TIMEOUT
+    finally:
+        sc.sc_debug_set_lookback(-1, -1, 0, 0)
+    st, y = _raw_segscan(x, h)
+    assert st == sc.SC_OK and sc.sc_get_device_error(stream()) == sc.SC_OK
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), oracle.scan_segmented(x, h, "sum", True))
+
+
+@pytest.mark.parametrize("delay_tile", [0, 9, 64])
+def test_slow_chunk_in_segmented_scan_gives_exact_results(delay_tile):
+    n = 150 * 8192 + 5
+    rng = np.random.default_rng(delay_tile + 1)
+    x = rng.integers(0, 1 << 32, n, dtype=np.uint64).astype(np.uint32)
+    h = (rng.random(n) < 2e-5).astype(np.uint8)          # most chunks without a head: long chains
+    sc.sc_debug_set_lookback(-1, delay_tile, 2_000_000, 0)
+    try:
+        st, y = _raw_segscan(x, h)
+        assert st == sc.SC_OK and sc.sc_get_device_error(stream()) == sc.SC_OK
+    finally:
+        sc.sc_debug_set_lookback(-1, -1, 0, 0)
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), oracle.scan_segmented(x, h, "sum", True))
