@@ -169,9 +169,8 @@ sc_status sc_scan_batched(sc_dtype dtype, sc_op op, int exclusive, const void *i
  * "is this the first element of its segment that satisfies the condition";
  * the head-flag form is the plain reading of a segment boundary.  Every
  * (dtype, op) pair of the plain scans; in == out is allowed; d_heads must not
- * overlap out.  One launch: operators with 4-byte elements other than the
- * float32 sum, on 16-byte aligned in, out and d_heads of at least 8192
- * elements, run on the persistent
+ * overlap out.  One launch: operators with 4-byte elements, on 16-byte
+ * aligned in, out and d_heads of at least 8192 elements, run on the persistent
  * kernel (flags copied in bulk beside each tile; a chunk of tiles that holds a
  * head publishes its complete prefix at once), everything else on the
  * one-tile-per-CTA kernel (likewise per tile). */

@@ -25,7 +25,8 @@
 //   persistent scan, with (value, flag) pairs as carries.
 //
 // Each value is read from HBM once (and once more from L2) and written once;
-// each flag is read once.  Operators with 4-byte elements and carries only.
+// each flag is read once.  Operators with 4-byte elements whose (value, flag)
+// pair fits 8 bytes: those whose carry is the element, and the float32 sum.
 #pragma once
 #include "sc_scan_tma.cuh"
 
@@ -34,18 +35,43 @@ namespace scg {
 namespace {
 
 // The pair form of a 4-byte operator: x = the value's bits, y = the flag.
+// make() builds a pair from a value, value() reads the carry back as an
+// element, flag() tells whether a head was seen.
 template <class Op>
 struct SegPairOp {
     using T = typename Op::T;
     using C = uint2;
     static_assert(sizeof(T) == 4 && std::is_same<typename Op::C, T>::value, "4-byte operators with C == T");
-    __device__ __forceinline__ static C c_identity() { return make_uint2(to_bits32(Op::identity()), 0u); }
+    __device__ __forceinline__ static C make(T v, bool f) { return make_uint2(to_bits32(v), f ? 1u : 0u); }
+    __device__ __forceinline__ static T value(C c) { T v; from_bits32(c.x, v); return v; }
+    __device__ __forceinline__ static bool flag(C c) { return c.y != 0u; }
+    __device__ __forceinline__ static C c_identity() { return make(Op::identity(), false); }
     __device__ __forceinline__ static C c_op(C a, C b) {
         if (b.y) return b;
-        T av, bv;
-        from_bits32(a.x, av);
-        from_bits32(b.x, bv);
-        return make_uint2(to_bits32(Op::op(av, bv)), a.y);
+        return make(Op::op(value(a), value(b)), a.y != 0u);
+    }
+};
+
+// The float32 sum: a float-float carry (high, low) whose low part's lowest
+// mantissa bit holds the flag (a change of at most 2^-48 of the carry, below
+// its 2^-44 precision), so that the pair stays 8 bytes.
+template <>
+struct SegPairOp<OpSumF32> {
+    using T = float;
+    using C = float2;
+    __device__ __forceinline__ static C tag(float2 v, bool f) {
+        return make_float2(v.x, __uint_as_float((__float_as_uint(v.y) & ~1u) | (f ? 1u : 0u)));
+    }
+    __device__ __forceinline__ static float2 plain(C c) {
+        return make_float2(c.x, __uint_as_float(__float_as_uint(c.y) & ~1u));
+    }
+    __device__ __forceinline__ static C make(T v, bool f) { return tag(make_float2(v, 0.0f), f); }
+    __device__ __forceinline__ static T value(C c) { return OpSumF32::lower(plain(c)); }
+    __device__ __forceinline__ static bool flag(C c) { return (__float_as_uint(c.y) & 1u) != 0u; }
+    __device__ __forceinline__ static C c_identity() { return make(0.0f, false); }
+    __device__ __forceinline__ static C c_op(C a, C b) {
+        if (flag(b)) return b;
+        return tag(OpSumF32::c_op(plain(a), plain(b)), flag(a));
     }
 };
 
@@ -83,7 +109,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                        const ScanParams p, const long long n_full_tiles) {
     using T = typename Op::T;
     using PO = SegPairOp<Op>;
-    using C = uint2;
+    using C = typename PO::C;
     using Ctrl = typename Cfg::Ctrl;
     constexpr int kTileBytes = Cfg::kTileBytes, kSA = Cfg::kSA, kSB = Cfg::kSB, kChunk = Cfg::kChunk;
     constexpr int kLag = Cfg::kLag, kComputeWarps = Cfg::kComputeWarps, kChunkSlots = Cfg::kChunkSlots;
@@ -246,7 +272,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     ctl->chunk_id[q % kChunkSlots] = c;
                     const bool stalled = p.lb.stall_tile >= 0 && p.lb.stall_tile / kChunk == c;
                     if (p.lb.delay_tile >= 0 && p.lb.delay_tile / kChunk == c) hook_delay(p.lb.delay_ns);
-                    if (!stalled) StatusIO<C>::publish(p.lb, c, (c == 0 || run.y) ? ST_PREFIX : ST_AGGREGATE, run);
+                    if (!stalled)
+                        StatusIO<C>::publish(p.lb, c, (c == 0 || PO::flag(run)) ? ST_PREFIX : ST_AGGREGATE, run);
                     mbar_arrive(B(ctl->agg[q % kChunkSlots]));
                 }
                 mbar_arrive(B(ctl->p1done[k % kR1]));
@@ -274,7 +301,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             if (lane == 0) {
                 const C agg = unpack_bits<C>(ctl->chunk_agg[q % kChunkSlots]);
                 const bool stalled = p.lb.stall_tile >= 0 && p.lb.stall_tile / kChunk == c;
-                if (ok && c != 0 && !agg.y && !stalled) StatusIO<C>::publish(p.lb, c, ST_PREFIX, PO::c_op(prefix, agg));
+                if (ok && c != 0 && !PO::flag(agg) && !stalled)
+                    StatusIO<C>::publish(p.lb, c, ST_PREFIX, PO::c_op(prefix, agg));
                 ctl->chunk_prefix[q % kChunkSlots] = pack_bits(prefix);
                 mbar_arrive(B(ctl->pre[q % kChunkSlots]));
             }
@@ -323,7 +351,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         T acc = v[0];
 #pragma unroll
         for (int w = 1; w < IPT; ++w) acc = ((hm >> w) & 1u) ? v[w] : Op::op(acc, v[w]);
-        return make_uint2(to_bits32(acc), hm != 0u ? 1u : 0u);
+        return PO::make(acc, hm != 0u);
     };
 
     // pass 1: head mask kept for pass 2, warp total published to the bookkeeping warp
@@ -370,8 +398,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             }
             C cin = shfl_up_v(x, 1);
             cin = lane == 0 ? base : PO::c_op(base, cin);
-            T run;
-            from_bits32(cin.x, run);
+            T run = PO::value(cin);
             if constexpr (kExcl) {
 #pragma unroll
                 for (int w = 0; w < IPT; ++w) {
