@@ -48,7 +48,7 @@ struct SegPairOp {
     __device__ __forceinline__ static C c_identity() { return make(Op::identity(), false); }
     __device__ __forceinline__ static C c_op(C a, C b) {
         if (b.y) return b;
-        return make(Op::op(value(a), value(b)), a.y != 0u);
+        return make_uint2(to_bits32(Op::op(value(a), value(b))), a.y);  // the flag passes through as is
     }
 };
 
