@@ -327,6 +327,12 @@ def suite_lines(args, dev, sc, synth):
     ms, b = timed(lambda: sc.sc_scan_segmented(sc.SC_I32, sc.SC_SUM, 1, x.data_ptr(), h.data_ptr(), y.data_ptr(), n,
                                                sp), 9 * n)
     emit("int32_segsum_n2^27", n, ms, b, {"segments": int(h.sum().item())})
+    xf = synth.make_torch(W["float32_segsum_n2^27"], device=dev)
+    yf = torch.empty_like(xf)
+    ms, b = timed(lambda: sc.sc_scan_segmented(sc.SC_F32, sc.SC_SUM, 1, xf.data_ptr(), h.data_ptr(), yf.data_ptr(), n,
+                                               sp), 9 * n)
+    emit("float32_segsum_n2^27", n, ms, b, {"segments": int(h.sum().item())})
+    del xf, yf
     # bin offsets (histogram + exclusive scan): CSR row offsets of a COO matrix, radix digit bucket starts
     for name, nbins in (("csr_rows_2^22", W["csr_rows_2^22"]["nrows"]), ("digit_bins_n2^27", 256)):
         bins = synth.make_torch(W[name], device=dev)

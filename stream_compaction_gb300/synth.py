@@ -247,6 +247,9 @@ WORKLOADS = {
     # segmented sum: values as the batched rows, heads with mean segment length 1024
     "int32_segsum_n2^27": dict(kind="int", n=1 << 27, lo=0, hi=255, seed=9, offset=0, op="sum",
                                heads=dict(seed=9, offset=SUBSTREAM, period=1024)),
+    # the same heads over float32 values on [-1, 1)
+    "float32_segsum_n2^27": dict(kind="pm1", n=1 << 27, seed=13, offset=0, op="sum",
+                                 heads=dict(seed=9, offset=SUBSTREAM, period=1024)),
     # bin offsets: the CSR row offsets of a COO matrix with 2^22 sorted rows
     # (about 2^27 entries), and the start of each bucket of an 8-bit radix digit
     "csr_rows_2^22": dict(kind="coo_rows", nrows=1 << 22, seed=10, offset=0),

@@ -148,6 +148,12 @@ def test_segmented_workload_full_size():
     x = xt.cpu().numpy()
     h = synth.make_heads_np(spec)
     assert np.array_equal(gpu_segmented(x, h, "sum", True), oracle.scan_segmented(x, h, "sum", True))
+    spec = synth.WORKLOADS["float32_segsum_n2^27"]
+    xt = synth.make_torch(spec, device="cuda")
+    torch.cuda.synchronize()
+    x = xt.cpu().numpy()
+    scale = oracle.scan_segmented(np.abs(x.astype(np.float64)), h, "sum", False)
+    check_f32(gpu_segmented(x, h, "sum", True), oracle.scan_segmented(x, h, "sum", True), scale)
 
 
 @pytest.mark.parametrize("op", ["sum", "max"])
