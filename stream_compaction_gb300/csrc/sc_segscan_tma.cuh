@@ -34,41 +34,57 @@ namespace scg {
 
 namespace {
 
-// The pair form of a 4-byte operator: x = the value's bits, y = the flag.
-// make() builds a pair from a value, value() reads the carry back as an
-// element, flag() tells whether a head was seen.
+// Pair forms of a 4-byte operator.  E: the in-tile pair (x = the element's
+// bits, y = the flag), combined in the element type; C: the carry pair that
+// travels between tiles.  make() builds an E from a value, value() reads an
+// E back, lift() / lower() convert between E and C, flag() reads C's flag.
 template <class Op>
 struct SegPairOp {
     using T = typename Op::T;
+    using E = uint2;
     using C = uint2;
     static_assert(sizeof(T) == 4 && std::is_same<typename Op::C, T>::value, "4-byte operators with C == T");
-    __device__ __forceinline__ static C make(T v, bool f) { return make_uint2(to_bits32(v), f ? 1u : 0u); }
-    __device__ __forceinline__ static T value(C c) { T v; from_bits32(c.x, v); return v; }
-    __device__ __forceinline__ static bool flag(C c) { return c.y != 0u; }
-    __device__ __forceinline__ static C c_identity() { return make(Op::identity(), false); }
-    __device__ __forceinline__ static C c_op(C a, C b) {
+    __device__ __forceinline__ static E make(T v, bool f) { return make_uint2(to_bits32(v), f ? 1u : 0u); }
+    __device__ __forceinline__ static T value(E e) { T v; from_bits32(e.x, v); return v; }
+    __device__ __forceinline__ static E e_identity() { return make(Op::identity(), false); }
+    __device__ __forceinline__ static E e_op(E a, E b) {
         if (b.y) return b;
         return make_uint2(to_bits32(Op::op(value(a), value(b))), a.y);  // the flag passes through as is
     }
+    __device__ __forceinline__ static C lift(E e) { return e; }
+    __device__ __forceinline__ static E lower(C c) { return c; }
+    __device__ __forceinline__ static bool flag(C c) { return c.y != 0u; }
+    __device__ __forceinline__ static C c_identity() { return e_identity(); }
+    __device__ __forceinline__ static C c_op(C a, C b) { return e_op(a, b); }
 };
 
 // The float32 sum: a float-float carry (high, low) whose low part's lowest
 // mantissa bit holds the flag (a change of at most 2^-48 of the carry, below
 // its 2^-44 precision), so that the pair stays 8 bytes.
+// Inside a tile the float32 sum's pairs are float32 (as in the plain scan);
+// between tiles its carry is a float-float pair.
 template <>
 struct SegPairOp<OpSumF32> {
     using T = float;
+    using E = uint2;
     using C = float2;
+    __device__ __forceinline__ static E make(T v, bool f) { return make_uint2(__float_as_uint(v), f ? 1u : 0u); }
+    __device__ __forceinline__ static T value(E e) { return __uint_as_float(e.x); }
+    __device__ __forceinline__ static E e_identity() { return make(0.0f, false); }
+    __device__ __forceinline__ static E e_op(E a, E b) {
+        if (b.y) return b;
+        return make_uint2(__float_as_uint(__fadd_rn(value(a), value(b))), a.y);
+    }
     __device__ __forceinline__ static C tag(float2 v, bool f) {
         return make_float2(v.x, __uint_as_float((__float_as_uint(v.y) & ~1u) | (f ? 1u : 0u)));
     }
     __device__ __forceinline__ static float2 plain(C c) {
         return make_float2(c.x, __uint_as_float(__float_as_uint(c.y) & ~1u));
     }
-    __device__ __forceinline__ static C make(T v, bool f) { return tag(make_float2(v, 0.0f), f); }
-    __device__ __forceinline__ static T value(C c) { return OpSumF32::lower(plain(c)); }
     __device__ __forceinline__ static bool flag(C c) { return (__float_as_uint(c.y) & 1u) != 0u; }
-    __device__ __forceinline__ static C c_identity() { return make(0.0f, false); }
+    __device__ __forceinline__ static C lift(E e) { return tag(make_float2(value(e), 0.0f), e.y != 0u); }
+    __device__ __forceinline__ static E lower(C c) { return make(OpSumF32::lower(plain(c)), flag(c)); }
+    __device__ __forceinline__ static C c_identity() { return tag(make_float2(0.0f, 0.0f), false); }
     __device__ __forceinline__ static C c_op(C a, C b) {
         if (flag(b)) return b;
         return tag(OpSumF32::c_op(plain(a), plain(b)), flag(a));
@@ -109,7 +125,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                        const ScanParams p, const long long n_full_tiles) {
     using T = typename Op::T;
     using PO = SegPairOp<Op>;
-    using C = typename PO::C;
+    using C = typename PO::C;  // carries between tiles
+    using E = typename PO::E;  // pairs inside a tile
     using Ctrl = typename Cfg::Ctrl;
     constexpr int kTileBytes = Cfg::kTileBytes, kSA = Cfg::kSA, kSB = Cfg::kSB, kChunk = Cfg::kChunk;
     constexpr int kLag = Cfg::kLag, kComputeWarps = Cfg::kComputeWarps, kChunkSlots = Cfg::kChunkSlots;
@@ -254,17 +271,17 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         C run = PO::c_identity();
         for (int k = 0;; ++k) {
             if (!warp_bar_wait(B(ctl->wready[k % kR1]), (k / kR1) & 1, wait_limit, end_k, k)) break;
-            C wv = lane < kComputeWarps ? unpack_bits<C>(ctl->wtot[k % kRing][lane]) : PO::c_identity();
+            E wv = lane < kComputeWarps ? unpack_bits<E>(ctl->wtot[k % kRing][lane]) : PO::e_identity();
 #pragma unroll
             for (int d = 1; d < kComputeWarps; d <<= 1) {  // ordered: lane 0 ends with warps 0..kComputeWarps-1
-                const C y = shfl_down_v(wv, d);
-                if (lane + d < kComputeWarps) wv = PO::c_op(wv, y);
+                const E y = shfl_down_v(wv, d);
+                if (lane + d < kComputeWarps) wv = PO::e_op(wv, y);
             }
             const int pos = k % kChunk;
             if (pos == 0) run = PO::c_identity();
             if (lane == 0) {
                 ctl->offset[k % kRing] = pack_bits(run);
-                run = PO::c_op(run, wv);
+                run = PO::c_op(run, PO::lift(wv));
                 if (pos == kChunk - 1) {
                     const int q = k / kChunk;
                     const long long c = ((long long)ctl->tile[(k - pos) % kRing]) / kChunk;
@@ -356,15 +373,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 
     // pass 1: head mask kept for pass 2, warp total published to the bookkeeping warp
     auto finish1 = [&](int k, int s, unsigned tu, const T (&v)[IPT]) {
-        C tot = PO::c_identity();
+        E tot = PO::e_identity();
         if (tu != kVoid) {
             const uint32_t hm = heads_of(s, (long long)tu);
             hmask[(k % kMaskSlots) * kCompute + ctid] = hm;
             tot = thread_total(v, hm);
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {  // ordered: lane 0 ends with lanes 0..31
-                const C y = shfl_down_v(tot, d);
-                if (lane + d < 32) tot = PO::c_op(tot, y);
+                const E y = shfl_down_v(tot, d);
+                if (lane + d < 32) tot = PO::e_op(tot, y);
             }
         }
         if (lane == 0) ctl->wtot[k % kRing][warp] = pack_bits(tot);
@@ -381,23 +398,25 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         if (tu != kVoid) {
             const long long t = tu;
             const uint32_t hm = hmask[(j % kMaskSlots) * kCompute + ctid];
-            C wv = lane < kComputeWarps ? unpack_bits<C>(ctl->wtot[j % kRing][lane]) : PO::c_identity();
+            E wv = lane < kComputeWarps ? unpack_bits<E>(ctl->wtot[j % kRing][lane]) : PO::e_identity();
 #pragma unroll
             for (int d = 1; d < kComputeWarps; d <<= 1) {
-                const C y = shfl_up_v(wv, d);
-                if (lane >= d) wv = PO::c_op(y, wv);
+                const E y = shfl_up_v(wv, d);
+                if (lane >= d) wv = PO::e_op(y, wv);
             }
-            const C wpre = shfl_idx_v(wv, warp > 0 ? warp - 1 : 0);
-            C base = PO::c_op(unpack_bits<C>(ctl->chunk_prefix[q % kChunkSlots]), unpack_bits<C>(ctl->offset[j % kRing]));
-            if (warp > 0) base = PO::c_op(base, wpre);
-            C x = thread_total(v, hm);
+            const E wpre = shfl_idx_v(wv, warp > 0 ? warp - 1 : 0);
+            // the tile's prefix in carry precision, then the element type
+            E base = PO::lower(
+                PO::c_op(unpack_bits<C>(ctl->chunk_prefix[q % kChunkSlots]), unpack_bits<C>(ctl->offset[j % kRing])));
+            if (warp > 0) base = PO::e_op(base, wpre);
+            E x = thread_total(v, hm);
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
-                const C y = shfl_up_v(x, d);
-                if (lane >= d) x = PO::c_op(y, x);
+                const E y = shfl_up_v(x, d);
+                if (lane >= d) x = PO::e_op(y, x);
             }
-            C cin = shfl_up_v(x, 1);
-            cin = lane == 0 ? base : PO::c_op(base, cin);
+            E cin = shfl_up_v(x, 1);
+            cin = lane == 0 ? base : PO::e_op(base, cin);
             T run = PO::value(cin);
             if constexpr (kExcl) {
 #pragma unroll
