@@ -38,6 +38,7 @@ struct OpSumU32 {  // int32 and uint32 sums: two's-complement wraparound mod 2^3
 // |a| + |b|; float32 operations only.
 __device__ __forceinline__ float2 ff_add(float2 a, float2 b) {
     const float s = __fadd_rn(a.x, b.x);
+    if (!isfinite(s)) return make_float2(s, 0.0f);  // inf or NaN, as a float32 sum gives it; no low part
     const float bv = __fsub_rn(s, a.x);
     const float e = __fadd_rn(__fsub_rn(a.x, __fsub_rn(s, bv)), __fsub_rn(b.x, bv));  // a.x + b.x == s + e exactly
     const float lo = __fadd_rn(e, __fadd_rn(a.y, b.y));

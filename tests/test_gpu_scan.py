@@ -171,3 +171,29 @@ def test_workload_uint32_exsum_n2p30():
     y = gpu_scan(x, "sum", True)
     ref = oracle.scan(x, "sum", True)
     assert np.array_equal(y, ref)
+
+
+def test_float32_sum_infinities_cross_tiles():
+    """Infinities and NaN carried between tiles and chunks stay what a float32 sum
+    makes of them: +inf after a +inf, NaN once -inf has followed, in the
+    persistent scan and in the persistent segmented scan (a head resets)."""
+    from test_gpu_segmented import gpu_segmented
+    n = (1 << 21) + 3 * 8192 + 5                      # persistent kernels: several tiles and chunks
+    rng = np.random.default_rng(17)
+    x = rng.uniform(-1, 1, n).astype(np.float32)
+    x[5000] = np.inf
+    x[(1 << 20) + 77] = -np.inf
+    for ex in (False, True):
+        y = gpu_scan(x, "sum", ex)
+        ref = oracle.scan(x, "sum", ex)
+        assert np.array_equal(np.isnan(y), np.isnan(ref)) and np.array_equal(np.isposinf(y), np.isposinf(ref))
+        fin = np.isfinite(ref)
+        assert np.allclose(y[fin], ref[fin], rtol=0, atol=1e-3)
+    h = np.zeros(n, np.uint8)
+    h[[100000, 1 << 20, (1 << 20) + 500000]] = 1          # the second -inf segment ends at the third head
+    for ex in (False, True):
+        y = gpu_segmented(x, h, "sum", ex)
+        ref = oracle.scan_segmented(x, h, "sum", ex)
+        assert np.array_equal(np.isnan(y), np.isnan(ref)) and np.array_equal(np.isinf(y), np.isinf(ref))
+        fin = np.isfinite(ref)
+        assert np.allclose(y[fin], ref[fin], rtol=0, atol=1e-3)
