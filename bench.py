@@ -40,7 +40,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=4)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--variant", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--suite", action="store_true")
@@ -459,7 +459,11 @@ def run_ours(args, rank, world, local_rank):
             raise RuntimeError(sc.status_string(st))
     hyn = hy.numpy().view(np.uint32)
     assert np.array_equal(hyn[:head], want), "e2e output mismatch"
-    e2e_value = n / statistics.mean(e2e_t) / 1e9
+    # median over the steps: on these hosts an occasional call stalls for about
+    # 150 ms outside the library (the same call otherwise takes 26 ms); the mean
+    # and every step's time are reported beside it
+    e2e_value = n / statistics.median(e2e_t) / 1e9
+    e2e_mean = n / statistics.mean(e2e_t) / 1e9
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -488,7 +492,8 @@ def run_ours(args, rank, world, local_rank):
         "hbm_gbs": achieved,
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "Gelem/s", "h2d_bytes_per_step": 4 * n, "d2h_bytes_per_step": 4 * n,
-                "steps": args.e2e_steps, "api": "sc_scan_host (pinned host buffers)"},
+                "steps": args.e2e_steps, "statistic": "median", "mean_value": e2e_mean,
+                "step_ms": [round(1e3 * t, 2) for t in e2e_t], "api": "sc_scan_host (pinned host buffers)"},
         "gpu_launches": launches,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_kind": peak_kind, "algorithmic_bytes_per_launch": alg_bytes},
