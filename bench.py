@@ -460,8 +460,8 @@ def run_ours(args, rank, world, local_rank):
     hyn = hy.numpy().view(np.uint32)
     assert np.array_equal(hyn[:head], want), "e2e output mismatch"
     # median over the steps: on these hosts an occasional call stalls for about
-    # 150 ms outside the library (the same call otherwise takes 26 ms); the mean
-    # and every step's time are reported beside it
+    # 150 ms (cause not identified; the same call otherwise takes 26 ms); the
+    # mean and every step's time are reported beside it
     e2e_value = n / statistics.median(e2e_t) / 1e9
     e2e_mean = n / statistics.mean(e2e_t) / 1e9
 
