@@ -11,7 +11,18 @@ Prints ONE JSON line (rank 0).  Usage:
 Under torchrun (N > 1) every rank scans its own replica of the workload on its
 own GPU (no collective on the data path: the work does not shard across
 GPUs); timing is the max over ranks.
-    --suite   also print one extra line per other workload (parity cases)
+
+The line's "configs" object holds one entry per configuration of the metric
+(int32 sums n = 2^20+17, float32 sum 2^26, int32 compaction 2^27, int32 max
+2^27, affine maps 2^26, the headline, 65536 x 4096 batched rows) and the
+small-row batched shapes: mean and median ms per launch with the L2 flushed
+before every launch (config 1 also back to back), GB/s and the fraction of the
+measured copy peak, the clocks over that entry's own timed region, a check of
+every output (the recurrence that defines the scan, mask selection for the
+compaction, the float32 bound against a float64 cumsum), and, in the CPU
+baseline leg, the oracle timed on the same input and compared with the GPU
+result.  --no-configs skips them.
+    --suite   also print one extra line per other workload (added operators)
 """
 from __future__ import annotations
 
@@ -25,6 +36,8 @@ import subprocess
 import sys
 import threading
 import time
+
+import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -44,6 +57,8 @@ def parse():
     ap.add_argument("--variant", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--suite", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration measurements (the configs object of the JSON line)")
     ap.add_argument("--profile-case", type=int, default=0, metavar="N",
                     help="no timing: run the headline scan on the first N elements --steps times (for ncu)")
     ap.add_argument("--profile-op", default="scan", choices=["scan", "scan_f32", "compact", "rows", "hier", "radix", "sort", "csr", "segsum"],
@@ -97,7 +112,10 @@ def recorded_traffic():
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+    """nvidia-smi clocks / throttle reasons sampled while timed regions run.
+
+    One sampling process runs from start() to close(); window(t0, t1) sums up
+    the samples taken between two host times (one timed region)."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -116,25 +134,22 @@ class ClockSampler:
             self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
-            return
+            return self
         self.t = threading.Thread(target=self._read, daemon=True)
         self.t.start()
         time.sleep(0.15)
+        return self
 
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append((time.time(), line.strip()))
 
-    def stop(self, t0, t1):
+    def window(self, t0, t1):
         if not self.proc:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.1)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        rows = [l for ts, l in self.lines if t0 - 0.06 <= ts <= t1 + 0.06] or [l for _, l in self.lines[-2:]]
+        time.sleep(0.12)  # the sample that covers t1 arrives up to one period later
+        rows = [l for ts, l in list(self.lines) if t0 - 0.06 <= ts <= t1 + 0.06] or \
+            [l for _, l in list(self.lines)[-2:]]
         sm, smax, reasons, power = [], [], set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
@@ -152,6 +167,21 @@ class ClockSampler:
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+
+    def close(self):
+        if not self.proc:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.proc = None
+
+    def stop(self, t0, t1):
+        w = self.window(t0, t1)
+        self.close()
+        return w
 
 
 def gpu_uuid(dev):
@@ -352,6 +382,245 @@ def suite_lines(args, dev, sc, synth):
     del flush
 
 
+# ------------------------------------------------- every configuration, measured
+# Full checks of a GPU result by the recurrence that defines the scan (no oracle:
+# y[0] and every y[i] from y[i-1] and one input element).  Together with y[0]
+# the recurrence fixes every output, so a check that passes at every index
+# proves the whole result.
+def _check_sum_u32(x, y, exclusive):
+    xu, yu = x.view(np.uint32).reshape(-1), y.view(np.uint32).reshape(-1)
+    if exclusive:
+        return bool(yu[0] == 0 and np.array_equal(yu[1:] - yu[:-1], xu[:-1]))
+    return bool(yu[0] == xu[0] and np.array_equal(yu[1:] - yu[:-1], xu[1:]))
+
+
+def _check_max_i32(x, y):
+    return bool(y[0] == x[0] and np.array_equal(y[1:], np.maximum(y[:-1], x[1:])))
+
+
+def _check_affine(x, y):
+    """Inclusive scan of maps h -> a*h + b (mod 2^32), the earlier map applied
+    first: y[i] = (a_i * A, a_i * B + b_i) with (A, B) = y[i-1]."""
+    a, b = x[:, 0].astype(np.uint32), x[:, 1].astype(np.uint32)
+    ya, yb = y[:, 0].astype(np.uint32), y[:, 1].astype(np.uint32)
+    ok = ya[0] == a[0] and yb[0] == b[0]
+    return bool(ok and np.array_equal(ya[1:], a[1:] * ya[:-1]) and np.array_equal(yb[1:], a[1:] * yb[:-1] + b[1:]))
+
+
+def _check_rows_exclusive(x, y):
+    xu, yu = x.view(np.uint32), y.view(np.uint32)
+    return bool(np.all(yu[:, 0] == 0) and np.array_equal(yu[:, 1:] - yu[:, :-1], xu[:, :-1]))
+
+
+def _f32_error_ratio(x, y, exclusive):
+    """max over i of |y_i - exact_i| / (1e-5 * sum_{k<=i} |x_k|), the exact prefix
+    from a float64 cumulative sum (its own error is far below the bound)."""
+    x64 = x.astype(np.float64)
+    exact = np.cumsum(x64)
+    if exclusive:
+        exact -= x64
+    bound = 1e-5 * np.cumsum(np.abs(x64))
+    return float(np.max(np.abs(y.astype(np.float64) - exact) / np.maximum(bound, 1e-300)))
+
+
+class ConfigRunner:
+    """Times one workload per configuration (L2 flushed before every launch, or
+    back to back for the latency-bound config), records the clocks over each
+    timed region, checks every output and, in the CPU-baseline leg, runs the
+    oracle on the same input and compares."""
+
+    def __init__(self, sc, synth, dev, sampler, peak, cpu_leg, min_s=0.4):
+        import torch
+        self.sc, self.synth, self.dev, self.sampler, self.peak = sc, synth, dev, sampler, peak
+        self.cpu_leg, self.min_s = cpu_leg, min_s
+        self.stream = torch.cuda.current_stream()
+        self.sp = int(self.stream.cuda_stream)
+        self.flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 2x L2: rewritten before each launch
+        self.out = {}
+        self.launches = 0
+
+    def _call(self, fn):
+        st = fn()
+        if st != self.sc.SC_OK:
+            raise RuntimeError(self.sc.status_string(st))
+
+    def timed(self, fn, flushed=True):
+        """Mean / median ms per launch (CUDA events on the launching stream) over
+        enough launches to fill min_s, and the host-time window of the region."""
+        import torch
+        for _ in range(3):
+            self._call(fn)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        self._call(fn)
+        e1.record(self.stream)
+        e1.synchronize()
+        one = max(e0.elapsed_time(e1), 1e-3) + (0.08 if flushed else 0.0)
+        iters = int(min(20000, max(20, self.min_s * 1e3 / one)))
+        l0 = self.sc.sc_launch_count()
+        if flushed:
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+            torch.cuda.synchronize()
+            t0 = time.time()
+            for a, b in evs:
+                self.flush.add_(1)
+                a.record(self.stream)
+                self._call(fn)
+                b.record(self.stream)
+            torch.cuda.synchronize()
+            t1 = time.time()
+            ms = [a.elapsed_time(b) for a, b in evs]
+            mean, med = statistics.mean(ms), statistics.median(ms)
+        else:
+            torch.cuda.synchronize()
+            t0 = time.time()
+            e0.record(self.stream)
+            for _ in range(iters):
+                self._call(fn)
+            e1.record(self.stream)
+            e1.synchronize()
+            t1 = time.time()
+            mean = med = e0.elapsed_time(e1) / iters
+        self.launches += self.sc.sc_launch_count() - l0
+        if self.sc.sc_get_device_error(self.sp) != self.sc.SC_OK:
+            raise RuntimeError("device error in a timed region")
+        return mean, med, iters, self.sampler.window(t0, t1) if self.sampler else None
+
+    def entry(self, name, n, nbytes, timing, check, extra=None, cpu=None, l2="flushed before every launch"):
+        mean, med, iters, clocks = timing
+        gbs = nbytes / (mean * 1e-3) / 1e9
+        d = {"n": n, "ms": mean, "ms_median": med, "launches": iters, "gelem_s": n / (mean * 1e-3) / 1e9,
+             "hbm_gbs": gbs, "frac": gbs / self.peak, "algorithmic_bytes": nbytes, "l2": l2, "clocks": clocks,
+             "parity": check}
+        if extra:
+            d.update(extra)
+        if cpu is not None:
+            d["cpu_baseline"] = cpu
+        self.out[name] = d
+
+    def oracle_leg(self, fn, n, compare):
+        """The CPU-baseline leg: the oracle, as it stands, on this config's input
+        (one host core), timed; and whether it agrees with the GPU result."""
+        if not self.cpu_leg:
+            return None
+        import oracle  # noqa: F401  (the CPU-baseline leg is the one place bench.py runs the oracle)
+        t = time.perf_counter()
+        ref = fn()
+        dt = time.perf_counter() - t
+        return {"value": n / dt / 1e9, "unit": "Gelem/s", "cores": 1, "kind": "oracle", "s": dt,
+                "matches_gpu": bool(compare(ref))}
+
+
+def measure_configs(args, sc, synth, dev, sampler, peak, headline):
+    """One entry per configuration of the headline metric (and the small-row
+    batched shapes), each with its own timing, clocks and full check."""
+    import torch
+    R = ConfigRunner(sc, synth, dev, sampler, peak, cpu_leg=not args.no_cpu_baseline)
+    W = synth.WORKLOADS
+    sp = R.sp
+    cpu = R.cpu_leg
+    if cpu:
+        import oracle
+
+    # 1: int32 sum, n = 2^20 + 17, inclusive and exclusive: latency-bound, so
+    # both L2-flushed (one launch between events) and L2-warm (back to back)
+    x = synth.make_torch(W["int32_sum_n1048593"], device=dev)
+    y = torch.empty_like(x)
+    n = x.numel()
+    xh = x.cpu().numpy()
+    for ex in (False, True):
+        fn = sc.sc_scan_exclusive if ex else sc.sc_scan_inclusive
+        call = lambda: fn(sc.SC_I32, sc.SC_SUM, x.data_ptr(), y.data_ptr(), n, sp)
+        name = "1_int32_sum_n1048593_" + ("exclusive" if ex else "inclusive")
+        tf = R.timed(call, flushed=True)
+        yh = y.cpu().numpy()
+        ok = _check_sum_u32(xh, yh, ex)
+        c = R.oracle_leg(lambda: oracle.scan(xh, "sum", ex), n, lambda r: np.array_equal(r, yh))
+        tw = R.timed(call, flushed=False)
+        R.entry(name, n, 8 * n, tf, "recurrence: every output" if ok else "MISMATCH",
+                {"us_flushed": 1e3 * tf[0], "us_warm": 1e3 * tw[0], "clocks_warm": tw[3],
+                 "note": "flushed: one launch between events (includes launch latency); warm: back to back"}, c)
+
+    # 2: float32 exclusive sum, n = 2^26, within 1e-5 * sum_{k<=i} |x_k|
+    x = synth.make_torch(W["float32_exsum_n2^26"], device=dev)
+    y = torch.empty_like(x)
+    n = x.numel()
+    t = R.timed(lambda: sc.sc_scan_exclusive(sc.SC_F32, sc.SC_SUM, x.data_ptr(), y.data_ptr(), n, sp))
+    xh, yh = x.cpu().numpy(), y.cpu().numpy()
+    ratio = _f32_error_ratio(xh, yh, True)
+    c = None
+    if cpu:
+        def cmp(ref):
+            return bool(np.all(np.abs(yh.astype(np.float64) - ref) <= 1e-5 * oracle.abs_prefix(xh)))
+        c = R.oracle_leg(lambda: oracle.scan(xh, "sum", True), n, cmp)
+    R.entry("2_float32_exsum_n2^26", n, 8 * n, t,
+            "bound: every output" if ratio <= 1.0 else "OUTSIDE BOUND",
+            {"max_err_over_bound": ratio, "bound": "1e-5 * sum_{k<=i} |x_k|, exact prefix from a float64 cumsum"}, c)
+
+    # 3: compaction of int32, x > 0, n = 2^27
+    x = synth.make_torch(W["int32_compact_gt0_n2^27"], device=dev)
+    y = torch.empty_like(x)
+    cnt = torch.empty(1, dtype=torch.int64, device=dev)
+    n = x.numel()
+    t = R.timed(lambda: sc.sc_compact_if(sc.SC_I32, x.data_ptr(), y.data_ptr(), cnt.data_ptr(), n, sc.SC_GT, 0.0, sp))
+    k = int(cnt.item())
+    xh = x.cpu().numpy()
+    yk = y[:k].cpu().numpy()
+    keep = xh[xh > 0]
+    ok = k == keep.size and np.array_equal(yk, keep)
+    c = R.oracle_leg(lambda: oracle.compact(xh, "gt", 0), n, lambda r: r[1] == k and np.array_equal(r[0], yk))
+    R.entry("3_int32_compact_gt0_n2^27", n, 4 * n + 4 * k, t,
+            "count and every kept element (mask selection)" if ok else "MISMATCH",
+            {"kept": k, "bytes_note": "4n read + 4 per kept element written"}, c)
+    del keep
+
+    # 4a: int32 inclusive max, n = 2^27
+    x = synth.make_torch(W["int32_max_n2^27"], device=dev)
+    y = torch.empty_like(x)
+    n = x.numel()
+    t = R.timed(lambda: sc.sc_scan_inclusive(sc.SC_I32, sc.SC_MAX, x.data_ptr(), y.data_ptr(), n, sp))
+    xh, yh = x.cpu().numpy(), y.cpu().numpy()
+    ok = _check_max_i32(xh, yh)
+    c = R.oracle_leg(lambda: oracle.scan(xh, "max", False), n, lambda r: np.array_equal(r, yh))
+    R.entry("4a_int32_max_n2^27", n, 8 * n, t, "recurrence: every output" if ok else "MISMATCH", None, c)
+
+    # 4b: affine maps, inclusive composition, n = 2^26 pairs
+    x = synth.make_torch(W["affine_u32_n2^26"], device=dev)
+    y = torch.empty_like(x)
+    n = x.shape[0]
+    t = R.timed(lambda: sc.sc_scan_inclusive(sc.SC_AFFINE_U32, sc.SC_COMPOSE, x.data_ptr(), y.data_ptr(), n, sp))
+    xh, yh = x.cpu().numpy().view(np.uint32), y.cpu().numpy().view(np.uint32)
+    ok = _check_affine(xh, yh)
+    c = R.oracle_leg(lambda: oracle.scan(xh, "affine", False), n, lambda r: np.array_equal(r, yh))
+    R.entry("4b_affine_u32_n2^26", n, 16 * n, t, "recurrence: every output" if ok else "MISMATCH", None, c)
+    del x, y, xh, yh
+
+    # 5a: the headline (timed above, inputs 32x larger than L2)
+    R.out["5a_uint32_exsum_n2^30"] = headline
+
+    # 5b and the small-row shapes: batched row-wise int32 exclusive sums
+    x = synth.make_torch(W["int32_rows_65536x4096"], device=dev)
+    y = torch.empty_like(x)
+    n = x.numel()
+    shapes = [(65536, 4096), (1 << 22, 64), (1 << 20, 256), (1 << 24, 16)]
+    shapes += [(n // c, c) for c in (33, 1000, 2047)]   # ragged row lengths: rows start inside tiles
+    for rows, cols in shapes:
+        name = ("5b_" if cols == 4096 else "") + "int32_rows_%dx%d" % (rows, cols)
+        m = rows * cols
+        t = R.timed(lambda: sc.sc_scan_batched(sc.SC_I32, sc.SC_SUM, 1, x.data_ptr(), y.data_ptr(), rows, cols, sp))
+        xh, yh = x[:m].cpu().numpy().reshape(rows, cols), y[:m].cpu().numpy().reshape(rows, cols)
+        ok = _check_rows_exclusive(xh, yh)
+        c = R.oracle_leg(lambda: oracle.scan_batched(xh, "sum", True), m, lambda r: np.array_equal(r, yh))
+        extra = {"rows": rows, "cols": cols}
+        if cols != 4096:
+            extra["note"] = "the 65536x4096 input (its first rows*cols elements) viewed as other row lengths"
+        R.entry(name, m, 8 * m, t, "recurrence: every output of every row" if ok else "MISMATCH", extra, c)
+        del xh, yh
+    del x, y, R.flush
+    return R.out, R.launches
+
+
 def combine_ranks(ms_local: float, units_local: int, world: int, device):
     """Max of the timed region over ranks, and whole-job throughput (Gelem/s):
     every rank processed units_local elements in at most that time."""
@@ -367,7 +636,6 @@ def combine_ranks(ms_local: float, units_local: int, world: int, device):
 
 
 def run_ours(args, rank, world, local_rank):
-    import numpy as np
     import torch
     import stream_compaction_gb300 as sc
     from stream_compaction_gb300 import build as scbuild, synth
@@ -403,9 +671,7 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize()
 
-    sampler = ClockSampler(gpu_uuid(dev) if rank == 0 else None) if rank == 0 else None
-    if sampler:
-        sampler.start()
+    sampler = ClockSampler(gpu_uuid(dev)).start() if rank == 0 else None
     l0 = sc.sc_launch_count()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -418,7 +684,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     t1 = time.time()
     launches = sc.sc_launch_count() - l0
-    clocks = sampler.stop(t0, t1) if sampler else None
+    clocks = sampler.window(t0, t1) if sampler else None
     ms = e0.elapsed_time(e1)
     if sc.sc_get_device_error(sp) != sc.SC_OK:
         raise RuntimeError("device error during the timed region")
@@ -427,11 +693,11 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return
 
-    # spot check of the timed output against a host recomputation of a prefix of it
-    head = 1 << 20
-    xh = x[:head].cpu().numpy().view(np.uint32)
-    want = np.concatenate([[0], np.cumsum(xh[:-1], dtype=np.uint32)])
-    assert np.array_equal(y[:head].cpu().numpy().view(np.uint32), want), "bench output mismatch"
+    # every one of the 2^30 timed outputs, checked by the recurrence of the
+    # exclusive sum (y[0] = 0, y[i] = y[i-1] + x[i-1] mod 2^32)
+    xh = x.cpu().numpy().view(np.uint32)
+    yh = y.cpu().numpy().view(np.uint32)
+    assert _check_sum_u32(xh, yh, True), "bench output mismatch"
 
     peak, peak_kind = peaks()
     alg_bytes = 8 * n
@@ -458,27 +724,41 @@ def run_ours(args, rank, world, local_rank):
         if st != sc.SC_OK:
             raise RuntimeError(sc.status_string(st))
     hyn = hy.numpy().view(np.uint32)
-    assert np.array_equal(hyn[:head], want), "e2e output mismatch"
+    assert np.array_equal(hyn, yh), "e2e output differs from the device-buffer scan"
     # median over the steps: on these hosts an occasional call stalls for about
     # 150 ms (cause not identified; the same call otherwise takes 26 ms); the
     # mean and every step's time are reported beside it
     e2e_value = n / statistics.median(e2e_t) / 1e9
     e2e_mean = n / statistics.mean(e2e_t) / 1e9
+    del hx, hy, hyn
 
     cpu = None
+    parity_5a = "recurrence: every output"
     if not args.no_cpu_baseline:
         import oracle
-        xn = hx.numpy().view(np.uint32)
         ts = []
         for _ in range(3):
             t = time.perf_counter()
-            ref = oracle.scan(xn, "sum", True)
+            ref = oracle.scan(xh, "sum", True)
             ts.append(time.perf_counter() - t)
-        assert np.array_equal(ref[:head], want) and np.array_equal(ref[-head:], hyn[-head:])
+        match = bool(np.array_equal(ref, yh))
+        assert match, "oracle disagrees with the timed output"
         del ref
+        parity_5a += "; oracle: every output equal"
         cpu = {"value": n / statistics.median(ts) / 1e9, "unit": "Gelem/s", "cores": 1, "kind": "oracle",
                "sample": "the full n=2^30 workload, 3 runs, median (sequential C loop, one thread)",
-               "host_cpus": os.cpu_count()}
+               "host_cpus": os.cpu_count(), "matches_gpu": match}
+    del xh, yh
+
+    headline = {"n": n, "ms": ms_step, "gelem_s": n / (ms_step * 1e-3) / 1e9, "hbm_gbs": achieved,
+                "frac": achieved / peak, "algorithmic_bytes": alg_bytes, "launches": args.steps,
+                "l2": "inputs 32x larger than L2, no flush", "clocks": clocks, "parity": parity_5a,
+                "note": "the headline line's own timed region"}
+    configs, cfg_launches = ({}, 0)
+    if not args.no_configs:
+        configs, cfg_launches = measure_configs(args, sc, synth, dev, sampler, peak, headline)
+    if sampler:
+        sampler.close()
 
     st_, nt, ipt, ld = sc.sc_scan_variant_info(args.variant)
     line = {
@@ -501,10 +781,11 @@ def run_ours(args, rank, world, local_rank):
         "comparison": {"hierarchical_ms": hms, "hierarchical_gelem_s": n / hms / 1e6,
                        "single_pass_speedup": hms / ms_step,
                        "torch_cumsum_ms": cms, "torch_cumsum_gelem_s": n / cms / 1e6},
+        "configs": configs,
+        "configs_gpu_launches": cfg_launches,
     }
     print(json.dumps(line), flush=True)
     if args.suite:
-        del hx, hy
         suite_lines(args, dev, sc, synth)
 
 
