@@ -268,19 +268,37 @@ sc_status sc_scan_host(sc_dtype dtype, sc_op op, int exclusive, const void *h_in
  *   - All calls on a device share the one array: calls whose work can overlap
  *     on the GPU (other streams, other host threads) race and corrupt each
  *     other.  Order them on one stream, or serialise them.
- *   - Each call clears the counter and error word it uses with a 16-byte
- *     cudaMemsetAsync on `stream`, then launches one scan kernel.
- *   - There is no error query for this path: look-back waits stay bounded,
- *     and a wait that gives up (only if a CTA is starved for seconds) leaves
- *     that call's output incomplete without a report.  Its launches are not
- *     counted by sc_launch_count. */
+ *   - The cached address belongs to the device's context of that first
+ *     call: do not use this entry point across a cudaDeviceReset.
+ *   - Each call clears the tile counter it uses with an 8-byte
+ *     cudaMemsetAsync on `stream`, then launches one scan kernel.  Its
+ *     launches are not counted by sc_launch_count.
+ *   - Look-back waits stay bounded (the bound of sc_debug_set_lookback, and
+ *     its test hooks, apply here too).  A wait that gives up (only if a CTA is
+ *     starved for seconds) leaves that call's output incomplete and sets the
+ *     array's error word, which sc_scan_noalloc_error reads and clears; calls
+ *     leave the word alone. */
 #define SC_NOALLOC_MAX_N (1LL << 27)
 sc_status sc_scan_noalloc(sc_dtype dtype, sc_op op, int exclusive, const void *in, void *out, int64_t n,
                           sc_stream_t stream);
+/* Wait for `stream`, then read and clear the error word of the fixed array on
+ * the current device: SC_OK, or SC_ERR_LOOKBACK_TIMEOUT if an sc_scan_noalloc
+ * call since the last query gave up a wait.  Allocates nothing (the word is
+ * copied into a host variable). */
+sc_status sc_scan_noalloc_error(sc_stream_t stream);
 
 /* Wait for `stream`, then read and clear the device error word of its
  * workspace.  SC_OK when no kernel reported a failure since the last call. */
 sc_status sc_get_device_error(sc_stream_t stream);
+
+/* Wait for `stream`, then free the device memory the library keeps for it on
+ * the current device: its look-back workspace (unless bound by the caller
+ * with sc_set_workspace, which the library never frees) and the staging
+ * buffers, streams and events sc_scan_host set up for it.  A later call on
+ * the stream sets them up again.  Must not run while another call on the same
+ * stream is in progress in another host thread.  SC_OK also when the stream
+ * holds nothing. */
+sc_status sc_release_stream(sc_stream_t stream);
 
 /* Number of kernels this library has launched in this process (all devices). */
 uint64_t sc_launch_count(void);
@@ -298,9 +316,12 @@ uint64_t sc_launch_count(void);
  * Returns SC_ERR_INVALID for an unknown variant. */
 sc_status sc_set_scan_variant(int variant);
 /* Select the fused-compaction kernel: 0 (default) the persistent TMA kernel
- * with 8 compute warps, 1 the same with 16 compute warps, 2 the
- * one-tile-per-CTA kernel (inputs that are not 16-byte aligned, or smaller than
- * one 32 KiB tile, always use the latter).  SC_ERR_INVALID otherwise. */
+ * with 8 compute warps, each kept element stored on its own (4-byte stores);
+ * 1 the same with 16 compute warps; 2 the one-tile-per-CTA kernel (inputs that
+ * are not 16-byte aligned, or smaller than one 32 KiB tile, always use the
+ * latter); 3 the persistent kernel with 8 compute warps that packs each warp's
+ * kept elements in shared memory and writes them as aligned 16-byte stores.
+ * SC_ERR_INVALID otherwise. */
 sc_status sc_set_compact_variant(int variant);
 /* Select how the radix pass ranks a warp step's keys by digit: 0 (default)
  * __match_any_sync on the digit's top 3 bits and one ballot per lower bit;
@@ -312,6 +333,18 @@ sc_status sc_set_radix_variant(int variant);
  * for 2, threads are the CTA's compute threads) of a uint32-sum variant;
  * SC_ERR_INVALID if it does not exist. */
 sc_status sc_scan_variant_info(int variant, int *threads, int *items, int *loader);
+
+/* Kernel family of the calling host thread's last scan or compaction launch
+ * (test hook: lets a test confirm which kernel a case reached). */
+typedef enum {
+    SC_PATH_NONE = 0,
+    SC_PATH_SCAN_ONE_TILE = 1,        /* one tile per CTA (plain, segmented or batched) */
+    SC_PATH_SCAN_PERSISTENT = 2,      /* persistent TMA-pipelined scan */
+    SC_PATH_SEGSCAN_PERSISTENT = 3,   /* persistent scan segmented by head flags */
+    SC_PATH_COMPACT_PERSISTENT = 4,   /* persistent fused compaction */
+    SC_PATH_COMPACT_ONE_TILE = 5      /* one-tile-per-CTA fused compaction */
+} sc_path;
+int sc_debug_last_path(void);
 
 /* Look-back test hooks.  stall_tile >= 0: that tile never publishes its
  * status, so its successors must time out (error SC_ERR_LOOKBACK_TIMEOUT).

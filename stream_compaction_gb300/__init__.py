@@ -53,6 +53,9 @@ SIGNATURES = {
     "sc_radix_sort_u32": ([_P, _P, _P, _I64, _P], _INT),
     "sc_bin_offsets": ([_P, _I64, _I64, _P, _P], _INT),
     "sc_get_device_error": ([_P], _INT),
+    "sc_release_stream": ([_P], _INT),
+    "sc_scan_noalloc_error": ([_P], _INT),
+    "sc_debug_last_path": ([], _INT),
     "sc_launch_count": ([], _U64),
     "sc_set_scan_variant": ([_INT], _INT),
     "sc_set_compact_variant": ([_INT], _INT),
@@ -162,6 +165,23 @@ def sc_get_device_error(stream: int) -> int:
 
 def sc_launch_count() -> int:
     return load().sc_launch_count()
+
+
+def sc_release_stream(stream: int) -> int:
+    return load().sc_release_stream(stream)
+
+
+def sc_scan_noalloc_error(stream: int) -> int:
+    return load().sc_scan_noalloc_error(stream)
+
+
+# kernel families reported by sc_debug_last_path
+(SC_PATH_NONE, SC_PATH_SCAN_ONE_TILE, SC_PATH_SCAN_PERSISTENT, SC_PATH_SEGSCAN_PERSISTENT,
+ SC_PATH_COMPACT_PERSISTENT, SC_PATH_COMPACT_ONE_TILE) = range(6)
+
+
+def sc_debug_last_path() -> int:
+    return load().sc_debug_last_path()
 
 
 def sc_set_scan_variant(variant: int) -> int:

@@ -57,11 +57,13 @@ int tma_cfg_of(int v) {
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_variant{0};
 std::atomic<int> g_radix_variant{0};    // placement ranking of the radix pass (scg::launch_radix_place)
-std::atomic<int> g_compact_variant{0};  // 0, 1: persistent kernel shapes; 2: one tile per CTA
+std::atomic<int> g_compact_variant{0};  // 0, 1, 3: persistent kernel shapes; 2: one tile per CTA
 std::atomic<long long> g_stall_tile{-1};
 std::atomic<long long> g_delay_tile{-1};
 std::atomic<unsigned> g_delay_ns{0};
 std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
+// Kernel family of the calling thread's last launch (SC_PATH_*; test hook).
+thread_local int g_last_path = SC_PATH_NONE;
 
 // ------------------------------------------------------------ workspaces
 struct Workspace {
@@ -311,15 +313,18 @@ sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_le
         const unsigned nchunks = (unsigned)ceil_div(n, seg_tile * scg::segscan_tma_chunk_tiles());
         p.lb = make_ctl(*ws, nchunks);
         const unsigned grid = (unsigned)std::min<int64_t>(num_sms(), nchunks);
+        g_last_path = SC_PATH_SEGSCAN_PERSISTENT;
         const cudaError_t e = scg::launch_segscan_tma(oid, p, excl, grid, s);
         return finish_launch(*ws, nchunks + grid * (unsigned)scg::tma_ids_per_cta(), e);
     }
     p.lb = make_ctl(*ws, ntiles);
     if (use_tma) {
         const unsigned grid = (unsigned)std::min<int64_t>(num_sms(), ntiles);
+        g_last_path = SC_PATH_SCAN_PERSISTENT;
         const cudaError_t e = dispatch_scan_tma(oid, p, excl, grid, s, tma_stats, cfg);
         return finish_launch(*ws, ntiles + grid * (unsigned)scg::tma_ids_per_cta(), e);
     }
+    g_last_path = SC_PATH_SCAN_ONE_TILE;
     // a grid no larger than the SM count is resident at once, so tiles may take
     // their ids from blockIdx.x (no counter round trip): every tile a look-back
     // waits on is already running
@@ -417,7 +422,7 @@ struct HostPipe {
     std::mutex mu;
 };
 std::mutex g_pipe_mu;
-std::map<int, HostPipe*> g_pipes;
+std::map<std::pair<int, cudaStream_t>, HostPipe*> g_pipes;  // per (device, caller stream)
 constexpr size_t kPipeBufBytes = 64ull << 20;  // 64 MiB per staging buffer
 
 sc_status pipe_init(HostPipe& hp) {
@@ -439,6 +444,36 @@ sc_status pipe_init(HostPipe& hp) {
     hp.buf_bytes = kPipeBufBytes;
     hp.ready = true;
     return SC_OK;
+}
+
+// Wait for a pipe's streams, then free its staging buffers, streams and events
+// (and the look-back workspace of its internal kernel stream).
+sc_status pipe_destroy(HostPipe& hp, int dev) {
+    sc_status st = SC_OK;
+    for (cudaStream_t q : {hp.h2d, hp.cmp, hp.d2h})
+        if (q && cudaStreamSynchronize(q) != cudaSuccess) st = SC_ERR_CUDA;
+    for (int i = 0; i < HostPipe::kBufs; ++i)
+        if (hp.dbuf[i]) cudaFree(hp.dbuf[i]);
+    if (hp.carry) cudaFree(hp.carry);
+    if (hp.cmp) {
+        std::lock_guard<std::mutex> lk(g_ws_mu);
+        auto it = g_ws.find({dev, hp.cmp});
+        if (it != g_ws.end()) {
+            if (it->second.owned && it->second.base) cudaFree(it->second.base);
+            g_ws.erase(it);
+        }
+    }
+    if (hp.ready) {
+        for (int i = 0; i < HostPipe::kBufs; ++i) {
+            cudaEventDestroy(hp.ev_h2d[i]);
+            cudaEventDestroy(hp.ev_cmp[i]);
+            cudaEventDestroy(hp.ev_d2h[i]);
+        }
+        cudaEventDestroy(hp.ev_start);
+    }
+    for (cudaStream_t q : {hp.h2d, hp.cmp, hp.d2h})
+        if (q) cudaStreamDestroy(q);
+    return st;
 }
 
 }  // namespace
@@ -663,7 +698,8 @@ sc_status sc_compact_if(sc_dtype dtype, const void* in, void* out, int64_t* d_co
     const int64_t ptile = scg::compact_tma_tile_elems();
     const int cvar = g_compact_variant.load();
     const bool use_tma = p.vec_ok && n >= ptile && n / ptile * (ptile * 4 / 128) < (int64_t)INT_MAX && num_sms() > 0 &&
-                         cvar < 2;
+                         cvar != 2;
+    const int tma_shape_id = cvar == 3 ? 2 : cvar;  // public variant -> persistent kernel shape (3: packed stores)
     const int64_t unit = use_tma ? ptile * scg::compact_tma_chunk_tiles() : scg::CompactConfig::TILE;
     const unsigned ntiles = (unsigned)ceil_div(n, unit);
     std::lock_guard<std::mutex> lk(g_ws_mu);
@@ -674,11 +710,13 @@ sc_status sc_compact_if(sc_dtype dtype, const void* in, void* out, int64_t* d_co
     cudaError_t e;
     if (use_tma) {
         const unsigned grid = (unsigned)std::min<int64_t>(num_sms(), ntiles);
-        if (dtype == SC_I32) e = scg::launch_compact_tma<int32_t>(p, wide, grid, s, cvar);
-        else if (dtype == SC_U32) e = scg::launch_compact_tma<uint32_t>(p, wide, grid, s, cvar);
-        else e = scg::launch_compact_tma<float>(p, wide, grid, s, cvar);
+        if (dtype == SC_I32) e = scg::launch_compact_tma<int32_t>(p, wide, grid, s, tma_shape_id);
+        else if (dtype == SC_U32) e = scg::launch_compact_tma<uint32_t>(p, wide, grid, s, tma_shape_id);
+        else e = scg::launch_compact_tma<float>(p, wide, grid, s, tma_shape_id);
+        g_last_path = SC_PATH_COMPACT_PERSISTENT;
         return finish_launch(*ws, ntiles + grid * (unsigned)scg::tma_ids_per_cta(), e);
     }
+    g_last_path = SC_PATH_COMPACT_ONE_TILE;
     if (dtype == SC_I32) e = scg::launch_compact<int32_t>(p, wide, s);
     else if (dtype == SC_U32) e = scg::launch_compact<uint32_t>(p, wide, s);
     else e = scg::launch_compact<float>(p, wide, s);
@@ -779,7 +817,7 @@ sc_status sc_scan_host(sc_dtype dtype, sc_op op, int exclusive, const void* h_in
     HostPipe* hp;
     {
         std::lock_guard<std::mutex> lk(g_pipe_mu);
-        HostPipe*& slot = g_pipes[dev];
+        HostPipe*& slot = g_pipes[{dev, reinterpret_cast<cudaStream_t>(stream)}];
         if (!slot) slot = new HostPipe();
         hp = slot;
     }
@@ -848,6 +886,39 @@ sc_status sc_get_device_error(sc_stream_t stream) {
 
 uint64_t sc_launch_count(void) { return g_launches.load(); }
 
+sc_status sc_release_stream(sc_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SC_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SC_ERR_CUDA;
+    sc_status st = SC_OK;
+    HostPipe* hp = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_pipe_mu);
+        auto it = g_pipes.find({dev, s});
+        if (it != g_pipes.end()) {
+            hp = it->second;
+            g_pipes.erase(it);
+        }
+    }
+    if (hp) {
+        {
+            std::lock_guard<std::mutex> lk(hp->mu);  // no sc_scan_host call of this stream still inside
+            st = pipe_destroy(*hp, dev);
+        }
+        delete hp;
+    }
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    auto it = g_ws.find({dev, s});
+    if (it != g_ws.end()) {
+        if (it->second.owned && it->second.base && cudaFree(it->second.base) != cudaSuccess) st = SC_ERR_CUDA;
+        g_ws.erase(it);
+    }
+    return st;
+}
+
+int sc_debug_last_path(void) { return g_last_path; }
+
 sc_status sc_debug_lookback_stats(sc_stream_t stream, uint64_t* out8) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (!out8) return SC_ERR_INVALID;
@@ -876,7 +947,7 @@ sc_status sc_set_scan_variant(int variant) {
 }
 
 sc_status sc_set_compact_variant(int variant) {
-    if (variant < 0 || variant > 2) return SC_ERR_INVALID;
+    if (variant < 0 || variant > 3) return SC_ERR_INVALID;
     g_compact_variant.store(variant);
     return SC_OK;
 }
@@ -919,6 +990,13 @@ sc_status sc_debug_set_lookback(int64_t stall_tile, int64_t delay_tile, uint32_t
 
 // Tile sizes (host side).
 namespace scg {
+void lookback_hooks(LookbackCtl* lb) {
+    lb->stall_tile = g_stall_tile.load();
+    lb->delay_tile = g_delay_tile.load();
+    lb->delay_ns = g_delay_ns.load();
+    lb->timeout_ns = g_timeout_ns.load();
+}
+
 int scan_tile_elems(int op_id, int variant) {
     const ScanShape sh = scan_shape(op_id, variant);
     return sh.nt * sh.ipt;

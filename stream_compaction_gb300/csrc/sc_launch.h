@@ -138,6 +138,9 @@ cudaError_t launch_radix_place(const uint32_t* in, uint32_t* out, long long n, i
                                const uint32_t* offsets, long long ntiles, unsigned int* error, int variant,
                                cudaStream_t s);
 
+// The current look-back test hooks (sc_debug_set_lookback) copied into lb.
+void lookback_hooks(LookbackCtl* lb);
+
 // Hierarchical (scan-then-propagate) comparison variant.
 constexpr int kHierNT = 256;
 int hier_tile_elems(int op_id);

@@ -38,7 +38,7 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 struct DeviceSlot {
-    void* addr = nullptr;     // device address of g_noalloc_scratch on this device
+    void* addr = nullptr;     // device address of g_noalloc_scratch on this device (its context at set-up)
     unsigned epoch = 0;       // last epoch used for the status words
     bool ready = false;
 };
@@ -99,16 +99,16 @@ extern "C" sc_status sc_scan_noalloc(sc_dtype dtype, sc_op op, int exclusive, co
     if (st != SC_OK) return st;
     unsigned char* base = static_cast<unsigned char*>(slot->addr);
 
-    // The array keeps the previous call's contents.  The counter and the error
-    // word must start at zero; status words of earlier calls carry an older
-    // epoch and read as "not yet published", so they need no clearing except
-    // when the epoch wraps.
+    // The array keeps the previous call's contents.  The tile counter must
+    // start at zero; status words of earlier calls carry an older epoch and
+    // read as "not yet published", so they need no clearing except when the
+    // epoch wraps.  The error word is left alone: it collects every call's
+    // failures until sc_scan_noalloc_error reads and clears it.
     if (slot->epoch >= kMaxEpoch) {
-        if (cudaMemsetAsync(base, 0, kScratchBytes, s) != cudaSuccess) return SC_ERR_CUDA;
+        if (cudaMemsetAsync(base + kHeader, 0, kScratchBytes - kHeader, s) != cudaSuccess) return SC_ERR_CUDA;
         slot->epoch = 0;
-    } else if (cudaMemsetAsync(base, 0, 16, s) != cudaSuccess) {
-        return SC_ERR_CUDA;
     }
+    if (cudaMemsetAsync(base, 0, 8, s) != cudaSuccess) return SC_ERR_CUDA;
 
     const int tile = scg::scan_tile_elems(oid, 0);
     scg::ScanParams p;
@@ -127,10 +127,7 @@ extern "C" sc_status sc_scan_noalloc(sc_dtype dtype, sc_op op, int exclusive, co
     p.lb.epoch = ++slot->epoch;
     p.lb.num_tiles = (unsigned)((n + tile - 1) / tile);
     p.lb.static_ids = 0;
-    p.lb.stall_tile = -1;
-    p.lb.delay_tile = -1;
-    p.lb.delay_ns = 0;
-    p.lb.timeout_ns = 2000000000ull;
+    scg::lookback_hooks(&p.lb);  // the time bound, and the test hooks when set
     p.lb.stats = nullptr;
     cudaError_t e;
     switch (oid) {
@@ -140,4 +137,19 @@ extern "C" sc_status sc_scan_noalloc(sc_dtype dtype, sc_op op, int exclusive, co
     default: e = scg::launch_scan<scg::OpAffineU32>(p, exclusive != 0, false, 0, s); break;
     }
     return e == cudaSuccess ? SC_OK : SC_ERR_CUDA;
+}
+
+extern "C" sc_status sc_scan_noalloc_error(sc_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SC_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SC_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (dev < 0 || dev >= kMaxDevices) return SC_ERR_CUDA;
+    if (!g_slots[dev].ready) return SC_OK;  // no call on this device yet
+    unsigned char* base = static_cast<unsigned char*>(g_slots[dev].addr);
+    unsigned int word = 0;
+    if (cudaMemcpy(&word, base + 8, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return SC_ERR_CUDA;
+    if (word != 0 && cudaMemset(base + 8, 0, sizeof(word)) != cudaSuccess) return SC_ERR_CUDA;
+    return (sc_status)word;
 }

@@ -96,11 +96,13 @@ def gpu_batched(x: np.ndarray, op: str, exclusive: bool) -> np.ndarray:
     return to_host(xout, x)
 
 
-def gpu_compact(x: np.ndarray, pred: str, threshold: float, offset: int = 0):
+def gpu_compact(x: np.ndarray, pred: str, threshold: float, offset: int = 0, out_offset: int | None = None):
+    """Compaction through the C ABI; offset / out_offset: element offsets of the
+    input and output buffers (16-byte aligned at 0)."""
     import torch
     n = x.shape[0]
     _, xin = to_device(x, offset)
-    _, xout = dev_buffer(max(n, 1), xin.dtype, 1 if offset else 0)
+    _, xout = dev_buffer(max(n, 1), xin.dtype, (1 if offset else 0) if out_offset is None else out_offset)
     (xout.view(torch.int32) if xout.dtype == torch.float32 else xout).fill_(-7)
     cnt = torch.full((1,), -1, dtype=torch.int64, device="cuda")
     st = sc.sc_compact_if(CODE[kind_of(x, "sum")], xin.data_ptr(), xout.data_ptr(), cnt.data_ptr(), n,

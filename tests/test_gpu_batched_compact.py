@@ -19,7 +19,8 @@ def _lib():
 
 # ------------------------------------------------------------- batched rows
 SHAPES = [(1, 1), (1, 5000), (3, 1), (7, 3), (100, 17), (5, 4096), (3, 4097), (2, 10000), (1000, 33),
-          (64, 8195), (257, 4095), (9, 12289), (4096, 16)]
+          (64, 8195), (257, 4095), (9, 12289), (4096, 16), (20000, 33), (300, 1000), (50, 2047), (8192, 64),
+          (2048, 256)]
 
 
 @pytest.mark.parametrize("shape", SHAPES)
@@ -196,10 +197,11 @@ def test_scan_host_other_ops(kind, op):
         assert np.array_equal(y, ref)
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
 def test_compact_kernel_variants(variant):
-    """Every compaction kernel (persistent with 8 or 16 compute warps, one tile per CTA)
-    gives the oracle's result, for ragged sizes, all predicates and both count widths' paths."""
+    """Every compaction kernel (persistent with 8 or 16 compute warps, one tile
+    per CTA, persistent with packed 16-byte stores) gives the oracle's result,
+    for ragged sizes, all predicates and both count widths' paths."""
     import stream_compaction_gb300 as sc
     assert sc.sc_set_compact_variant(variant) == sc.SC_OK
     try:
@@ -221,5 +223,48 @@ def test_compact_kernel_variants(variant):
                     assert c == rc and np.array_equal(out.view(np.int32), ref.view(np.int32)), (n, dtype, pred)
                     if c < n:
                         assert np.all(full[c:n].view(np.int32) == -7)
+    finally:
+        sc.sc_set_compact_variant(0)
+
+
+def _kept_pattern(kind, n, rng):
+    """int32 inputs whose x > 0 pattern stresses the packed stores: every
+    element kept (a warp's run fills its whole slot ring), none, one in a
+    hundred, all but one in a hundred, alternating, and runs of random length."""
+    if kind == "all":
+        return np.arange(1, n + 1, dtype=np.int32)
+    if kind == "none":
+        return -np.arange(1, n + 1, dtype=np.int32)
+    if kind == "sparse":
+        return np.where(rng.random(n) < 0.01, 1, -1).astype(np.int32) * np.arange(1, n + 1, dtype=np.int32)
+    if kind == "dense":
+        return np.where(rng.random(n) < 0.99, 1, -1).astype(np.int32) * np.arange(1, n + 1, dtype=np.int32)
+    if kind == "alternate":
+        return np.where(np.arange(n) % 2 == 0, 1, -1).astype(np.int32) * np.arange(1, n + 1, dtype=np.int32)
+    runs = np.repeat(rng.integers(0, 2, n // 7 + 1) * 2 - 1, 7)[:n]   # runs of 7 kept / 7 dropped, at random
+    return (runs * np.arange(1, n + 1)).astype(np.int32)
+
+
+@pytest.mark.parametrize("variant", [0, 1, 3])
+@pytest.mark.parametrize("out_offset", [0, 1, 2, 3])
+@pytest.mark.parametrize("kind", ["all", "none", "sparse", "dense", "alternate", "runs"])
+def test_compact_persistent_output_alignment(variant, out_offset, kind):
+    """The persistent kernels on 16-byte aligned inputs, with the output 0-3
+    elements past a 16-byte boundary: each warp's run of kept elements starts
+    anywhere inside an aligned group, so the packed path's partial end groups
+    and its full 16-byte groups both occur.  Every kept element against the
+    oracle, and nothing written past the count."""
+    import stream_compaction_gb300 as sc
+    assert sc.sc_set_compact_variant(variant) == sc.SC_OK
+    try:
+        rng = np.random.default_rng(out_offset * 10 + len(kind))
+        for n in (8192, 8192 * 5 + 1, 8192 * 40 + 4097):
+            x = _kept_pattern(kind, n, rng)
+            out, c, full = gpu_compact(x, "gt", 0, offset=0, out_offset=out_offset)
+            assert sc.sc_debug_last_path() == sc.SC_PATH_COMPACT_PERSISTENT
+            ref, rc = oracle.compact(x, "gt", 0)
+            assert c == rc and np.array_equal(out, ref), (n, kind)
+            if c < n:
+                assert np.all(full[c:n].view(np.int32) == -7), (n, kind)
     finally:
         sc.sc_set_compact_variant(0)

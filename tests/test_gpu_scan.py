@@ -197,3 +197,63 @@ def test_float32_sum_infinities_cross_tiles():
         assert np.array_equal(np.isnan(y), np.isnan(ref)) and np.array_equal(np.isinf(y), np.isinf(ref))
         fin = np.isfinite(ref)
         assert np.allclose(y[fin], ref[fin], rtol=0, atol=1e-3)
+
+
+# ------------------------------------- persistent scan: in place, boundaries
+# Sizes just past the short-scan limit (2^21) and around the persistent
+# kernel's 8192-element tiles and 2-tile chunks, each with a ragged end.
+P_SIZES = [(1 << 21) + 1, (1 << 21) + 8192, (1 << 22) - 1, (1 << 22) + 16384 + 1, 3 * (1 << 21) + 77]
+P_KINDS = [("u32", "sum"), ("f32", "sum"), ("maxi32", "max"), ("affine", "affine"), ("i64", "sum"),
+           ("f64", "sum"), ("maxcount", "maxcount")]
+
+
+def _p_input(kind, op, n, seed):
+    if kind in ("i64", "f64", "maxcount"):
+        from test_gpu_ops import make_input
+        return make_input(kind, op, n, seed)
+    return _input(kind, n, seed)
+
+
+@pytest.mark.parametrize("kind,op", P_KINDS)
+@pytest.mark.parametrize("n", P_SIZES)
+def test_persistent_scan_in_place_at_boundaries(kind, op, n):
+    """16-byte aligned arrays above the short-scan limit take the persistent
+    kernel, whose pass 2 re-reads each tile from global memory while the TMA
+    stores of other tiles are in flight: in place and out of place, inclusive
+    and exclusive, every output against the oracle."""
+    import stream_compaction_gb300 as sc
+    from gpu_helpers import check_f64
+    x = _p_input(kind, op, n, seed=n % 1000 + len(kind))
+    for exclusive in (False, True):
+        ref = oracle.scan(x, op, exclusive)
+        for inplace in (False, True):
+            y = gpu_scan(x, op, exclusive, inplace=inplace)
+            assert sc.sc_debug_last_path() == sc.SC_PATH_SCAN_PERSISTENT, (kind, n)
+            what = "%s n=%d excl=%d inplace=%d" % (kind, n, exclusive, inplace)
+            if kind == "f32":
+                check_f32(y, ref, oracle.abs_prefix(x), what)
+            elif kind == "f64":
+                check_f64(y, ref, oracle.abs_prefix(x), what)
+            else:
+                assert np.array_equal(y, ref), what
+
+
+@pytest.mark.parametrize("kind,op,n", [("u32", "sum", (1 << 24) + 4097), ("affine", "affine", (1 << 23) + 5),
+                                       ("f32", "sum", (1 << 24) + 3)])
+def test_host_scan_in_place_across_chunks(kind, op, n):
+    """sc_scan_host with h_in == h_out: the staging chunks are 64 MiB (2^24
+    four-byte or 2^23 eight-byte elements), so these sizes carry the running
+    total across a chunk boundary into a ragged last chunk."""
+    import stream_compaction_gb300 as sc
+    from gpu_helpers import CODE, OPC, stream
+    x = _input(kind, n, seed=n % 977)
+    for exclusive in (False, True):
+        h = np.ascontiguousarray(x.copy())
+        code = CODE["affine" if kind == "affine" else kind]
+        st = sc.sc_scan_host(code, OPC[op], int(exclusive), h.ctypes.data, h.ctypes.data, n, stream())
+        assert st == sc.SC_OK, sc.status_string(st)
+        ref = oracle.scan(x, op, exclusive)
+        if kind == "f32":
+            check_f32(h, ref, oracle.abs_prefix(x), "host in place")
+        else:
+            assert np.array_equal(h, ref)

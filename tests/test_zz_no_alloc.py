@@ -67,12 +67,64 @@ def test_noalloc_matches_allocating_path_twice(kind, exclusive):
 
 
 def test_noalloc_full_capacity_and_limits():
+    """At the limit every status slot of the fixed array is in use: seeded
+    full-range uint32 input, every output against the oracle, on two calls in
+    a row (the second reuses the array the first left behind)."""
+    from stream_compaction_gb300 import synth
     n = sc.SC_NOALLOC_MAX_N
-    x = np.ones(n, dtype=np.uint32)
-    for _ in range(2):
-        got = _run(True, x, "sum", True)
-        assert got[0] == 0 and got[-1] == n - 1 and np.array_equal(got[:4096], np.arange(4096, dtype=np.uint32))
+    for call in range(2):
+        x = synth.full_u32_np(n, seed=20 + call)
+        got = _run(True, x, "sum", call == 0)
+        assert np.array_equal(got, oracle.scan(x, "sum", call == 0)), call
     # beyond the fixed scratch: refused before any launch
     assert sc.sc_scan_noalloc(sc.SC_U32, sc.SC_SUM, 1, 0x1000, 0x1000, n + 1, stream()) == sc.SC_ERR_WORKSPACE
     assert sc.sc_scan_noalloc(sc.SC_U32, sc.SC_SUM, 1, 0, 0, 0, stream()) == sc.SC_OK
     assert sc.sc_scan_noalloc(sc.SC_F32, sc.SC_MAX, 1, 0, 0, 0, stream()) == sc.SC_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kind", ["u32", "f32", "affine"])
+@pytest.mark.parametrize("exclusive", [False, True])
+def test_noalloc_unaligned_and_in_place(kind, exclusive):
+    """Element-aligned (not 16-byte aligned) buffers take the kernel's
+    partial-tile loads; in == out scans in place; both against the oracle."""
+    n = 5 * 4096 + 77
+    x, op = _inputs(kind, n, seed=31 + exclusive)
+    ref = oracle.scan(x, op, exclusive)
+    code = CODE["affine" if kind == "affine" else kind]
+    off = 2 if kind == "affine" else 1
+    for offset, inplace in ((off, False), (0, True), (off, True)):
+        _, xin = to_device(x, offset)
+        if inplace:
+            xout = xin
+        else:
+            _, xout = dev_buffer(xin.numel(), xin.dtype, offset + 2)
+        st = sc.sc_scan_noalloc(code, OPC[op], int(exclusive), xin.data_ptr(), xout.data_ptr(), n, stream())
+        assert st == sc.SC_OK, sc.status_string(st)
+        got = to_host(xout, x)
+        if kind == "f32":
+            assert np.all(np.abs(got.astype(np.float64) - ref) <= 1e-5 * oracle.abs_prefix(x)), (offset, inplace)
+        else:
+            assert np.array_equal(got, ref), (offset, inplace)
+    assert sc.sc_scan_noalloc_error(stream()) == sc.SC_OK
+
+
+def test_noalloc_timeout_is_reported():
+    """A tile that never publishes (test hook, 50 ms bound): its successors give
+    up, the array's error word records it, sc_scan_noalloc_error reports and
+    clears it, and the next call is exact again."""
+    n = 64 * 4096
+    x = np.ones(n, dtype=np.uint32)
+    _, xin = to_device(x)
+    _, xout = dev_buffer(n, xin.dtype)
+    assert sc.sc_scan_noalloc_error(stream()) == sc.SC_OK
+    assert sc.sc_debug_set_lookback(5, -1, 0, 50_000_000) == sc.SC_OK
+    try:
+        assert sc.sc_scan_noalloc(sc.SC_U32, sc.SC_SUM, 1, xin.data_ptr(), xout.data_ptr(), n, stream()) == sc.SC_OK
+        assert sc.sc_scan_noalloc_error(stream()) == sc.SC_ERR_LOOKBACK_TIMEOUT
+        assert sc.sc_scan_noalloc_error(stream()) == sc.SC_OK   # cleared by the first query
+    finally:
+        sc.sc_debug_set_lookback(-1, -1, 0, 0)
+    for _ in range(2):
+        assert sc.sc_scan_noalloc(sc.SC_U32, sc.SC_SUM, 1, xin.data_ptr(), xout.data_ptr(), n, stream()) == sc.SC_OK
+        assert np.array_equal(to_host(xout, x), np.arange(n, dtype=np.uint32))
+    assert sc.sc_scan_noalloc_error(stream()) == sc.SC_OK
