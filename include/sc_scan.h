@@ -315,12 +315,20 @@ uint64_t sc_launch_count(void);
  * variants 1, 6, 9, 10 and 11 select their shape, any other the default.
  * Returns SC_ERR_INVALID for an unknown variant. */
 sc_status sc_set_scan_variant(int variant);
+/* Distance between consecutive look-back status words (every single-pass
+ * kernel): 0 (default) the widest of 128, 64, 32 and 16 bytes that the
+ * workspace holds for the call's tiles or chunks; 16 / 32 / 64 / 128 that many
+ * bytes where the workspace holds it (else packed); -1 packed (8 bytes for
+ * 4-byte carries, 16 for 8-byte ones).  SC_ERR_INVALID otherwise. */
+sc_status sc_set_status_stride(int bytes);
 /* Select the fused-compaction kernel: 0 (default) the persistent TMA kernel
  * with 8 compute warps, each kept element stored on its own (4-byte stores);
  * 1 the same with 16 compute warps; 2 the one-tile-per-CTA kernel (inputs that
  * are not 16-byte aligned, or smaller than one 32 KiB tile, always use the
  * latter); 3 the persistent kernel with 8 compute warps that packs each warp's
- * kept elements in shared memory and writes them as aligned 16-byte stores.
+ * kept elements in shared memory and writes them as aligned 16-byte stores;
+ * 4 and 5 as 0 with 4 fresh-tile and 2 re-load stages, or 2 and 4, instead
+ * of 3 and 3.
  * SC_ERR_INVALID otherwise. */
 sc_status sc_set_compact_variant(int variant);
 /* Select how the radix pass ranks a warp step's keys by digit: 0 (default)

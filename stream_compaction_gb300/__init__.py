@@ -59,6 +59,7 @@ SIGNATURES = {
     "sc_launch_count": ([], _U64),
     "sc_set_scan_variant": ([_INT], _INT),
     "sc_set_compact_variant": ([_INT], _INT),
+    "sc_set_status_stride": ([_INT], _INT),
     "sc_set_radix_variant": ([_INT], _INT),
     "sc_scan_variant_info": ([_INT, ctypes.POINTER(_INT), ctypes.POINTER(_INT), ctypes.POINTER(_INT)], _INT),
     "sc_debug_set_lookback": ([_I64, _I64, _U32, _U64], _INT),
@@ -190,6 +191,10 @@ def sc_set_scan_variant(variant: int) -> int:
 
 def sc_set_compact_variant(variant: int) -> int:
     return load().sc_set_compact_variant(variant)
+
+
+def sc_set_status_stride(nbytes: int) -> int:
+    return load().sc_set_status_stride(nbytes)
 
 
 def sc_set_radix_variant(variant: int) -> int:

@@ -57,7 +57,7 @@ int tma_cfg_of(int v) {
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_variant{0};
 std::atomic<int> g_radix_variant{0};    // placement ranking of the radix pass (scg::launch_radix_place)
-std::atomic<int> g_compact_variant{0};  // 0, 1, 3: persistent kernel shapes; 2: one tile per CTA
+std::atomic<int> g_compact_variant{0};  // 0, 1, 3, 4, 5: persistent kernel shapes; 2: one tile per CTA
 std::atomic<long long> g_stall_tile{-1};
 std::atomic<long long> g_delay_tile{-1};
 std::atomic<unsigned> g_delay_ns{0};
@@ -140,7 +140,27 @@ LookbackCtl make_ctl(Workspace& ws, unsigned num_tiles) {
     lb.delay_ns = g_delay_ns.load();
     lb.timeout_ns = g_timeout_ns.load();
     lb.stats = reinterpret_cast<unsigned long long*>(ws.base + kStatsOffset);
+    lb.stride_words = 0;
     return lb;
+}
+
+// Status stride of a look-back over `units` tiles or chunks in a status area
+// of `area` bytes (the part of the workspace reserved for the statuses of the
+// call's n, lookback_bytes(n) - kStatusOffset: other data, such as the radix
+// pass's digit counts, may follow it): the widest of 128, 64, 32 and 16 bytes
+// that fits.  Packed
+// statuses share 128-byte L2 lines (16 four-byte carries to a line), which
+// many SMs poll while others write them; measured on GB300 (uint32 sum, 2^30,
+// persistent kernel) packed statuses held the scan at 0.83 of the copy peak
+// and statuses in lines of their own reach 0.98.  sc_set_status_stride
+// overrides the choice (g_status_stride).
+std::atomic<int> g_status_stride{0};
+unsigned status_stride_words(size_t area, int64_t units) {
+    const int forced = g_status_stride.load();
+    if (forced < 0) return 0;
+    for (size_t b = 128; b >= 16; b /= 2)
+        if ((forced == 0 || (size_t)forced == b) && (size_t)(units - 1) * b + 16 <= area) return (unsigned)(b / 8);
+    return 0;
 }
 
 // After a launch: every CTA of the grid takes exactly one tile id, so the
@@ -278,7 +298,7 @@ sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_le
     const bool vec_ok = aligned(in, 16) && aligned(out, 16);
     const int eb = scg::oid_elem_bytes(oid);
     const int cfg = tma_cfg_of(api_variant);
-    scg::TmaShape sh{0, 0, 0, 0};
+    scg::TmaShape sh{0, 0, 0, 0, 1, 2};
     if (cfg >= 0) scg::tma_shape(cfg, &sh);
     const int64_t tma_tile = cfg >= 0 ? sh.tile_bytes / eb : 0;
     const bool tma_stats = api_variant == kTmaStatsVariant;
@@ -312,6 +332,7 @@ sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_le
         n >= seg_tile && !carry_in && !carry_out && n / seg_tile * 256 < (int64_t)INT_MAX && num_sms() > 0) {
         const unsigned nchunks = (unsigned)ceil_div(n, seg_tile * scg::segscan_tma_chunk_tiles());
         p.lb = make_ctl(*ws, nchunks);
+        p.lb.stride_words = status_stride_words(lookback_bytes(n) - kStatusOffset, nchunks);
         const unsigned grid = (unsigned)std::min<int64_t>(num_sms(), nchunks);
         g_last_path = SC_PATH_SEGSCAN_PERSISTENT;
         const cudaError_t e = scg::launch_segscan_tma(oid, p, excl, grid, s);
@@ -319,10 +340,11 @@ sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_le
     }
     p.lb = make_ctl(*ws, ntiles);
     if (use_tma) {
-        const unsigned grid = (unsigned)std::min<int64_t>(num_sms(), ntiles);
+        p.lb.stride_words = status_stride_words(lookback_bytes(n) - kStatusOffset, ntiles);
+        const unsigned grid = (unsigned)std::min<int64_t>((int64_t)num_sms() * sh.ctas_per_sm, ntiles);
         g_last_path = SC_PATH_SCAN_PERSISTENT;
         const cudaError_t e = dispatch_scan_tma(oid, p, excl, grid, s, tma_stats, cfg);
-        return finish_launch(*ws, ntiles + grid * (unsigned)scg::tma_ids_per_cta(), e);
+        return finish_launch(*ws, ntiles + grid * (unsigned)sh.ids_per_cta, e);
     }
     g_last_path = SC_PATH_SCAN_ONE_TILE;
     // a grid no larger than the SM count is resident at once, so tiles may take
@@ -330,6 +352,7 @@ sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_le
     // waits on is already running
     const int sms = num_sms();
     p.lb.static_ids = sms > 0 && ntiles <= (unsigned)sms;
+    p.lb.stride_words = status_stride_words(lookback_bytes(n) - kStatusOffset, ntiles);
     return finish_launch(*ws, p.lb.static_ids ? 0u : ntiles,
                          dispatch_scan(oid, p, excl, segmented, legacy_variant, s));
 }
@@ -699,7 +722,8 @@ sc_status sc_compact_if(sc_dtype dtype, const void* in, void* out, int64_t* d_co
     const int cvar = g_compact_variant.load();
     const bool use_tma = p.vec_ok && n >= ptile && n / ptile * (ptile * 4 / 128) < (int64_t)INT_MAX && num_sms() > 0 &&
                          cvar != 2;
-    const int tma_shape_id = cvar == 3 ? 2 : cvar;  // public variant -> persistent kernel shape (3: packed stores)
+    // public variant -> persistent kernel shape (3: packed stores, 4: 4 + 2 stages, 5: 2 + 4 stages)
+    const int tma_shape_id = cvar == 3 ? 2 : cvar == 4 ? 3 : cvar == 5 ? 4 : cvar;
     const int64_t unit = use_tma ? ptile * scg::compact_tma_chunk_tiles() : scg::CompactConfig::TILE;
     const unsigned ntiles = (unsigned)ceil_div(n, unit);
     std::lock_guard<std::mutex> lk(g_ws_mu);
@@ -707,6 +731,7 @@ sc_status sc_compact_if(sc_dtype dtype, const void* in, void* out, int64_t* d_co
     sc_status st = acquire_ws(s, lookback_bytes(n), &ws);
     if (st != SC_OK) return st;
     p.lb = make_ctl(*ws, ntiles);
+    p.lb.stride_words = status_stride_words(lookback_bytes(n) - kStatusOffset, ntiles);
     cudaError_t e;
     if (use_tma) {
         const unsigned grid = (unsigned)std::min<int64_t>(num_sms(), ntiles);
@@ -946,8 +971,14 @@ sc_status sc_set_scan_variant(int variant) {
     return SC_OK;
 }
 
+sc_status sc_set_status_stride(int bytes) {
+    if (bytes != 0 && bytes != -1 && bytes != 16 && bytes != 32 && bytes != 64 && bytes != 128) return SC_ERR_INVALID;
+    g_status_stride.store(bytes);
+    return SC_OK;
+}
+
 sc_status sc_set_compact_variant(int variant) {
-    if (variant < 0 || variant > 3) return SC_ERR_INVALID;
+    if (variant < 0 || variant > 5) return SC_ERR_INVALID;
     g_compact_variant.store(variant);
     return SC_OK;
 }
@@ -962,7 +993,7 @@ sc_status sc_scan_variant_info(int variant, int* threads, int* items, int* loade
     if (variant < 0 || variant > max_variant()) return SC_ERR_INVALID;
     const int cfg = tma_cfg_of(variant);
     if (cfg >= 0) {  // persistent TMA kernel: compute threads, 4-byte items per compute thread
-        scg::TmaShape sh{0, 0, 0, 0};
+        scg::TmaShape sh{0, 0, 0, 0, 1, 2};
         scg::tma_shape(cfg, &sh);
         if (threads) *threads = sh.compute_threads;
         if (items) *items = sh.tile_bytes / 4 / sh.compute_threads;
@@ -990,6 +1021,7 @@ sc_status sc_debug_set_lookback(int64_t stall_tile, int64_t delay_tile, uint32_t
 
 // Tile sizes (host side).
 namespace scg {
+unsigned lookback_stride_words(size_t area, long long units) { return status_stride_words(area, units); }
 void lookback_hooks(LookbackCtl* lb) {
     lb->stall_tile = g_stall_tile.load();
     lb->delay_tile = g_delay_tile.load();

@@ -63,8 +63,9 @@ using namespace persist;
 
 constexpr int kTileBytes = 32768;       // 256 rows of 128 bytes
 constexpr int kRows = kTileBytes / 128;
-constexpr int kSA = 3;                  // pass-1 stages: fresh tiles from HBM
-constexpr int kSB = 3;                  // pass-2 stages: the same tiles again, from L2
+constexpr int kStages = 6;              // 32 KiB stages: kSA for fresh tiles from HBM, the rest for the
+                                        // pass-2 re-loads of the same tiles from L2 (a kernel parameter)
+constexpr int kMaxSB = 4;               // most re-load stages of any split
 constexpr int kChunk = 2;               // tiles per counter tick and per look-back status
 constexpr int kLag = 8;                 // pass 2 of tile k follows pass 1 of tile k + kLag
 constexpr int kLbWarps = 3;
@@ -76,7 +77,7 @@ constexpr int kLbPer = 8;
 constexpr unsigned kSentinel = 0xffffffffu;
 constexpr unsigned kVoid = 0xfffffffeu;
 constexpr int kCtrlBytes = 30720;
-constexpr int kSmemBytes = (kSA + kSB) * kTileBytes + 1024 + kCtrlBytes;
+constexpr int kSmemBytes = kStages * kTileBytes + 1024 + kCtrlBytes;
 constexpr int kMaxComputeWarps = 16;
 constexpr int kMaskRing = 12;           // tiles whose row information is kept (pass 1 -> pass 2)
 static_assert(kMaskRing > kLag, "row information outlives the lag");
@@ -100,14 +101,14 @@ struct CompactShape {
 };
 
 static_assert(kChunkSlots % kLbWarps == 0, "a look-back warp owns fixed chunk slots");
-static_assert(kR1 > kLag && kLag >= kSB, "pass-1-done ring covers the lag");
-static_assert(kRing >= kSA + kLag + kSB + 4, "tile ring outlives every reader");
+static_assert(kR1 > kLag && kLag >= kMaxSB, "pass-1-done ring covers the lag");
+static_assert(kRing >= kStages + kLag + 4, "tile ring outlives every reader");
 static_assert(kChunkSlots * kChunk >= kLag + 2 * kChunk, "chunk ring covers the lag");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct Ctrl {
-    unsigned long long a_full[kSA], a_empty[kSA];
-    unsigned long long b_full[kSB], b_empty[kSB];
+    unsigned long long a_full[kStages], a_empty[kStages];   // the first kSA used
+    unsigned long long b_full[kStages], b_empty[kStages];   // the first kSB used
     unsigned long long p1done[kR1], wready[kR1];
     unsigned long long agg[kChunkSlots], pre[kChunkSlots];
     // per row of a tile, from pass 1: the flag mask (one bit per element of the
@@ -137,10 +138,15 @@ __device__ __forceinline__ void sts32(uint32_t a, uint32_t v) {
 // kPack: pass 2 packs each warp's kept elements in its own part of the
 // re-load stage and writes them out as aligned 16-byte stores (a comparison
 // shape); otherwise every kept element is a 4-byte store of its own (the
-// default: fewer instructions, and L2 merges the partial sectors).
-template <class T, class CntOp, int CW, bool kPack>
+// default: fewer instructions, and L2 merges the partial sectors), and a warp
+// frees its re-load stage as soon as it has read its part into registers.
+// kSA_: fresh-tile stages; the other kStages - kSA_ hold the re-loads.
+template <class T, class CntOp, int CW, bool kPack, int kSA_>
 __global__ void __launch_bounds__(CompactShape<CW>::kThreads, 1)
     compact_tma_kernel(const __grid_constant__ CUtensorMap tm_in, const CompactParams p, const long long n_full_tiles) {
+    constexpr int kSA = kSA_, kSB = kStages - kSA_;
+    static_assert(kSA >= 2 && kSB >= 2 && kSB <= kMaxSB, "stage split");
+    static_assert(!kPack || kSB >= 3, "the packed stores keep their stage until the prefix arrives");
     using C = typename CntOp::C;
     using Sh = CompactShape<CW>;
     constexpr int kComputeWarps = Sh::kComputeWarps, kBookWarp = Sh::kBookWarp;
@@ -150,7 +156,7 @@ __global__ void __launch_bounds__(CompactShape<CW>::kThreads, 1)
     constexpr int kPerThread = kChunksPerThread * 4;  // pass-1 elements per thread
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + (kSA + kSB) * kTileBytes);
+    Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + kStages * kTileBytes);
     const uint32_t stageA = smem_u32(smem);
     const uint32_t stageB = stageA + kSA * kTileBytes;
     auto B = [](const unsigned long long& b) { return smem_u32(&b); };
@@ -453,6 +459,15 @@ __global__ void __launch_bounds__(CompactShape<CW>::kThreads, 1)
         if constexpr (kPack) p2_store_packed(j, v, r);
         else p2_store_direct(v, r, p2_out(j));
     };
+    // Direct stores: the warp's part of a full re-loaded tile is in registers
+    // after p2_load, so the stage is freed at once (producer B can re-load into
+    // it while this warp waits for the prefix and stores).
+    auto release_b = [&](int j) {
+        if constexpr (!kPack) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B(ctl->b_empty[j % kSB]));
+        }
+    };
 
     // general forms (first kLag tiles, the partial tile, void tiles, the drain)
     auto pass1 = [&](int k, int s, unsigned tu) {
@@ -475,6 +490,7 @@ __global__ void __launch_bounds__(CompactShape<CW>::kThreads, 1)
                 uint2 r[kSteps];
                 p2_load(j, v);
                 p2_rows(j, r);
+                release_b(j);
                 p2_store(j, v, r);
             } else {
                 const T* in = static_cast<const T*>(p.in) + t * TILE + (long long)warp * (kRowsPerWarp * 32);
@@ -487,7 +503,7 @@ __global__ void __launch_bounds__(CompactShape<CW>::kThreads, 1)
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(B(ctl->b_empty[j % kSB]));
+        if (lane == 0 && (kPack || tu == kVoid || (long long)tu >= n_full_tiles)) mbar_arrive(B(ctl->b_empty[j % kSB]));
     };
     const auto pre_bar = [&](int j) { return B(ctl->pre[(j / kChunk) % kChunkSlots]); };
     const auto pre_par = [&](int j) { return (uint32_t)(((j / kChunk) / kChunkSlots) & 1); };
@@ -517,6 +533,7 @@ __global__ void __launch_bounds__(CompactShape<CW>::kThreads, 1)
             uint2 r[kSteps];
             p2_load(j, v);
             p2_rows(j, r);
+            release_b(j);
             p1_publish(k, p1_flags(s));
             __syncwarp();
             if (lane == 0) {
@@ -526,7 +543,7 @@ __global__ void __launch_bounds__(CompactShape<CW>::kThreads, 1)
             if (!wait(pre_bar(j), pre_par(j))) { draining = false; break; }
             p2_store(j, v, r);
             __syncwarp();
-            if (lane == 0) mbar_arrive(B(ctl->b_empty[j % kSB]));
+            if (kPack && lane == 0) mbar_arrive(B(ctl->b_empty[j % kSB]));
         } else {
             pass1(k, s, tu);
             if (!wait(pre_bar(j), pre_par(j))) { draining = false; break; }
@@ -545,21 +562,22 @@ __global__ void __launch_bounds__(CompactShape<CW>::kThreads, 1)
 // ----------------------------------------------------------------- host side
 namespace {
 
-template <class T, class CntOp, int CW, bool kPack>
+template <class T, class CntOp, int CW, bool kPack, int SA>
 cudaError_t launch_ct(const CompactParams& p, unsigned grid, cudaStream_t s) {
     const long long nfull = p.n / TILE;
     CUtensorMap a;
     if (!make_map(&a, p.in, (unsigned long long)nfull * kRows, kRows)) return cudaErrorInvalidValue;
     static std::atomic<unsigned long long> done_mask{0};
-    const cudaError_t e = allow_smem(compact_tma_kernel<T, CntOp, CW, kPack>, kSmemBytes, done_mask);
+    const cudaError_t e = allow_smem(compact_tma_kernel<T, CntOp, CW, kPack, SA>, kSmemBytes, done_mask);
     if (e != cudaSuccess) return e;
-    compact_tma_kernel<T, CntOp, CW, kPack><<<grid, CompactShape<CW>::kThreads, kSmemBytes, s>>>(a, p, nfull);
+    compact_tma_kernel<T, CntOp, CW, kPack, SA><<<grid, CompactShape<CW>::kThreads, kSmemBytes, s>>>(a, p, nfull);
     return cudaGetLastError();
 }
 
-template <class T, int CW, bool kPack>
+template <class T, int CW, bool kPack, int SA>
 cudaError_t launch_ct_count(const CompactParams& p, bool wide_count, unsigned grid, cudaStream_t s) {
-    return wide_count ? launch_ct<T, OpCountU64, CW, kPack>(p, grid, s) : launch_ct<T, OpCountU32, CW, kPack>(p, grid, s);
+    return wide_count ? launch_ct<T, OpCountU64, CW, kPack, SA>(p, grid, s)
+                      : launch_ct<T, OpCountU32, CW, kPack, SA>(p, grid, s);
 }
 
 }  // namespace
@@ -572,12 +590,15 @@ int compact_tma_chunk_tiles() { return kChunk; }
 // compute warps, kept elements packed into aligned 16-byte stores (measured on
 // GB300 at 2^27 int32, x > 0: store sectors 33.8 M -> 9.0 M, but 76 M -> 104 M
 // instructions and 171 -> 189 us: the compute warps' instruction stream, not
-// the store path, bounds this kernel)
+// the store path, bounds this kernel); shapes 3 and 4: as shape 0 with 4
+// fresh-tile and 2 re-load stages, or 2 and 4
 template <class T>
 cudaError_t launch_compact_tma(const CompactParams& p, bool wide_count, unsigned grid, cudaStream_t s, int shape) {
-    if (shape == 0) return launch_ct_count<T, 8, false>(p, wide_count, grid, s);
-    if (shape == 1) return launch_ct_count<T, 16, false>(p, wide_count, grid, s);
-    if (shape == 2) return launch_ct_count<T, 8, true>(p, wide_count, grid, s);
+    if (shape == 0) return launch_ct_count<T, 8, false, 3>(p, wide_count, grid, s);
+    if (shape == 1) return launch_ct_count<T, 16, false, 3>(p, wide_count, grid, s);
+    if (shape == 2) return launch_ct_count<T, 8, true, 3>(p, wide_count, grid, s);
+    if (shape == 3) return launch_ct_count<T, 8, false, 4>(p, wide_count, grid, s);
+    if (shape == 4) return launch_ct_count<T, 8, false, 2>(p, wide_count, grid, s);
     return cudaErrorInvalidValue;
 }
 

@@ -356,31 +356,36 @@ __device__ __forceinline__ void st_relaxed_v2u64(unsigned long long* p, unsigned
 // An 8-byte carry travels in two words (one 16-byte store), each holding one
 // half of the payload and the same [epoch | flag] tag; a reader accepts the
 // pair only when both tags agree, so a half-updated pair reads as "not yet".
+// A tile's status sits at word tile * stride_words (0: packed, kWords apart).
 template <class C>
 struct StatusIO {
     static constexpr int kWords = sizeof(C) == 4 ? 1 : 2;
 
+    __device__ __forceinline__ static unsigned long long* slot(const LookbackCtl& lb, long long tile) {
+        return lb.status + tile * (lb.stride_words ? (long long)lb.stride_words : (long long)kWords);
+    }
+
     __device__ __forceinline__ static void publish(const LookbackCtl& lb, long long tile, unsigned flag, C v) {
         const unsigned long long tag = ((unsigned long long)lb.epoch << 2) | flag;
         if constexpr (kWords == 1) {
-            st_relaxed_u64(lb.status + tile, ((unsigned long long)to_bits32(v) << 32) | tag);
+            st_relaxed_u64(slot(lb, tile), ((unsigned long long)to_bits32(v) << 32) | tag);
         } else {
             const unsigned long long b = to_bits64(v);
-            st_relaxed_v2u64(lb.status + 2 * tile, (b << 32) | tag, (b & 0xffffffff00000000ull) | tag);
+            st_relaxed_v2u64(slot(lb, tile), (b << 32) | tag, (b & 0xffffffff00000000ull) | tag);
         }
     }
 
     // Returns the flag (ST_INVALID when the word belongs to another call).
     __device__ __forceinline__ static unsigned read(const LookbackCtl& lb, long long tile, C& v) {
         if constexpr (kWords == 1) {
-            const unsigned long long w = ld_relaxed_u64(lb.status + tile);
+            const unsigned long long w = ld_relaxed_u64(slot(lb, tile));
             const uint32_t tag = (uint32_t)w;
             if ((tag >> 2) != lb.epoch) return ST_INVALID;
             from_bits32((uint32_t)(w >> 32), v);
             return tag & 3u;
         } else {
             unsigned long long w0, w1;
-            ld_relaxed_v2u64(lb.status + 2 * tile, w0, w1);
+            ld_relaxed_v2u64(slot(lb, tile), w0, w1);
             const uint32_t t0 = (uint32_t)w0, t1 = (uint32_t)w1;
             if (t0 != t1 || (t0 >> 2) != lb.epoch) return ST_INVALID;
             from_bits64((w1 & 0xffffffff00000000ull) | (w0 >> 32), v);
@@ -543,6 +548,87 @@ __device__ bool lookback_prefix_adaptive(const LookbackCtl& lb, long long tile, 
         if (pm) break;
         end -= 32LL * per;
         per = min(per * 2, kMaxPer);
+    }
+    if (polls_out) *polls_out = polls;
+    prefix = acc;
+    return true;
+}
+
+// Look-back with one wide window whose polls re-read only what is missing.
+// The first window covers the 32 * kPer predecessors before `tile` in one
+// round trip (lane l reads kPer consecutive statuses); while any status after
+// the newest inclusive prefix (P) in the window is unpublished, only those
+// unpublished statuses are read again, so a poll costs a few loads instead of
+// the whole window.  A window without any P is folded whole and the next one
+// (the 32 * kPer statuses before it) is read the same way.  Same fold order,
+// poison and time-bound contract as lookback_prefix.
+template <class Op, int kPer>
+__device__ bool lookback_prefix_sticky(const LookbackCtl& lb, long long tile, typename Op::C& prefix,
+                                       unsigned* windows_out = nullptr, unsigned* polls_out = nullptr) {
+    using C = typename Op::C;
+    constexpr int W = 32 * kPer;
+    const int lane = threadIdx.x & 31;
+    C acc = Op::c_identity();
+    long long end = tile;
+    unsigned long long t_start = 0;
+    unsigned polls = 0;
+    while (true) {
+        const long long first = end - W + (long long)lane * kPer;
+        C val[kPer];
+        unsigned flag[kPer];
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            val[j] = Op::c_identity();
+            flag[j] = ST_PREFIX;  // tiles before 0 act as an identity prefix
+            if (first + j >= 0) flag[j] = StatusIO<C>::read(lb, first + j, val[j]);
+        }
+        int newest_p = -1, hp = -1;
+        while (true) {
+            newest_p = -1;
+#pragma unroll
+            for (int j = 0; j < kPer; ++j)
+                if (flag[j] == ST_PREFIX) newest_p = j;
+            const uint32_t pm = __ballot_sync(0xffffffffu, newest_p >= 0);
+            hp = pm ? 31 - __clz(pm) : -1;
+            bool poison = false, invalid = false;
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+                const bool after = lane > hp || (lane == hp && j > newest_p);
+                poison |= after && flag[j] == ST_POISON;
+                invalid |= after && flag[j] == ST_INVALID;
+            }
+            if (__any_sync(0xffffffffu, poison)) return false;
+            if (!__any_sync(0xffffffffu, invalid)) break;
+            if (t_start == 0) t_start = global_ns();
+            ++polls;
+            if (polls > (1u << 26) || global_ns() - t_start > lb.timeout_ns) {
+                if (lane == 0) raise_error(lb.error, DEV_LOOKBACK_TIMEOUT);
+                return false;
+            }
+            __nanosleep(32);
+            // re-read only the unpublished statuses after the newest P
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+                const bool after = lane > hp || (lane == hp && j > newest_p);
+                if (after && flag[j] == ST_INVALID) flag[j] = StatusIO<C>::read(lb, first + j, val[j]);
+            }
+        }
+        C x = Op::c_identity();
+        if (lane >= hp) {
+            const int j0 = lane == hp ? newest_p : 0;
+#pragma unroll
+            for (int j = 0; j < kPer; ++j)
+                if (j >= j0) x = Op::c_op(x, val[j]);
+        }
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const C y = shfl_down_v(x, d);
+            if (lane + d < 32) x = Op::c_op(x, y);
+        }
+        acc = Op::c_op(shfl_idx_v(x, 0), acc);
+        if (windows_out) ++*windows_out;
+        if (hp >= 0) break;
+        end -= W;
     }
     if (polls_out) *polls_out = polls;
     prefix = acc;

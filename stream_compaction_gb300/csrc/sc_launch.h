@@ -101,6 +101,8 @@ struct TmaShape {
     int chunk_tiles;
     int compute_threads;
     int threads;
+    int ctas_per_sm;  // the grid is at most this many CTAs per SM
+    int ids_per_cta;  // counter ticks per CTA beyond the chunks (see tma_ids_per_cta)
 };
 int tma_num_cfgs();
 int tma_ids_per_cta();
@@ -140,6 +142,9 @@ cudaError_t launch_radix_place(const uint32_t* in, uint32_t* out, long long n, i
 
 // The current look-back test hooks (sc_debug_set_lookback) copied into lb.
 void lookback_hooks(LookbackCtl* lb);
+// Status stride (LookbackCtl::stride_words) for `units` tiles or chunks whose
+// statuses live in `area` bytes.
+unsigned lookback_stride_words(size_t area, long long units);
 
 // Hierarchical (scan-then-propagate) comparison variant.
 constexpr int kHierNT = 256;

@@ -129,6 +129,7 @@ extern "C" sc_status sc_scan_noalloc(sc_dtype dtype, sc_op op, int exclusive, co
     p.lb.static_ids = 0;
     scg::lookback_hooks(&p.lb);  // the time bound, and the test hooks when set
     p.lb.stats = nullptr;
+    p.lb.stride_words = scg::lookback_stride_words(kScratchBytes - kHeader, p.lb.num_tiles);
     cudaError_t e;
     switch (oid) {
     case 0: e = scg::launch_scan<scg::OpSumU32>(p, exclusive != 0, false, 0, s); break;

@@ -24,6 +24,7 @@ struct LookbackCtl {
     unsigned int delay_ns;
     unsigned long long timeout_ns;  // bound on any single look-back wait
     unsigned long long* stats;      // instrumented variants only: 8 counters (see sc_scan.cuh)
+    unsigned int stride_words;      // 64-bit words from one tile's status to the next (0: packed)
 };
 
 struct ScanParams {

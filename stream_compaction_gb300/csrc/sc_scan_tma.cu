@@ -15,6 +15,11 @@ bool tma_shape(int cfg, TmaShape* sh) {
     case 2: cfg_info<Cfg2>(sh); return true;
     case 3: cfg_info<Cfg3>(sh); return true;
     case 4: cfg_info<Cfg4>(sh); return true;
+    case 5: cfg_info<Cfg5>(sh); return true;
+    case 6: cfg_info<Cfg6>(sh); return true;
+    case 7: cfg_info<Cfg7>(sh); return true;
+    case 8: cfg_info<Cfg8>(sh); return true;
+    case 9: cfg_info<Cfg9>(sh); return true;
     default: return false;
     }
 }
@@ -29,6 +34,11 @@ cudaError_t launch_scan_tma(const ScanParams& p, bool exclusive, unsigned grid, 
         case 2: return launch_cfg<Op, Cfg2>(p, exclusive, grid, s, false);
         case 3: return launch_cfg<Op, Cfg3>(p, exclusive, grid, s, false);
         case 4: return launch_cfg<Op, Cfg4>(p, exclusive, grid, s, false);
+        case 5: return launch_cfg<Op, Cfg5>(p, exclusive, grid, s, false);
+        case 6: return launch_cfg<Op, Cfg6>(p, exclusive, grid, s, false);
+        case 7: return launch_cfg<Op, Cfg7>(p, exclusive, grid, s, false);
+        case 8: return launch_cfg<Op, Cfg8>(p, exclusive, grid, s, false);
+        case 9: return launch_cfg<Op, Cfg9>(p, exclusive, grid, s, false);
         default: break;
         }
     }

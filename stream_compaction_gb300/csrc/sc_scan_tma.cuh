@@ -60,8 +60,30 @@ using namespace persist;
 
 // Shape of the persistent kernel: tile bytes, fresh / re-load ring depths,
 // compute warps, pass-1 to pass-2 lag (tiles) and tiles per chunk.
-template <int TileBytes, int SA, int SB, int CW, int Lag, int Chunk>
+// P1First: each compute iteration finishes pass 1 of its fresh tile (reads,
+// warp totals published, stage freed) before it waits for the pass-2 tile and
+// its prefix, so chunk aggregates never wait behind an older chunk's prefix
+// (otherwise both tiles' reads come first and the two scan chains interleave).
+// IdLate: producer A requests the next chunk id while it issues the last tile
+// of the current chunk (one tile ahead) instead of at the first (a whole chunk
+// ahead), so chunk ids follow the order in which chunks are worked on more
+// closely.
+// LbWarps: look-back warps; MinBlocks: CTAs resident per SM (each then gets
+// its share of the SM's shared memory and registers).
+// LbSticky > 0: the look-back reads one window of 32 * LbSticky chunks and
+// re-polls only the statuses still missing (lookback_prefix_sticky);
+// 0: windows of 32 chunks doubling to 256, re-read whole on every poll
+// (lookback_prefix_adaptive).
+template <int TileBytes, int SA, int SB, int CW, int Lag, int Chunk, bool P1First = false, int LbWarps = 3,
+          int MinBlocks = 1, bool IdLate = false, int LbSticky = 0>
 struct TmaCfg {
+    static constexpr bool kP1First = P1First;
+    static constexpr bool kIdLate = IdLate;
+    static constexpr int kLbSticky = LbSticky;
+    // chunk ids each CTA takes beyond the chunks it works on: the one that
+    // ends its loop, and (without IdLate) the one requested ahead of it
+    static constexpr int kIdsPerCta = IdLate ? 1 : 2;
+    static constexpr int kMinBlocks = MinBlocks;
     static constexpr int kTileBytes = TileBytes;  // rows of 128 bytes
     static constexpr int kSA = SA;                // pass-1 stages: fresh tiles from HBM
     static constexpr int kSB = SB;                // pass-2 stages: the same tiles again, from L2
@@ -71,7 +93,7 @@ struct TmaCfg {
     static constexpr int kChunkSlots = 6;         // chunk bookkeeping ring
     static constexpr int kRing = 64;              // per-tile bookkeeping ring
     static constexpr int kR1 = 32;                // pass-1-done barrier ring
-    static constexpr int kLbWarps = 3;
+    static constexpr int kLbWarps = LbWarps;
     static constexpr int kStoreWarps = SB % 2 == 0 ? 2 : 1;
     static constexpr int kBookWarp = kComputeWarps + kLbWarps;
     static constexpr int kProducerA = kBookWarp + 1;
@@ -82,7 +104,12 @@ struct TmaCfg {
     static constexpr int kRows = kTileBytes / 128;
     static constexpr int kBytesPerThread = kTileBytes / kCompute;
     static constexpr int kThreadsPerRow = 128 / kBytesPerThread;
-    static constexpr int kCtrlBytes = 16384;
+    // control block: 16 KiB, or what the stages leave of the CTA's share of
+    // shared memory (227 KiB for one CTA per SM; 228 KiB less 1 KiB reserved
+    // per CTA, shared, for more)
+    static constexpr int kSmemCap = MinBlocks == 1 ? 232448 : 233472 / MinBlocks - 1024;
+    static constexpr int kCtrlBytes =
+        (kSA + kSB) * kTileBytes + 1024 + 16384 <= kSmemCap ? 16384 : (kSmemCap - 1024 - (kSA + kSB) * kTileBytes) / 128 * 128;
     static constexpr int kSmemBytes = (kSA + kSB) * kTileBytes + 1024 + kCtrlBytes;
 
     // Parity waits on an mbarrier are exact only if the waiter is at most one
@@ -97,7 +124,7 @@ struct TmaCfg {
     static_assert(kChunkSlots * kChunk >= kLag + 2 * kChunk, "chunk ring covers the lag");
     static_assert(kBytesPerThread % 16 == 0 && kBytesPerThread <= 128, "16-byte chunks within one row");
     static_assert(kRows <= 256, "one TMA box per stage");
-    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+    static_assert(kSmemBytes <= kSmemCap, "shared memory per CTA");
 
     struct Ctrl {
         unsigned long long a_full[kSA], a_empty[kSA];
@@ -127,7 +154,14 @@ using Cfg1 = TmaCfg<16384, 6, 6, 16, 12, 4>;
 using Cfg2 = TmaCfg<32768, 3, 3, 16, 6, 2>;
 using Cfg3 = TmaCfg<16384, 6, 6, 8, 12, 4>;
 using Cfg4 = TmaCfg<32768, 3, 3, 8, 8, 2>;
-constexpr int kNumCfgs = 5;
+// few fresh-tile stages and a deep re-load ring
+// shorter lags, pass 1 first, other stage splits
+using Cfg5 = TmaCfg<32768, 3, 3, 8, 5, 2>;
+using Cfg6 = TmaCfg<32768, 3, 3, 8, 4, 2>;
+using Cfg7 = TmaCfg<32768, 3, 3, 8, 4, 2, true>;
+using Cfg8 = TmaCfg<32768, 2, 4, 8, 4, 2>;
+using Cfg9 = TmaCfg<24576, 2, 6, 12, 6, 2>;
+constexpr int kNumCfgs = 10;
 
 // For operators with costly combines, pass 1 keeps each compute thread's
 // total of a tile in shared memory for pass 2 (kLag + 2 tiles deep) where the
@@ -157,7 +191,7 @@ constexpr unsigned kVoid = 0xfffffffeu;      // past the last tile, inside the l
 // look-back warps waited for chunk aggregates, [7] ns the fresh-tile producer
 // waited for a free stage.
 template <class Op, bool kExcl, bool kStats, class Cfg>
-__global__ void __launch_bounds__(Cfg::kThreads, 1)
+__global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
     scan_tma_kernel(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtensorMap tm_out,
                     const ScanParams p, const long long n_full_tiles) {
     using T = typename Op::T;
@@ -240,9 +274,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             const int pos = k % kChunk;
             if (pos == 0) {
                 c = (long long)(a0 - base);
-                a0 = atomicAdd(ctr, 1ull);
+                if (!Cfg::kIdLate) a0 = atomicAdd(ctr, 1ull);
             }
             const bool done = c >= num_chunks;
+            if (Cfg::kIdLate && !done && pos == kChunk - 1) a0 = atomicAdd(ctr, 1ull);
             const long long t = c * kChunk + pos;
             ctl->tile[k % kRing] = done ? kSentinel : (t < num_tiles ? (unsigned)t : kVoid);
             if (done) vstore(&ctl->end_k, k);
@@ -374,7 +409,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 if (p.carry_in) prefix = *static_cast<const C*>(p.carry_in);
             } else {
                 unsigned wnd = 0, pl = 0;
-                ok = lookback_prefix_adaptive<Op, kLbPer>(p.lb, c, prefix, kStats ? &wnd : nullptr, kStats ? &pl : nullptr);
+                if constexpr (Cfg::kLbSticky > 0)
+                    ok = lookback_prefix_sticky<Op, Cfg::kLbSticky>(p.lb, c, prefix, kStats ? &wnd : nullptr,
+                                                                     kStats ? &pl : nullptr);
+                else
+                    ok = lookback_prefix_adaptive<Op, kLbPer>(p.lb, c, prefix, kStats ? &wnd : nullptr,
+                                                              kStats ? &pl : nullptr);
                 windows += wnd;
                 polls += pl;
                 if (!ok && lane == 0) StatusIO<C>::publish(p.lb, c, ST_POISON, Op::c_identity());
@@ -569,14 +609,18 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         if (tu1 == kSentinel) break;
         const int j = k - kLag;
         unsigned tu2 = kVoid;
+        T v1[IPT], v2[IPT];
+        if constexpr (Cfg::kP1First) {
+            if (tu1 != kVoid) fetch(stageA + s * kTileBytes, tu1, v1);
+            finish1(k, s, tu1, v1);
+        }
         if (j >= 0) {
             if (!wait2(j)) { draining = false; break; }
             tu2 = ctl->tile[j % kRing];
         }
-        T v1[IPT], v2[IPT];
-        if (tu1 != kVoid) fetch(stageA + s * kTileBytes, tu1, v1);
+        if (!Cfg::kP1First && tu1 != kVoid) fetch(stageA + s * kTileBytes, tu1, v1);
         if (j >= 0 && tu2 != kVoid) fetch(stageB + (j % kSB) * kTileBytes, tu2, v2);
-        finish1(k, s, tu1, v1);
+        if (!Cfg::kP1First) finish1(k, s, tu1, v1);
         if (j >= 0) finish2(j, tu2, v2);
     }
     if (draining)
@@ -629,6 +673,8 @@ void cfg_info(TmaShape* sh) {
     sh->chunk_tiles = Cfg::kChunk;
     sh->compute_threads = Cfg::kCompute;
     sh->threads = Cfg::kThreads;
+    sh->ctas_per_sm = Cfg::kMinBlocks;
+    sh->ids_per_cta = Cfg::kIdsPerCta;
 }
 
 }  // namespace

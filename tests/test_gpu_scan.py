@@ -95,7 +95,7 @@ def _num_variants():
     return v
 
 
-@pytest.mark.parametrize("variant", range(21))
+@pytest.mark.parametrize("variant", range(30))
 def test_uint32_variants(variant):
     import stream_compaction_gb300 as sc
     if variant >= _num_variants():
