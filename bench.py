@@ -77,9 +77,10 @@ def peaks():
         return 6800.0, "fallback"
 
 
-# The sources the headline kernel (the persistent TMA scan) is compiled from.
+# The sources the headline kernel (the persistent TMA scan) is compiled from,
+# and the host dispatch that picks its shape and look-back status layout.
 HEADLINE_SOURCES = ("sc_scan_tma.cu", "sc_scan_tma.cuh", "sc_scan.cuh", "sc_persist.cuh", "sc_tma.cuh", "sc_device.cuh",
-                    "sc_params.h")
+                    "sc_params.h", "sc_launch.h", "sc_api.cu")
 
 
 def kernel_sources_hash() -> str:

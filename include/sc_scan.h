@@ -328,7 +328,7 @@ sc_status sc_set_status_stride(int bytes);
  * latter); 3 the persistent kernel with 8 compute warps that packs each warp's
  * kept elements in shared memory and writes them as aligned 16-byte stores;
  * 4 and 5 as 0 with 4 fresh-tile and 2 re-load stages, or 2 and 4, instead
- * of 3 and 3.
+ * of 3 and 3; 6 and 7 as 0 with a pass-2 lag of 6 or 4 tiles instead of 8.
  * SC_ERR_INVALID otherwise. */
 sc_status sc_set_compact_variant(int variant);
 /* Select how the radix pass ranks a warp step's keys by digit: 0 (default)

@@ -57,7 +57,7 @@ int tma_cfg_of(int v) {
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_variant{0};
 std::atomic<int> g_radix_variant{0};    // placement ranking of the radix pass (scg::launch_radix_place)
-std::atomic<int> g_compact_variant{0};  // 0, 1, 3, 4, 5: persistent kernel shapes; 2: one tile per CTA
+std::atomic<int> g_compact_variant{0};  // 2: one tile per CTA; the others: persistent kernel shapes
 std::atomic<long long> g_stall_tile{-1};
 std::atomic<long long> g_delay_tile{-1};
 std::atomic<unsigned> g_delay_ns{0};
@@ -722,8 +722,9 @@ sc_status sc_compact_if(sc_dtype dtype, const void* in, void* out, int64_t* d_co
     const int cvar = g_compact_variant.load();
     const bool use_tma = p.vec_ok && n >= ptile && n / ptile * (ptile * 4 / 128) < (int64_t)INT_MAX && num_sms() > 0 &&
                          cvar != 2;
-    // public variant -> persistent kernel shape (3: packed stores, 4: 4 + 2 stages, 5: 2 + 4 stages)
-    const int tma_shape_id = cvar == 3 ? 2 : cvar == 4 ? 3 : cvar == 5 ? 4 : cvar;
+    // public variant -> persistent kernel shape (3: packed stores, 4: 4 + 2 stages, 5: 2 + 4 stages,
+    // 6 and 7: lag 6 and 4)
+    const int tma_shape_id = cvar >= 3 ? cvar - 1 : cvar;
     const int64_t unit = use_tma ? ptile * scg::compact_tma_chunk_tiles() : scg::CompactConfig::TILE;
     const unsigned ntiles = (unsigned)ceil_div(n, unit);
     std::lock_guard<std::mutex> lk(g_ws_mu);
@@ -978,7 +979,7 @@ sc_status sc_set_status_stride(int bytes) {
 }
 
 sc_status sc_set_compact_variant(int variant) {
-    if (variant < 0 || variant > 5) return SC_ERR_INVALID;
+    if (variant < 0 || variant > 7) return SC_ERR_INVALID;
     g_compact_variant.store(variant);
     return SC_OK;
 }

@@ -67,7 +67,7 @@ constexpr int kStages = 6;              // 32 KiB stages: kSA for fresh tiles fr
                                         // pass-2 re-loads of the same tiles from L2 (a kernel parameter)
 constexpr int kMaxSB = 4;               // most re-load stages of any split
 constexpr int kChunk = 2;               // tiles per counter tick and per look-back status
-constexpr int kLag = 8;                 // pass 2 of tile k follows pass 1 of tile k + kLag
+constexpr int kMaxLag = 8;              // pass 2 of tile k follows pass 1 of tile k + lag (a kernel parameter)
 constexpr int kLbWarps = 3;
 constexpr int kChunkSlots = 6;
 constexpr int kRing = 32;
@@ -80,7 +80,7 @@ constexpr int kCtrlBytes = 30720;
 constexpr int kSmemBytes = kStages * kTileBytes + 1024 + kCtrlBytes;
 constexpr int kMaxComputeWarps = 16;
 constexpr int kMaskRing = 12;           // tiles whose row information is kept (pass 1 -> pass 2)
-static_assert(kMaskRing > kLag, "row information outlives the lag");
+static_assert(kMaskRing > kMaxLag, "row information outlives the lag");
 
 // Compute-warp count of a compaction shape: each warp owns kRowsPerWarp rows
 // (128 bytes each) of a tile in both passes.
@@ -101,9 +101,9 @@ struct CompactShape {
 };
 
 static_assert(kChunkSlots % kLbWarps == 0, "a look-back warp owns fixed chunk slots");
-static_assert(kR1 > kLag && kLag >= kMaxSB, "pass-1-done ring covers the lag");
-static_assert(kRing >= kStages + kLag + 4, "tile ring outlives every reader");
-static_assert(kChunkSlots * kChunk >= kLag + 2 * kChunk, "chunk ring covers the lag");
+static_assert(kR1 > kMaxLag, "pass-1-done ring covers the lag");
+static_assert(kRing >= kStages + kMaxLag + 4, "tile ring outlives every reader");
+static_assert(kChunkSlots * kChunk >= kMaxLag + 2 * kChunk, "chunk ring covers the lag");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct Ctrl {
@@ -141,11 +141,13 @@ __device__ __forceinline__ void sts32(uint32_t a, uint32_t v) {
 // default: fewer instructions, and L2 merges the partial sectors), and a warp
 // frees its re-load stage as soon as it has read its part into registers.
 // kSA_: fresh-tile stages; the other kStages - kSA_ hold the re-loads.
-template <class T, class CntOp, int CW, bool kPack, int kSA_>
+// kLag_: pass 2 of tile k follows pass 1 of tile k + kLag_.
+template <class T, class CntOp, int CW, bool kPack, int kSA_, int kLag_>
 __global__ void __launch_bounds__(CompactShape<CW>::kThreads, 1)
     compact_tma_kernel(const __grid_constant__ CUtensorMap tm_in, const CompactParams p, const long long n_full_tiles) {
-    constexpr int kSA = kSA_, kSB = kStages - kSA_;
+    constexpr int kSA = kSA_, kSB = kStages - kSA_, kLag = kLag_;
     static_assert(kSA >= 2 && kSB >= 2 && kSB <= kMaxSB, "stage split");
+    static_assert(kLag <= kMaxLag && kLag >= kSB, "lag");
     static_assert(!kPack || kSB >= 3, "the packed stores keep their stage until the prefix arrives");
     using C = typename CntOp::C;
     using Sh = CompactShape<CW>;
@@ -562,22 +564,22 @@ __global__ void __launch_bounds__(CompactShape<CW>::kThreads, 1)
 // ----------------------------------------------------------------- host side
 namespace {
 
-template <class T, class CntOp, int CW, bool kPack, int SA>
+template <class T, class CntOp, int CW, bool kPack, int SA, int Lag>
 cudaError_t launch_ct(const CompactParams& p, unsigned grid, cudaStream_t s) {
     const long long nfull = p.n / TILE;
     CUtensorMap a;
     if (!make_map(&a, p.in, (unsigned long long)nfull * kRows, kRows)) return cudaErrorInvalidValue;
     static std::atomic<unsigned long long> done_mask{0};
-    const cudaError_t e = allow_smem(compact_tma_kernel<T, CntOp, CW, kPack, SA>, kSmemBytes, done_mask);
+    const cudaError_t e = allow_smem(compact_tma_kernel<T, CntOp, CW, kPack, SA, Lag>, kSmemBytes, done_mask);
     if (e != cudaSuccess) return e;
-    compact_tma_kernel<T, CntOp, CW, kPack, SA><<<grid, CompactShape<CW>::kThreads, kSmemBytes, s>>>(a, p, nfull);
+    compact_tma_kernel<T, CntOp, CW, kPack, SA, Lag><<<grid, CompactShape<CW>::kThreads, kSmemBytes, s>>>(a, p, nfull);
     return cudaGetLastError();
 }
 
-template <class T, int CW, bool kPack, int SA>
+template <class T, int CW, bool kPack, int SA, int Lag = kMaxLag>
 cudaError_t launch_ct_count(const CompactParams& p, bool wide_count, unsigned grid, cudaStream_t s) {
-    return wide_count ? launch_ct<T, OpCountU64, CW, kPack, SA>(p, grid, s)
-                      : launch_ct<T, OpCountU32, CW, kPack, SA>(p, grid, s);
+    return wide_count ? launch_ct<T, OpCountU64, CW, kPack, SA, Lag>(p, grid, s)
+                      : launch_ct<T, OpCountU32, CW, kPack, SA, Lag>(p, grid, s);
 }
 
 }  // namespace
@@ -591,7 +593,8 @@ int compact_tma_chunk_tiles() { return kChunk; }
 // GB300 at 2^27 int32, x > 0: store sectors 33.8 M -> 9.0 M, but 76 M -> 104 M
 // instructions and 171 -> 189 us: the compute warps' instruction stream, not
 // the store path, bounds this kernel); shapes 3 and 4: as shape 0 with 4
-// fresh-tile and 2 re-load stages, or 2 and 4
+// fresh-tile and 2 re-load stages, or 2 and 4; shapes 5 and 6: as shape 0
+// with a pass-2 lag of 6 or 4 tiles instead of 8
 template <class T>
 cudaError_t launch_compact_tma(const CompactParams& p, bool wide_count, unsigned grid, cudaStream_t s, int shape) {
     if (shape == 0) return launch_ct_count<T, 8, false, 3>(p, wide_count, grid, s);
@@ -599,6 +602,8 @@ cudaError_t launch_compact_tma(const CompactParams& p, bool wide_count, unsigned
     if (shape == 2) return launch_ct_count<T, 8, true, 3>(p, wide_count, grid, s);
     if (shape == 3) return launch_ct_count<T, 8, false, 4>(p, wide_count, grid, s);
     if (shape == 4) return launch_ct_count<T, 8, false, 2>(p, wide_count, grid, s);
+    if (shape == 5) return launch_ct_count<T, 8, false, 3, 6>(p, wide_count, grid, s);
+    if (shape == 6) return launch_ct_count<T, 8, false, 3, 4>(p, wide_count, grid, s);
     return cudaErrorInvalidValue;
 }
 

@@ -554,87 +554,6 @@ __device__ bool lookback_prefix_adaptive(const LookbackCtl& lb, long long tile, 
     return true;
 }
 
-// Look-back with one wide window whose polls re-read only what is missing.
-// The first window covers the 32 * kPer predecessors before `tile` in one
-// round trip (lane l reads kPer consecutive statuses); while any status after
-// the newest inclusive prefix (P) in the window is unpublished, only those
-// unpublished statuses are read again, so a poll costs a few loads instead of
-// the whole window.  A window without any P is folded whole and the next one
-// (the 32 * kPer statuses before it) is read the same way.  Same fold order,
-// poison and time-bound contract as lookback_prefix.
-template <class Op, int kPer>
-__device__ bool lookback_prefix_sticky(const LookbackCtl& lb, long long tile, typename Op::C& prefix,
-                                       unsigned* windows_out = nullptr, unsigned* polls_out = nullptr) {
-    using C = typename Op::C;
-    constexpr int W = 32 * kPer;
-    const int lane = threadIdx.x & 31;
-    C acc = Op::c_identity();
-    long long end = tile;
-    unsigned long long t_start = 0;
-    unsigned polls = 0;
-    while (true) {
-        const long long first = end - W + (long long)lane * kPer;
-        C val[kPer];
-        unsigned flag[kPer];
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            val[j] = Op::c_identity();
-            flag[j] = ST_PREFIX;  // tiles before 0 act as an identity prefix
-            if (first + j >= 0) flag[j] = StatusIO<C>::read(lb, first + j, val[j]);
-        }
-        int newest_p = -1, hp = -1;
-        while (true) {
-            newest_p = -1;
-#pragma unroll
-            for (int j = 0; j < kPer; ++j)
-                if (flag[j] == ST_PREFIX) newest_p = j;
-            const uint32_t pm = __ballot_sync(0xffffffffu, newest_p >= 0);
-            hp = pm ? 31 - __clz(pm) : -1;
-            bool poison = false, invalid = false;
-#pragma unroll
-            for (int j = 0; j < kPer; ++j) {
-                const bool after = lane > hp || (lane == hp && j > newest_p);
-                poison |= after && flag[j] == ST_POISON;
-                invalid |= after && flag[j] == ST_INVALID;
-            }
-            if (__any_sync(0xffffffffu, poison)) return false;
-            if (!__any_sync(0xffffffffu, invalid)) break;
-            if (t_start == 0) t_start = global_ns();
-            ++polls;
-            if (polls > (1u << 26) || global_ns() - t_start > lb.timeout_ns) {
-                if (lane == 0) raise_error(lb.error, DEV_LOOKBACK_TIMEOUT);
-                return false;
-            }
-            __nanosleep(32);
-            // re-read only the unpublished statuses after the newest P
-#pragma unroll
-            for (int j = 0; j < kPer; ++j) {
-                const bool after = lane > hp || (lane == hp && j > newest_p);
-                if (after && flag[j] == ST_INVALID) flag[j] = StatusIO<C>::read(lb, first + j, val[j]);
-            }
-        }
-        C x = Op::c_identity();
-        if (lane >= hp) {
-            const int j0 = lane == hp ? newest_p : 0;
-#pragma unroll
-            for (int j = 0; j < kPer; ++j)
-                if (j >= j0) x = Op::c_op(x, val[j]);
-        }
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const C y = shfl_down_v(x, d);
-            if (lane + d < 32) x = Op::c_op(x, y);
-        }
-        acc = Op::c_op(shfl_idx_v(x, 0), acc);
-        if (windows_out) ++*windows_out;
-        if (hp >= 0) break;
-        end -= W;
-    }
-    if (polls_out) *polls_out = polls;
-    prefix = acc;
-    return true;
-}
-
 // --------------------------------------------------------------- tile I/O
 // 16-byte vectors <-> items.
 template <class T>

@@ -64,25 +64,15 @@ using namespace persist;
 // warp totals published, stage freed) before it waits for the pass-2 tile and
 // its prefix, so chunk aggregates never wait behind an older chunk's prefix
 // (otherwise both tiles' reads come first and the two scan chains interleave).
-// IdLate: producer A requests the next chunk id while it issues the last tile
-// of the current chunk (one tile ahead) instead of at the first (a whole chunk
-// ahead), so chunk ids follow the order in which chunks are worked on more
-// closely.
 // LbWarps: look-back warps; MinBlocks: CTAs resident per SM (each then gets
 // its share of the SM's shared memory and registers).
-// LbSticky > 0: the look-back reads one window of 32 * LbSticky chunks and
-// re-polls only the statuses still missing (lookback_prefix_sticky);
-// 0: windows of 32 chunks doubling to 256, re-read whole on every poll
-// (lookback_prefix_adaptive).
 template <int TileBytes, int SA, int SB, int CW, int Lag, int Chunk, bool P1First = false, int LbWarps = 3,
-          int MinBlocks = 1, bool IdLate = false, int LbSticky = 0>
+          int MinBlocks = 1>
 struct TmaCfg {
     static constexpr bool kP1First = P1First;
-    static constexpr bool kIdLate = IdLate;
-    static constexpr int kLbSticky = LbSticky;
     // chunk ids each CTA takes beyond the chunks it works on: the one that
-    // ends its loop, and (without IdLate) the one requested ahead of it
-    static constexpr int kIdsPerCta = IdLate ? 1 : 2;
+    // ends its loop and the one requested ahead of it
+    static constexpr int kIdsPerCta = 2;
     static constexpr int kMinBlocks = MinBlocks;
     static constexpr int kTileBytes = TileBytes;  // rows of 128 bytes
     static constexpr int kSA = SA;                // pass-1 stages: fresh tiles from HBM
@@ -90,7 +80,10 @@ struct TmaCfg {
     static constexpr int kChunk = Chunk;          // tiles per counter tick and per look-back status
     static constexpr int kLag = Lag;              // pass 2 of tile k follows pass 1 of tile k + kLag
     static constexpr int kComputeWarps = CW;
-    static constexpr int kChunkSlots = 6;         // chunk bookkeeping ring
+    // chunk bookkeeping ring: covers the lag, a multiple of the look-back warps
+    static constexpr int kChunkSlots =
+        ((((Lag + 2 * Chunk + Chunk - 1) / Chunk > 6 ? (Lag + 2 * Chunk + Chunk - 1) / Chunk : 6) + LbWarps - 1) /
+         LbWarps) * LbWarps;
     static constexpr int kRing = 64;              // per-tile bookkeeping ring
     static constexpr int kR1 = 32;                // pass-1-done barrier ring
     static constexpr int kLbWarps = LbWarps;
@@ -146,21 +139,22 @@ struct TmaCfg {
 };
 
 // The shapes compiled in.  0 is the default of every operator (32 KiB tiles,
-// 3 + 3 stages, 8 compute warps, pass-2 lag of 6 tiles, 2-tile chunks: the
-// fastest of the shapes measured on GB300 for 2^30 uint32); the others are
-// uint32-sum variants kept for on-GPU comparison.
-using Cfg0 = TmaCfg<32768, 3, 3, 8, 6, 2>;
+// 3 + 3 stages, 8 compute warps, pass-2 lag of 5 tiles, 2-tile chunks, pass 1
+// first: the fastest of the shapes measured on GB300 for uint32 sums of
+// 2^28-2^30 elements, with look-back statuses in lines of their own); the
+// others are uint32-sum variants kept for on-GPU comparison.
+using Cfg0 = TmaCfg<32768, 3, 3, 8, 5, 2, true>;
 using Cfg1 = TmaCfg<16384, 6, 6, 16, 12, 4>;
 using Cfg2 = TmaCfg<32768, 3, 3, 16, 6, 2>;
 using Cfg3 = TmaCfg<16384, 6, 6, 8, 12, 4>;
 using Cfg4 = TmaCfg<32768, 3, 3, 8, 8, 2>;
-// few fresh-tile stages and a deep re-load ring
-// shorter lags, pass 1 first, other stage splits
-using Cfg5 = TmaCfg<32768, 3, 3, 8, 5, 2>;
-using Cfg6 = TmaCfg<32768, 3, 3, 8, 4, 2>;
-using Cfg7 = TmaCfg<32768, 3, 3, 8, 4, 2, true>;
-using Cfg8 = TmaCfg<32768, 2, 4, 8, 4, 2>;
-using Cfg9 = TmaCfg<24576, 2, 6, 12, 6, 2>;
+// the former default (lag 6, both tiles' reads first), pass 1 first at lag 6,
+// 16 compute warps, 1-tile chunks
+using Cfg5 = TmaCfg<32768, 3, 3, 8, 6, 2>;
+using Cfg6 = TmaCfg<32768, 3, 3, 8, 6, 2, true>;
+using Cfg7 = TmaCfg<32768, 3, 3, 16, 6, 2, true>;
+using Cfg8 = TmaCfg<32768, 3, 3, 8, 6, 1>;
+using Cfg9 = TmaCfg<32768, 3, 3, 16, 5, 2, true>;
 constexpr int kNumCfgs = 10;
 
 // For operators with costly combines, pass 1 keeps each compute thread's
@@ -274,10 +268,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
             const int pos = k % kChunk;
             if (pos == 0) {
                 c = (long long)(a0 - base);
-                if (!Cfg::kIdLate) a0 = atomicAdd(ctr, 1ull);
+                a0 = atomicAdd(ctr, 1ull);
             }
             const bool done = c >= num_chunks;
-            if (Cfg::kIdLate && !done && pos == kChunk - 1) a0 = atomicAdd(ctr, 1ull);
             const long long t = c * kChunk + pos;
             ctl->tile[k % kRing] = done ? kSentinel : (t < num_tiles ? (unsigned)t : kVoid);
             if (done) vstore(&ctl->end_k, k);
@@ -409,12 +402,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
                 if (p.carry_in) prefix = *static_cast<const C*>(p.carry_in);
             } else {
                 unsigned wnd = 0, pl = 0;
-                if constexpr (Cfg::kLbSticky > 0)
-                    ok = lookback_prefix_sticky<Op, Cfg::kLbSticky>(p.lb, c, prefix, kStats ? &wnd : nullptr,
-                                                                     kStats ? &pl : nullptr);
-                else
-                    ok = lookback_prefix_adaptive<Op, kLbPer>(p.lb, c, prefix, kStats ? &wnd : nullptr,
-                                                              kStats ? &pl : nullptr);
+                ok = lookback_prefix_adaptive<Op, kLbPer>(p.lb, c, prefix, kStats ? &wnd : nullptr,
+                                                          kStats ? &pl : nullptr);
                 windows += wnd;
                 polls += pl;
                 if (!ok && lane == 0) StatusIO<C>::publish(p.lb, c, ST_POISON, Op::c_identity());

@@ -197,11 +197,11 @@ def test_scan_host_other_ops(kind, op):
         assert np.array_equal(y, ref)
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5, 6, 7])
 def test_compact_kernel_variants(variant):
     """Every compaction kernel (persistent with 8 or 16 compute warps, one tile
     per CTA, persistent with packed 16-byte stores, persistent with 4 + 2 or
-    2 + 4 stages) gives the oracle's result,
+    2 + 4 stages, persistent with a lag of 6 or 4 tiles) gives the oracle's result,
     for ragged sizes, all predicates and both count widths' paths."""
     import stream_compaction_gb300 as sc
     assert sc.sc_set_compact_variant(variant) == sc.SC_OK
@@ -246,7 +246,7 @@ def _kept_pattern(kind, n, rng):
     return (runs * np.arange(1, n + 1)).astype(np.int32)
 
 
-@pytest.mark.parametrize("variant", [0, 1, 3, 4, 5])
+@pytest.mark.parametrize("variant", [0, 1, 3, 4, 5, 6, 7])
 @pytest.mark.parametrize("out_offset", [0, 1, 2, 3])
 @pytest.mark.parametrize("kind", ["all", "none", "sparse", "dense", "alternate", "runs"])
 def test_compact_persistent_output_alignment(variant, out_offset, kind):
