@@ -153,9 +153,13 @@ sc_status sc_scan_exclusive(sc_dtype dtype, sc_op op, const void *in, void *out,
 
 /* Independent scans of the rows of a row-major rows x cols matrix (leading
  * dimension cols, contiguous): row r of out is the scan of row r of in, each
- * starting again from the identity.  One kernel launch: tiles that start a
- * row take no carry, longer rows chain their tiles through the look-back.
- * Same dtypes, ops and aliasing rules as sc_scan_inclusive. */
+ * starting again from the identity.  One kernel launch: a scan segmented at
+ * the multiples of cols (the heads computed from the element index, no flag
+ * array), on the persistent kernel for operators with 4-byte elements and
+ * 16-byte aligned arrays of at least 8192 elements, else on the
+ * one-tile-per-CTA kernel; a chunk or tile that holds a row start publishes
+ * its complete prefix at once, so look-backs stop there.  Same dtypes, ops
+ * and aliasing rules as sc_scan_inclusive. */
 sc_status sc_scan_batched(sc_dtype dtype, sc_op op, int exclusive, const void *in, void *out,
                           int64_t rows, int64_t cols, sc_stream_t stream);
 
@@ -307,12 +311,13 @@ uint64_t sc_launch_count(void);
 
 /* Select the kernel of the uint32/int32 sum.  0 (default): the persistent
  * TMA-pipelined kernel wherever it applies (16-byte aligned arrays of more
- * than 2^21 elements), else the one-tile-per-CTA kernel (for n <= 2^21 its
- * shape of 16384-element tiles with 128-tile look-back windows, variant 10);
- * v >= 1: one of the precompiled shapes (see sc_scan_variant_info), kept for
- * on-GPU comparison; for int32/uint32 sums segmented by head flags (default:
- * the shape of variant 9) and batched rows (default: the shape of variant 1)
- * variants 1, 6, 9, 10 and 11 select their shape, any other the default.
+ * than 2^22 elements; scans segmented by head flags and batched rows whose
+ * length does not divide 4096 on its segmented form), else the
+ * one-tile-per-CTA kernel (for n <= 2^22 its shape of 8192-element tiles of
+ * 512 threads, variant 4); v >= 1: one of the precompiled shapes (see
+ * sc_scan_variant_info), kept for on-GPU comparison (always on the kernel the
+ * shape belongs to); for one-tile segmented scans and batched rows variants
+ * 1, 6, 9, 10 and 11 select their shape, any other the default.
  * Returns SC_ERR_INVALID for an unknown variant. */
 sc_status sc_set_scan_variant(int variant);
 /* Distance between consecutive look-back status words (every single-pass

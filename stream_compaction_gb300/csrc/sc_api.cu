@@ -37,11 +37,15 @@ constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 constexpr int kTmaStatsVariant = scg::kNumSumU32Variants + 1;
 // Up to this many elements the default path is the one-tile-per-CTA kernel:
 // measured on GB300, the persistent kernel's pipeline start-up (about 9 us)
-// costs more than a short scan, and the one-tile kernel with 128-tile look-back
-// windows (uint32-sum shape kSmallShape) finishes n = 2^20 in about 2/3 of the
-// persistent kernel's time; the two are level near 2^22.
-constexpr int64_t kSmallScanMax = int64_t(1) << 21;
-constexpr int kSmallShape = 9;  // 16384-element tiles, 512 threads, 128-tile windows
+// costs more than a short scan.  For short uint32 sums the one-tile shape
+// kSmallShape: with look-back statuses in L2 lines of their own, 8192-element
+// tiles of 512 threads finish n = 2^20 + 17 in 10.5 us with the L2 flushed
+// (7.0 us back to back), against 12.4 (8.2) for 16384-element tiles and 11.5
+// (7.4) for 4096-element ones; up to 2^22 + 17 elements that shape also beats
+// the persistent kernel (16.3 against 18.6 us), at 2^23 the persistent kernel
+// wins (24.8 against 25.7 us).
+constexpr int64_t kSmallScanMax = int64_t(1) << 22;
+constexpr int kSmallShape = 3;  // 8192-element tiles, 512 threads x 16 items
 // Scans segmented by head flags (int32/uint32 sums): 4096-element tiles, 128-tile
 // look-back windows, 8 CTAs per SM; measured on GB300 with 2^27 elements and a
 // head every 1024 on average: 351 us against 377 us for shape 0.
@@ -325,11 +329,19 @@ sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_le
     p.vec_ok = vec_ok;
     p.carry_in = carry_in;
     p.carry_out = carry_out;
-    // scans segmented by head flags: the persistent kernel when the operator
-    // has that form and the arrays are 16-byte aligned and hold a full tile
+    // scans segmented by head flags, and batched rows (heads at the multiples
+    // of the row length): the persistent kernel when the operator has that
+    // form and the arrays are 16-byte aligned and hold a full tile
+    // Batched rows whose length divides the one-tile kernel's tile stay there
+    // (every tile starts a row: no look-back at all; measured on GB300 with
+    // 2^28 int32, rows of 16-4096: 0.77-0.80 of the copy peak against 0.70 on
+    // the persistent kernel); other row lengths (33, 1000, 2047: 0.56 there)
+    // take the persistent kernel (0.69-0.70).
     const int64_t seg_tile = scg::segscan_tma_tile_elems();
-    if (heads && api_variant == 0 && scg::segscan_tma_supported(oid) && vec_ok && aligned(heads, 16) &&
-        n >= seg_tile && !carry_in && !carry_out && n / seg_tile * 256 < (int64_t)INT_MAX && num_sms() > 0) {
+    const bool rows_fit_tiles = seg_len > 0 && scg::scan_tile_elems(oid, legacy_variant) % seg_len == 0;
+    if (segmented && !rows_fit_tiles && api_variant == 0 && scg::segscan_tma_supported(oid) && vec_ok &&
+        (!heads || aligned(heads, 16)) && n >= seg_tile && !carry_in && !carry_out &&
+        n / seg_tile * 256 < (int64_t)INT_MAX && num_sms() > 0) {
         const unsigned nchunks = (unsigned)ceil_div(n, seg_tile * scg::segscan_tma_chunk_tiles());
         p.lb = make_ctl(*ws, nchunks);
         p.lb.stride_words = status_stride_words(lookback_bytes(n) - kStatusOffset, nchunks);

@@ -1,5 +1,5 @@
 // Persistent, warp-specialised single-pass scan (the default path for
-// 16-byte-aligned arrays of more than 2^21 elements).  The kernel and its
+// 16-byte-aligned arrays of more than 2^22 elements).  The kernel and its
 // launch helpers; sc_scan_tma.cu instantiates it for the first operators,
 // sc_ops_*.cu for the others.
 //
@@ -126,6 +126,7 @@ struct TmaCfg {
         unsigned long long wready[kR1];                   // all compute warps wrote their pass-1 totals
         unsigned long long agg[kChunkSlots], pre[kChunkSlots];
         unsigned tile[kRing];
+        unsigned seg_r[kRing];                            // batched rows: the tile's first index mod the row length
         unsigned long long offset[kRing];                 // carry-typed: fold of the chunk's earlier tiles
         unsigned long long wtot[kRing][kComputeWarps];    // element-typed warp totals from pass 1
         unsigned long long chunk_agg[kChunkSlots], chunk_prefix[kChunkSlots];

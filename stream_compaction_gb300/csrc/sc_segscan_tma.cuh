@@ -1,6 +1,8 @@
 // Persistent, warp-specialised scan segmented by head flags (one byte per
-// element, nonzero = a segment starts there): the same pipeline as the
-// persistent scan (sc_scan_tma.cuh) with the flags carried along.
+// element, nonzero = a segment starts there), or by rows of a fixed length
+// (batched rows: the heads are the multiples of the row length, computed from
+// the element index): the same pipeline as the persistent scan
+// (sc_scan_tma.cuh) with the heads carried along.
 //
 // "Lecture 7: Parallel pattern -- prefix sum / scan" (UIUC ECE408 notes),
 // section 2, names the segmented scan (the running value restarts at every
@@ -115,11 +117,15 @@ __device__ __forceinline__ uint32_t head_bits16(const uint4& q) {
     return m;
 }
 
-using SegCfg = TmaCfg<32768, 3, 2, 8, 6, 2>;  // 3 fresh-tile stages + flags, 2 re-load stages
+// pass-2 lag 5 with pass 1 first, as the plain persistent scan
+using SegCfg = TmaCfg<32768, 3, 2, 8, 5, 2, true>;      // 3 fresh-tile stages + flags, 2 re-load stages
+using SegRowsCfg = TmaCfg<32768, 3, 3, 8, 5, 2, true>;  // heads at multiples of a row length: no flags to hold
 
 }  // namespace
 
-template <class Op, bool kExcl, class Cfg>
+// kPeriodic: the heads are the multiples of p.seg_len (batched rows), computed
+// from the element index; otherwise p.heads holds one flag byte per element.
+template <class Op, bool kExcl, class Cfg, bool kPeriodic>
 __global__ void __launch_bounds__(Cfg::kThreads, 1)
     segscan_tma_kernel(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtensorMap tm_out,
                        const ScanParams p, const long long n_full_tiles) {
@@ -152,6 +158,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long num_tiles = p.n / TILE + (p.n % TILE != 0);
     const long long num_chunks = p.lb.num_tiles;
+    // batched rows no longer than 2^31 elements: head positions in 32-bit arithmetic
+    const bool short_rows = kPeriodic && p.seg_len <= 0x7fffffffLL;
     const unsigned long long wait_limit = p.lb.timeout_ns + 500000000ull;
     const volatile int* end_k = &ctl->end_k;
 
@@ -202,12 +210,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             const bool done = c >= num_chunks;
             const long long t = c * kChunk + pos;
             ctl->tile[k % kRing] = done ? kSentinel : (t < num_tiles ? (unsigned)t : kVoid);
+            // batched rows: the row position of the tile's first element, once per tile
+            if (kPeriodic && short_rows && !done && t < num_tiles) ctl->seg_r[k % kRing] = (unsigned)((t * TILE) % p.seg_len);
             if (done) vstore(&ctl->end_k, k);
             issued = k;
             if (!done && t < n_full_tiles) {
-                mbar_arrive_expect_tx(B(ctl->a_full[s]), kTileBytes + TILE);
+                mbar_arrive_expect_tx(B(ctl->a_full[s]), kTileBytes + (kPeriodic ? 0 : TILE));
                 tma_load_2d_hint(stageA + s * kTileBytes, &tm_in, 0, (int)(t * kRows), B(ctl->a_full[s]), keep);
-                bulk_load_1d_hint(headsA + s * TILE, p.heads + t * TILE, TILE, B(ctl->a_full[s]), drop);
+                if (!kPeriodic) bulk_load_1d_hint(headsA + s * TILE, p.heads + t * TILE, TILE, B(ctl->a_full[s]), drop);
             } else {
                 mbar_arrive(B(ctl->a_full[s]));  // sentinel, void slot, or the ragged last tile
             }
@@ -351,8 +361,25 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             load_partial_tile<T, IPT>(static_cast<const T*>(p.in) + t * TILE, v, p.n - t * TILE, Op::identity());
         }
     };
-    // the head bits of this thread's items of tile t (fresh tile in stage s)
-    auto heads_of = [&](int s, long long t) -> uint32_t {
+    // batched rows: the thread's offset inside a tile, mod the row length
+    const uint32_t row_len = short_rows ? (uint32_t)p.seg_len : 0u;
+    const uint32_t rc = short_rows ? (uint32_t)(ctid * IPT) % row_len : 0u;
+    // head bits of the thread's items of tile t in ring slot `slot` (batched rows)
+    auto heads_periodic = [&](int slot, long long t) -> uint32_t {
+        if constexpr (kPeriodic) {
+            if (!short_rows) return head_bits<IPT>(t * TILE + (long long)ctid * IPT, p.seg_len);
+            uint32_t r = ctl->seg_r[slot % kRing] + rc;  // < 2 * row_len <= 2^32 - 2
+            if (r >= row_len) r -= row_len;
+            uint32_t hm = 0;
+            for (uint32_t k = r == 0 ? 0u : row_len - r; k < (uint32_t)IPT; k += row_len) hm |= 1u << k;
+            return hm;
+        } else {
+            return 0u;
+        }
+    };
+    // the head bits of this thread's items of tile t (fresh tile in stage s, ring slot k)
+    auto heads_of = [&](int s, int k, long long t) -> uint32_t {
+        if constexpr (kPeriodic) return heads_periodic(k, t);
         if (t < n_full_tiles) {
             const uint32_t hb = headsA + s * TILE + ctid * IPT;
             return head_bits16(lds128(hb)) | (head_bits16(lds128(hb + 16)) << 16);
@@ -375,8 +402,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     auto finish1 = [&](int k, int s, unsigned tu, const T (&v)[IPT]) {
         E tot = PO::e_identity();
         if (tu != kVoid) {
-            const uint32_t hm = heads_of(s, (long long)tu);
-            hmask[(k % kMaskSlots) * kCompute + ctid] = hm;
+            const uint32_t hm = heads_of(s, k, (long long)tu);
+            if (!kPeriodic) hmask[(k % kMaskSlots) * kCompute + ctid] = hm;
             tot = thread_total(v, hm);
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {  // ordered: lane 0 ends with lanes 0..31
@@ -397,7 +424,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         const int q = j / kChunk;
         if (tu != kVoid) {
             const long long t = tu;
-            const uint32_t hm = hmask[(j % kMaskSlots) * kCompute + ctid];
+            const uint32_t hm = kPeriodic ? heads_periodic(j, t) : hmask[(j % kMaskSlots) * kCompute + ctid];
             E wv = lane < kComputeWarps ? unpack_bits<E>(ctl->wtot[j % kRing][lane]) : PO::e_identity();
 #pragma unroll
             for (int d = 1; d < kComputeWarps; d <<= 1) {
@@ -462,11 +489,22 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         if (tu1 == kSentinel) break;
         const int j = k - kLag;
         unsigned tu2 = kVoid;
-        if (j >= 0) {
+        if (!Cfg::kP1First && j >= 0) {
             if (!wait2(j)) { draining = false; break; }
             tu2 = ctl->tile[j % kRing];
         }
         T v1[IPT], v2[IPT];
+        if constexpr (Cfg::kP1First) {
+            if (tu1 != kVoid) fetch(stageA + s * kTileBytes, tu1, v1);
+            finish1(k, s, tu1, v1);
+            if (j >= 0) {
+                if (!wait2(j)) { draining = false; break; }
+                tu2 = ctl->tile[j % kRing];
+                if (tu2 != kVoid) fetch(stageB + (j % kSB) * kTileBytes, tu2, v2);
+                finish2(j, tu2, v2);
+            }
+            continue;
+        }
         if (tu1 != kVoid) fetch(stageA + s * kTileBytes, tu1, v1);
         if (j >= 0 && tu2 != kVoid) fetch(stageB + (j % kSB) * kTileBytes, tu2, v2);
         finish1(k, s, tu1, v1);
@@ -485,9 +523,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 // ----------------------------------------------------------------- host side
 namespace {
 
-template <class Op, bool kExcl>
-cudaError_t launch_seg_one(const ScanParams& p, unsigned grid, cudaStream_t s) {
-    using Cfg = SegCfg;
+template <class Op, bool kExcl, class Cfg, bool kPeriodic>
+cudaError_t launch_seg_cfg(const ScanParams& p, unsigned grid, cudaStream_t s) {
     using T = typename Op::T;
     const long long tile = Cfg::kTileBytes / sizeof(T);
     const long long nfull = p.n / tile;
@@ -495,14 +532,25 @@ cudaError_t launch_seg_one(const ScanParams& p, unsigned grid, cudaStream_t s) {
     const unsigned long long rows = (unsigned long long)nfull * Cfg::kRows;
     if (nfull < 1 || !make_map(&a, p.in, rows, Cfg::kRows) || !make_map(&b, p.out, rows, Cfg::kRows))
         return cudaErrorInvalidValue;
-    // stages and control block, then kSA flag buffers and the pass-2 mask ring
-    constexpr int smem = Cfg::kSmemBytes + Cfg::kSA * Cfg::kCompute * 32 + (Cfg::kLag + 2) * Cfg::kCompute * 4;
+    // stages and control block, then (flags only) kSA flag buffers and the pass-2 mask ring
+    constexpr int smem =
+        Cfg::kSmemBytes + (kPeriodic ? 0 : Cfg::kSA * Cfg::kCompute * 32 + (Cfg::kLag + 2) * Cfg::kCompute * 4);
     static_assert(smem <= 232448, "shared memory per CTA");
     static std::atomic<unsigned long long> done_mask{0};
-    const cudaError_t e = allow_smem(segscan_tma_kernel<Op, kExcl, Cfg>, smem, done_mask);
+    const cudaError_t e = allow_smem(segscan_tma_kernel<Op, kExcl, Cfg, kPeriodic>, smem, done_mask);
     if (e != cudaSuccess) return e;
-    segscan_tma_kernel<Op, kExcl, Cfg><<<grid, Cfg::kThreads, smem, s>>>(a, b, p, nfull);
+    segscan_tma_kernel<Op, kExcl, Cfg, kPeriodic><<<grid, Cfg::kThreads, smem, s>>>(a, b, p, nfull);
     return cudaGetLastError();
+}
+
+// Head flags (p.heads) or batched rows (heads at multiples of p.seg_len).
+template <class Op, bool kExcl>
+cudaError_t launch_seg_one(const ScanParams& p, unsigned grid, cudaStream_t s) {
+    static_assert(SegCfg::kTileBytes == SegRowsCfg::kTileBytes && SegCfg::kChunk == SegRowsCfg::kChunk,
+                  "both shapes share the host's tile and chunk sizes");
+    if (p.heads) return launch_seg_cfg<Op, kExcl, SegCfg, false>(p, grid, s);
+    if (p.seg_len <= 0) return cudaErrorInvalidValue;
+    return launch_seg_cfg<Op, kExcl, SegRowsCfg, true>(p, grid, s);
 }
 
 }  // namespace

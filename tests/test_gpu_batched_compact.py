@@ -46,6 +46,44 @@ def test_batched(shape, exclusive, kind):
         assert np.array_equal(y, ref)
 
 
+@pytest.mark.parametrize("kind,op", [("i32", "sum"), ("u32", "xor"), ("i32", "min"), ("u32", "prod"), ("f32", "max"),
+                                     ("f32", "sum")])
+@pytest.mark.parametrize("shape", [(8192, 1), (8192, 5), (4099, 3), (1000, 33), (300, 1000), (20, 8191), (9, 12289),
+                                   (3, 40000), (1024, 64), (64, 4096)])
+def test_batched_rows_persistent(kind, op, shape):
+    """Rows of 4-byte elements on 16-byte aligned arrays of at least one tile
+    whose length does not divide 4096 take the persistent segmented kernel
+    with heads at the multiples of the row length (the others the one-tile
+    kernel, where every tile starts a row): rows shorter than, equal to and
+    longer than a thread's 32 items, a warp's part and the 8192-element tile,
+    in place and not."""
+    import stream_compaction_gb300 as sc
+    from gpu_helpers import CODE, OPC, dev_buffer, stream, to_host
+    from test_gpu_ops import make_input
+    rows, cols = shape
+    x = make_input(kind, op, rows * cols, seed=rows + cols).reshape(rows, cols)
+    for exclusive in (False, True):
+        ref = oracle.scan_batched(x, op, exclusive)
+        for inplace in (False, True):
+            _, xin = to_device(x)
+            xout = xin if inplace else dev_buffer(xin.numel(), xin.dtype)[1]
+            st = sc.sc_scan_batched(CODE[kind], OPC[op], int(exclusive), xin.data_ptr(), xout.data_ptr(), rows, cols,
+                                    stream())
+            assert st == sc.SC_OK, sc.status_string(st)
+            want = sc.SC_PATH_SCAN_ONE_TILE if 4096 % cols == 0 else sc.SC_PATH_SEGSCAN_PERSISTENT
+            assert sc.sc_debug_last_path() == want, shape
+            assert sc.sc_get_device_error(stream()) == sc.SC_OK
+            y = to_host(xout, x)
+            if kind == "f32" and op == "sum":
+                s_abs = np.stack([oracle.abs_prefix(r) for r in x])
+                check_f32(y.reshape(-1), ref.reshape(-1), s_abs.reshape(-1))
+            elif kind == "f32":
+                from gpu_helpers import same_float
+                assert same_float(y, ref), (shape, exclusive, inplace)
+            else:
+                assert np.array_equal(y, ref), (shape, exclusive, inplace)
+
+
 def test_workload_int32_rows_65536x4096():
     import torch
     spec = synth.WORKLOADS["int32_rows_65536x4096"]

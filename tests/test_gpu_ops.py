@@ -5,7 +5,7 @@ sums and (max, count) pairs, each against the CPU oracle.
 Integer operators, float max / min and (max, count) must match bit for bit
 (float NaN outputs: both NaN); float64 sums must lie within the bound
 documented in include/sc_scan.h (gpu_helpers.check_f64).  Sizes cover one
-element, ragged tiles of both element sizes, the short-scan path (n <= 2^21)
+element, ragged tiles of both element sizes, the short-scan path (n <= 2^22)
 and the persistent kernel (larger n) with a ragged last chunk.
 """
 import numpy as np
@@ -23,7 +23,7 @@ CASES = [("i32", "min"), ("u32", "max"), ("u32", "min"), ("i32", "prod"), ("u32"
          ("u64", "prod"), ("u64", "and"), ("i64", "or"), ("u64", "xor"), ("i64", "max"), ("i64", "min"),
          ("u64", "max"), ("u64", "min"), ("f32", "max"), ("f32", "min"), ("f64", "sum"), ("f64", "max"),
          ("f64", "min"), ("maxcount", "maxcount")]
-SIZES = [1, 2, 31, 33, 2047, 2049, 4097, 3 * 4096 + 5, 100003, (1 << 21) + 1, 3 * (1 << 21) + 77]
+SIZES = [1, 2, 31, 33, 2047, 2049, 4097, 3 * 4096 + 5, 100003, (1 << 21) + 1, (1 << 22) + 1, 3 * (1 << 21) + 77]
 
 _NP = {"i32": np.int32, "u32": np.uint32, "i64": np.int64, "u64": np.uint64, "f32": np.float32, "f64": np.float64}
 

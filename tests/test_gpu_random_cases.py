@@ -1,5 +1,5 @@
 """Seeded random cases across the entry points, against the oracle: sizes near
-the boundaries between kernel paths (one-tile kernel up to 2^21 elements,
+the boundaries between kernel paths (one-tile kernel up to 2^22 elements,
 8192-element tiles and 2-tile chunks of the persistent kernels), element
 offsets that break 16-byte alignment, in-place calls, exclusive and
 inclusive forms, head densities and operators.  Each case is exact (integers,
@@ -24,7 +24,7 @@ def _lib():
 
 
 def _size(rng):
-    base = int(rng.choice([8192, 16384, 1 << 21, 3 * 16384, 4096, 64 * 16384]))
+    base = int(rng.choice([8192, 16384, 1 << 21, 1 << 22, 3 * 16384, 4096, 64 * 16384]))
     return max(1, base * int(rng.integers(1, 3)) + int(rng.integers(-70, 70)))
 
 

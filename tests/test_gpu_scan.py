@@ -178,7 +178,7 @@ def test_float32_sum_infinities_cross_tiles():
     makes of them: +inf after a +inf, NaN once -inf has followed, in the
     persistent scan and in the persistent segmented scan (a head resets)."""
     from test_gpu_segmented import gpu_segmented
-    n = (1 << 21) + 3 * 8192 + 5                      # persistent kernels: several tiles and chunks
+    n = (1 << 22) + 3 * 8192 + 5                      # persistent kernels: several tiles and chunks
     rng = np.random.default_rng(17)
     x = rng.uniform(-1, 1, n).astype(np.float32)
     x[5000] = np.inf
@@ -200,9 +200,9 @@ def test_float32_sum_infinities_cross_tiles():
 
 
 # ------------------------------------- persistent scan: in place, boundaries
-# Sizes just past the short-scan limit (2^21) and around the persistent
+# Sizes just past the short-scan limit (2^22) and around the persistent
 # kernel's 8192-element tiles and 2-tile chunks, each with a ragged end.
-P_SIZES = [(1 << 21) + 1, (1 << 21) + 8192, (1 << 22) - 1, (1 << 22) + 16384 + 1, 3 * (1 << 21) + 77]
+P_SIZES = [(1 << 22) + 1, (1 << 22) + 8192, (1 << 23) - 1, (1 << 22) + 16384 + 1, 3 * (1 << 22) + 77]
 P_KINDS = [("u32", "sum"), ("f32", "sum"), ("maxi32", "max"), ("affine", "affine"), ("i64", "sum"),
            ("f64", "sum"), ("maxcount", "maxcount")]
 
