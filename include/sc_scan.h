@@ -20,10 +20,11 @@
  *   (SC_I32, SC_SUM), (SC_U32, SC_SUM)  sum modulo 2^32 (two's complement
  *                                        wraparound; identical bits for both);
  *   (SC_F32, SC_SUM)                    float32 sum; within a tile in fp32, the
- *                                        carry between tiles as a float-float
- *                                        pair (about 44 bits); result
- *                                        within 1e-5 * sum_{k<=i} |x[k]| of the
- *                                        exact prefix (not bitwise
+ *                                        inclusive prefix carried between tiles
+ *                                        as a float-float pair (about 45 bits),
+ *                                        tile totals folded in fp32 onto it;
+ *                                        result within 1e-5 * sum_{k<=i} |x[k]|
+ *                                        of the exact prefix (not bitwise
  *                                        reproducible: the look-back may fold
  *                                        tile totals in a different grouping
  *                                        from run to run);

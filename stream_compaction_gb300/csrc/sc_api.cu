@@ -77,6 +77,10 @@ struct Workspace {
     bool dirty = true;                 // needs a zeroing memset before use
     unsigned long long counter_base = 0;
     unsigned epoch = 0;
+    // bytes from here on may hold data other than status words (a radix pass's
+    // digit counts, the hierarchical variant's totals), which a look-back
+    // must not read as statuses: cleared up to a call's status area first
+    size_t junk_from = SIZE_MAX;
 };
 
 std::mutex g_ws_mu;
@@ -96,7 +100,12 @@ sc_status refuse_capture(cudaStream_t s) {
     return cs == cudaStreamCaptureStatusNone ? SC_OK : SC_ERR_UNSUPPORTED;
 }
 
-sc_status acquire_ws(cudaStream_t s, size_t need, Workspace** out) {
+// status_need: the end of the call's look-back status area (lookback_bytes(n));
+// max_epoch: the largest epoch the call's status format holds (2^30 - 1, or
+// 2^7 - 1 for one-word float-float carries): past it the workspace is cleared
+// and the epochs start again.
+sc_status acquire_ws(cudaStream_t s, size_t need, Workspace** out, size_t status_need = 0,
+                     unsigned max_epoch = kMaxEpoch) {
     const sc_status cap = refuse_capture(s);
     if (cap != SC_OK) return cap;
     int dev = 0;
@@ -120,11 +129,15 @@ sc_status acquire_ws(cudaStream_t s, size_t need, Workspace** out) {
         ws.owned = true;
         ws.dirty = true;
     }
-    if (ws.dirty || ws.epoch >= kMaxEpoch) {
+    if (ws.dirty || ws.epoch >= max_epoch) {
         if (cudaMemsetAsync(ws.base, 0, ws.bytes, s) != cudaSuccess) return SC_ERR_CUDA;
         ws.counter_base = 0;
         ws.epoch = 0;
         ws.dirty = false;
+        ws.junk_from = SIZE_MAX;
+    } else if (status_need > ws.junk_from) {
+        if (cudaMemsetAsync(ws.base + ws.junk_from, 0, status_need - ws.junk_from, s) != cudaSuccess) return SC_ERR_CUDA;
+        ws.junk_from = status_need;
     }
     *out = &ws;
     return SC_OK;
@@ -318,7 +331,9 @@ sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_le
     const unsigned ntiles = (unsigned)ceil_div(n, tile);
     std::lock_guard<std::mutex> lk(g_ws_mu);
     Workspace* ws = nullptr;
-    sc_status st = acquire_ws(s, lookback_bytes(n), &ws);
+    // float32 sums carry float-float pairs in one-word statuses with a 7-bit epoch
+    const unsigned max_epoch = oid == scg::OID_SUM_F32 ? (1u << scg::kFloat2EpochBits) - 1 : kMaxEpoch;
+    sc_status st = acquire_ws(s, lookback_bytes(n), &ws, lookback_bytes(n), max_epoch);
     if (st != SC_OK) return st;
     ScanParams p;
     p.in = in;
@@ -633,9 +648,10 @@ static sc_status radix_one_pass(const uint32_t* in, uint32_t* out, int64_t n, in
     {
         std::lock_guard<std::mutex> lk(g_ws_mu);
         Workspace* ws = nullptr;
-        const sc_status st = acquire_ws(s, counts_off + (size_t)m * 4, &ws);
+        const sc_status st = acquire_ws(s, counts_off + (size_t)m * 4, &ws, lookback_bytes(m));
         if (st != SC_OK) return st;
         base = ws->base;
+        ws->junk_from = std::min(ws->junk_from, counts_off);  // the digit counts follow the scan's statuses
     }
     uint32_t* counts = reinterpret_cast<uint32_t*>(base + counts_off);
     cudaError_t e = scg::launch_radix_count(in, n, shift, mask, counts, ntiles, s);
@@ -741,7 +757,7 @@ sc_status sc_compact_if(sc_dtype dtype, const void* in, void* out, int64_t* d_co
     const unsigned ntiles = (unsigned)ceil_div(n, unit);
     std::lock_guard<std::mutex> lk(g_ws_mu);
     Workspace* ws = nullptr;
-    sc_status st = acquire_ws(s, lookback_bytes(n), &ws);
+    sc_status st = acquire_ws(s, lookback_bytes(n), &ws, lookback_bytes(n));
     if (st != SC_OK) return st;
     p.lb = make_ctl(*ws, ntiles);
     p.lb.stride_words = status_stride_words(lookback_bytes(n) - kStatusOffset, ntiles);
@@ -835,6 +851,7 @@ sc_status sc_scan_hierarchical(sc_dtype dtype, sc_op op, int exclusive, const vo
     Workspace* ws = nullptr;
     st = acquire_ws(s, std::max(need, lookback_bytes(n)), &ws);
     if (st != SC_OK) return st;
+    ws->junk_from = kStatusOffset;  // per-level totals where statuses go
     return hier_level(oid, elem_bytes(dtype), in, out, n, exclusive != 0, ws->base, kStatusOffset, s);
 }
 

@@ -59,6 +59,13 @@ struct OpSumF32 {
     __device__ __forceinline__ static C c_op(C a, C b) { return ff_add(a, b); }
     __device__ __forceinline__ static C lift(T a) { return make_float2(a, 0.0f); }
     __device__ __forceinline__ static T lower(C c) { return __fadd_rn(c.x, c.y); }
+    // look-back: aggregates folded in float32, one float-float add onto the prefix
+    static constexpr bool kLowFold = true;
+    using L = float;
+    __device__ __forceinline__ static L low(C c) { return c.x; }
+    __device__ __forceinline__ static L low_identity() { return 0.0f; }
+    __device__ __forceinline__ static L low_op(L a, L b) { return __fadd_rn(a, b); }
+    __device__ __forceinline__ static C with_low(C prefix, L s) { return ff_add(prefix, make_float2(s, 0.0f)); }
 };
 
 struct OpMaxI32 {  // identity INT32_MIN (the "-infinity" of the PMPP identity table)
@@ -394,8 +401,108 @@ struct StatusIO {
     }
 };
 
+// Float-float carries (the float32 sum's (high, low) pair, and its
+// segmented form, which keeps a segment flag in the low part's lowest bit)
+// travel in ONE 64-bit word: the high part's 32 bits, then the low part as a
+// signed 22-bit multiple of 2^-21 ulp(high) (|low| <= ulp(high)/2, so the
+// multiple fits; quantisation error <= 2^-22 ulp(high) = 2^-45 |high|), a
+// 7-bit epoch, the 2-bit flag and the low part's lowest bit:
+//   [high:32 | lowq:22 | epoch:7 | flag:2 | lowbit:1].
+// One word is read and written whole, and a one-word status measured about
+// half of the float32 sum's gap to the uint32 sum on GB300 (the other half
+// is the float-float arithmetic, see LowFold).  The host keeps the epoch of
+// calls with this carry below 2^7 (it clears the status area when the
+// workspace's epoch would pass 127).
+template <>
+struct StatusIO<float2> {
+    static constexpr int kWords = 1;
+
+    __device__ __forceinline__ static unsigned long long* slot(const LookbackCtl& lb, long long tile) {
+        return lb.status + tile * (lb.stride_words ? (long long)lb.stride_words : 1ll);
+    }
+    // exponent field of the high part; the low part's scale is ulp(high) * 2^-21 = 2^(e - 171)
+    __device__ __forceinline__ static int expo(float hi) { return (int)((__float_as_uint(hi) >> 23) & 0xffu); }
+
+    __device__ __forceinline__ static void publish(const LookbackCtl& lb, long long tile, unsigned flag, float2 v) {
+        const uint32_t lob = __float_as_uint(v.y);
+        const int e = expo(v.x);
+        int q = 0;
+        if (e != 0 && e != 255) q = __float2int_rn(ldexpf(__uint_as_float(lob & ~1u), 171 - e));
+        q = max(-(1 << 21), min((1 << 21) - 1, q));
+        const uint32_t lo = ((uint32_t)q << 10) | ((lb.epoch & 0x7fu) << 3) | ((flag & 3u) << 1) | (lob & 1u);
+        st_relaxed_u64(slot(lb, tile), ((unsigned long long)__float_as_uint(v.x) << 32) | lo);
+    }
+
+    __device__ __forceinline__ static unsigned read(const LookbackCtl& lb, long long tile, float2& v) {
+        const unsigned long long w = ld_relaxed_u64(slot(lb, tile));
+        const uint32_t lo = (uint32_t)w;
+        if (((lo >> 3) & 0x7fu) != lb.epoch) return ST_INVALID;
+        const float hi = __uint_as_float((uint32_t)(w >> 32));
+        const int q = (int)lo >> 10;  // arithmetic shift: the signed multiple
+        const float l = ldexpf((float)q, expo(hi) - 171);
+        v = make_float2(hi, __uint_as_float((__float_as_uint(l) & ~1u) | (lo & 1u)));
+        return (lo >> 1) & 3u;
+    }
+};
+
 // Record a device-side failure (first error wins).
 __device__ __forceinline__ void raise_error(unsigned int* err, unsigned code) { atomicCAS(err, 0u, code); }
+
+// Operators whose look-back may fold the aggregates after the newest
+// inclusive prefix in a cheaper, lower precision L (Op::low, Op::low_op) and
+// combine that sum with the prefix once (Op::with_low).  The float32 sum does:
+// its aggregates are float32 chunk totals (their low parts dropped), each
+// folded into exactly one prefix, so the float32 rounding of these folds adds
+// at most about log2(256) * 2^-24 of the sum of |x| over the folded chunks,
+// and the carried prefixes stay float-float.
+template <class Op, class = void>
+struct LowFold { static constexpr bool value = false; };
+template <class Op>
+struct LowFold<Op, std::void_t<decltype(Op::kLowFold)>> { static constexpr bool value = Op::kLowFold; };
+
+// The low-precision accumulator type of a LowFold operator (unused otherwise).
+template <class Op, bool = LowFold<Op>::value>
+struct LowFoldType {
+    using L = int;
+    __device__ __forceinline__ static L identity() { return 0; }
+};
+template <class Op>
+struct LowFoldType<Op, true> {
+    using L = typename Op::L;
+    __device__ __forceinline__ static L identity() { return Op::low_identity(); }
+};
+
+// One look-back window of a LowFold operator: the aggregates after the newest
+// inclusive prefix (lane hp, entry newest_p; hp < 0: none in the window) are
+// folded in the low precision into low_acc (which holds those of the newer
+// windows); when the window holds the prefix, prefix (+) low_acc is left in
+// acc and true returned.  Entries j >= per are unused.
+template <class Op, int kMax>
+__device__ __forceinline__ bool fold_window_low(const typename Op::C (&val)[kMax], int per, int newest_p, int hp,
+                                                typename Op::L& low_acc, typename Op::C& acc) {
+    using C = typename Op::C;
+    using L = typename Op::L;
+    const int lane = threadIdx.x & 31;
+    L xs = Op::low_identity();
+    C pv = Op::c_identity();
+    if (lane >= hp) {
+        const int j0 = lane == hp ? newest_p + 1 : 0;
+#pragma unroll
+        for (int j = 0; j < kMax; ++j) {
+            if (j < per && j >= j0) xs = Op::low_op(xs, Op::low(val[j]));
+            if (lane == hp && j == newest_p) pv = val[j];
+        }
+    }
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const L y = shfl_down_v(xs, d);
+        if (lane + d < 32) xs = Op::low_op(xs, y);
+    }
+    low_acc = Op::low_op(shfl_idx_v(xs, 0), low_acc);
+    if (hp < 0) return false;
+    acc = Op::with_low(shfl_idx_v(pv, hp), low_acc);
+    return true;
+}
 
 // Warp-collective decoupled look-back for tile `tile` (> 0).  A window covers
 // the 32*kPer predecessors [end - 32*kPer, end): lane l reads the kPer
@@ -415,6 +522,7 @@ __device__ bool lookback_prefix(const LookbackCtl& lb, long long tile, typename 
     constexpr int W = 32 * kPer;
     const int lane = threadIdx.x & 31;
     C acc = Op::c_identity();
+    typename LowFoldType<Op>::L low_acc = LowFoldType<Op>::identity();
     long long end = tile;
     unsigned long long t_start = 0;
     unsigned polls = 0;
@@ -455,21 +563,25 @@ __device__ bool lookback_prefix(const LookbackCtl& lb, long long tile, typename 
             sleep_ns = min(sleep_ns * 2u, 256u);
             continue;
         }
-        C x = Op::c_identity();
-        if (lane >= hp) {
-            const int j0 = lane == hp ? newest_p : 0;
-#pragma unroll
-            for (int j = 0; j < kPer; ++j)
-                if (j >= j0) x = Op::c_op(x, val[j]);
-        }
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const C y = shfl_down_v(x, d);
-            if (lane + d < 32) x = Op::c_op(x, y);
-        }
-        acc = Op::c_op(shfl_idx_v(x, 0), acc);
         if (windows_out) ++*windows_out;
-        if (pm) break;
+        if constexpr (LowFold<Op>::value) {
+            if (fold_window_low<Op, kPer>(val, kPer, newest_p, hp, low_acc, acc)) break;
+        } else {
+            C x = Op::c_identity();
+            if (lane >= hp) {
+                const int j0 = lane == hp ? newest_p : 0;
+#pragma unroll
+                for (int j = 0; j < kPer; ++j)
+                    if (j >= j0) x = Op::c_op(x, val[j]);
+            }
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const C y = shfl_down_v(x, d);
+                if (lane + d < 32) x = Op::c_op(x, y);
+            }
+            acc = Op::c_op(shfl_idx_v(x, 0), acc);
+            if (pm) break;
+        }
         end -= W;
     }
     if (polls_out) *polls_out = polls;
@@ -490,6 +602,7 @@ __device__ bool lookback_prefix_adaptive(const LookbackCtl& lb, long long tile, 
     using C = typename Op::C;
     const int lane = threadIdx.x & 31;
     C acc = Op::c_identity();
+    typename LowFoldType<Op>::L low_acc = LowFoldType<Op>::identity();
     long long end = tile;
     int per = kFirstPer;
     unsigned long long t_start = 0;
@@ -531,21 +644,25 @@ __device__ bool lookback_prefix_adaptive(const LookbackCtl& lb, long long tile, 
             sleep_ns = min(sleep_ns * 2u, 256u);
             continue;
         }
-        C x = Op::c_identity();
-        if (lane >= hp) {
-            const int j0 = lane == hp ? newest_p : 0;
-#pragma unroll
-            for (int j = 0; j < kMaxPer; ++j)
-                if (j < per && j >= j0) x = Op::c_op(x, val[j]);
-        }
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const C y = shfl_down_v(x, d);
-            if (lane + d < 32) x = Op::c_op(x, y);
-        }
-        acc = Op::c_op(shfl_idx_v(x, 0), acc);
         if (windows_out) ++*windows_out;
-        if (pm) break;
+        if constexpr (LowFold<Op>::value) {
+            if (fold_window_low<Op, kMaxPer>(val, per, newest_p, hp, low_acc, acc)) break;
+        } else {
+            C x = Op::c_identity();
+            if (lane >= hp) {
+                const int j0 = lane == hp ? newest_p : 0;
+#pragma unroll
+                for (int j = 0; j < kMaxPer; ++j)
+                    if (j < per && j >= j0) x = Op::c_op(x, val[j]);
+            }
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const C y = shfl_down_v(x, d);
+                if (lane + d < 32) x = Op::c_op(x, y);
+            }
+            acc = Op::c_op(shfl_idx_v(x, 0), acc);
+            if (pm) break;
+        }
         end -= 32LL * per;
         per = min(per * 2, kMaxPer);
     }

@@ -47,6 +47,10 @@ enum ScanOpId : int {
 };
 constexpr int kFirstExtraOid = OID_PROD_U32;
 
+// Epoch bits of the one-word float-float look-back status (float32 sums):
+// calls with that carry run with epochs below 2^kFloat2EpochBits.
+constexpr unsigned kFloat2EpochBits = 7;
+
 // Element bytes of an operator id (4, or 8 for 64-bit types and pairs).
 constexpr int oid_elem_bytes(int oid) {
     return (oid == OID_AFFINE_U32 || oid == OID_MAXCOUNT_I32 || (oid >= OID_SUM_U64 && oid <= OID_MIN_U64) ||

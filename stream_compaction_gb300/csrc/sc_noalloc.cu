@@ -104,7 +104,9 @@ extern "C" sc_status sc_scan_noalloc(sc_dtype dtype, sc_op op, int exclusive, co
     // read as "not yet published", so they need no clearing except when the
     // epoch wraps.  The error word is left alone: it collects every call's
     // failures until sc_scan_noalloc_error reads and clears it.
-    if (slot->epoch >= kMaxEpoch) {
+    // float32 sums carry float-float pairs in one-word statuses with a 7-bit epoch
+    const unsigned max_epoch = oid == 1 ? (1u << scg::kFloat2EpochBits) - 1 : kMaxEpoch;
+    if (slot->epoch >= max_epoch) {
         if (cudaMemsetAsync(base + kHeader, 0, kScratchBytes - kHeader, s) != cudaSuccess) return SC_ERR_CUDA;
         slot->epoch = 0;
     }

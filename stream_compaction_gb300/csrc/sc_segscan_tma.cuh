@@ -91,6 +91,15 @@ struct SegPairOp<OpSumF32> {
         if (flag(b)) return b;
         return tag(OpSumF32::c_op(plain(a), plain(b)), flag(a));
     }
+    // look-back: a chunk that holds a head publishes its inclusive prefix at
+    // once, so the aggregates after the newest prefix carry no flag and fold
+    // as a float32 sum (as OpSumF32's)
+    static constexpr bool kLowFold = true;
+    using L = float;
+    __device__ __forceinline__ static L low(C c) { return c.x; }
+    __device__ __forceinline__ static L low_identity() { return 0.0f; }
+    __device__ __forceinline__ static L low_op(L a, L b) { return __fadd_rn(a, b); }
+    __device__ __forceinline__ static C with_low(C prefix, L s) { return c_op(prefix, tag(make_float2(s, 0.0f), false)); }
 };
 
 // 1-D bulk copy global -> shared, completing on an mbarrier (16-byte aligned

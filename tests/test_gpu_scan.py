@@ -261,3 +261,35 @@ def test_host_scan_in_place_across_chunks(kind, op, n):
             check_f32(h, ref, oracle.abs_prefix(x), "host in place")
         else:
             assert np.array_equal(h, ref)
+
+
+def test_float32_statuses_across_epoch_wraps_and_workspace_reuse():
+    """Float32 sums carry float-float pairs in one-word look-back statuses with
+    a 7-bit epoch, so the library clears the status area whenever a stream's
+    epoch would pass 127.  Many calls on one stream, float32 sums interleaved
+    with uint32 sums (which keep counting epochs past 127), the hierarchical
+    variant and a radix pass (both leave other data where statuses go), each
+    checked against the oracle."""
+    import stream_compaction_gb300 as sc
+    from gpu_helpers import stream
+    rng = np.random.default_rng(11)
+    xs = {n: rng.uniform(-1, 1, n).astype(np.float32) for n in (100003, (1 << 22) + 8195)}
+    refs = {n: oracle.scan(x, "sum", True) for n, x in xs.items()}
+    scales = {n: oracle.abs_prefix(x) for n, x in xs.items()}
+    u = _input("u32", 300007, seed=5)
+    uref = oracle.scan(u, "sum", False)
+    keys = _input("u32", 70001, seed=6)
+    for it in range(420):
+        n = (1 << 22) + 8195 if it % 7 == 3 else 100003
+        y = gpu_scan(xs[n], "sum", True)
+        check_f32(y, refs[n], scales[n], "it %d" % it)
+        if it % 3 == 0:
+            assert np.array_equal(gpu_scan(u, "sum", False), uref)
+        if it % 50 == 7:
+            assert np.array_equal(gpu_scan(u, "sum", False, hierarchical=True), uref)
+        if it % 50 == 19:
+            import torch
+            kd = torch.from_numpy(keys.view(np.int32)).cuda()
+            ko = torch.empty_like(kd)
+            assert sc.sc_radix_pass_u32(kd.data_ptr(), ko.data_ptr(), keys.size, 8, 8, stream()) == sc.SC_OK
+            assert np.array_equal(ko.cpu().numpy().view(np.uint32), oracle.radix_pass(keys, 8, 8))
