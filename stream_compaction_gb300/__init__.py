@@ -178,7 +178,7 @@ def sc_scan_noalloc_error(stream: int) -> int:
 
 # kernel families reported by sc_debug_last_path
 (SC_PATH_NONE, SC_PATH_SCAN_ONE_TILE, SC_PATH_SCAN_PERSISTENT, SC_PATH_SEGSCAN_PERSISTENT,
- SC_PATH_COMPACT_PERSISTENT, SC_PATH_COMPACT_ONE_TILE) = range(6)
+ SC_PATH_COMPACT_PERSISTENT, SC_PATH_COMPACT_ONE_TILE, SC_PATH_ROWS_PERSISTENT) = range(7)
 
 
 def sc_debug_last_path() -> int:

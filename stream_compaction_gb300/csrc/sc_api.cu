@@ -344,15 +344,28 @@ sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_le
     p.vec_ok = vec_ok;
     p.carry_in = carry_in;
     p.carry_out = carry_out;
+    // Batched rows whose length divides the rows kernel's 8192-element tile:
+    // every tile holds whole rows, so the persistent rows kernel scans each
+    // tile on its own (no look-back, one read of each element).
+    const int64_t rows_tile = scg::rows_tma_tile_elems();
+    if (seg_len > 0 && !heads && rows_tile % seg_len == 0 && api_variant == 0 && scg::rows_tma_supported(oid) &&
+        vec_ok && n >= rows_tile && !carry_in && !carry_out && n / rows_tile * 256 < (int64_t)INT_MAX &&
+        num_sms() > 0) {
+        const int64_t tiles = ceil_div(n, rows_tile);
+        p.lb = make_ctl(*ws, (unsigned)tiles);
+        const unsigned grid = (unsigned)std::min<int64_t>(num_sms(), tiles);
+        g_last_path = SC_PATH_ROWS_PERSISTENT;
+        return finish_launch(*ws, 0, scg::launch_rows_tma(oid, p, excl, grid, s));
+    }
+    // Other batched rows whose length divides the one-tile kernel's tile stay
+    // there (every tile starts a row: no look-back at all; measured on GB300
+    // with 2^28 int32, rows of 16-4096: 0.77-0.80 of the copy peak against 0.70
+    // on the persistent segmented kernel); other row lengths (33, 1000, 2047:
+    // 0.56 there) take the persistent segmented kernel (0.75).
+    const int64_t seg_tile = scg::segscan_tma_tile_elems();
     // scans segmented by head flags, and batched rows (heads at the multiples
     // of the row length): the persistent kernel when the operator has that
     // form and the arrays are 16-byte aligned and hold a full tile
-    // Batched rows whose length divides the one-tile kernel's tile stay there
-    // (every tile starts a row: no look-back at all; measured on GB300 with
-    // 2^28 int32, rows of 16-4096: 0.77-0.80 of the copy peak against 0.70 on
-    // the persistent kernel); other row lengths (33, 1000, 2047: 0.56 there)
-    // take the persistent kernel (0.69-0.70).
-    const int64_t seg_tile = scg::segscan_tma_tile_elems();
     const bool rows_fit_tiles = seg_len > 0 && scg::scan_tile_elems(oid, legacy_variant) % seg_len == 0;
     if (segmented && !rows_fit_tiles && api_variant == 0 && scg::segscan_tma_supported(oid) && vec_ok &&
         (!heads || aligned(heads, 16)) && n >= seg_tile && !carry_in && !carry_out &&

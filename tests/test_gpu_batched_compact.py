@@ -47,15 +47,16 @@ def test_batched(shape, exclusive, kind):
 
 
 @pytest.mark.parametrize("kind,op", [("i32", "sum"), ("u32", "xor"), ("i32", "min"), ("u32", "prod"), ("f32", "max"),
-                                     ("f32", "sum")])
+                                     ("f32", "sum"), ("i32", "max")])
 @pytest.mark.parametrize("shape", [(8192, 1), (8192, 5), (4099, 3), (1000, 33), (300, 1000), (20, 8191), (9, 12289),
-                                   (3, 40000), (1024, 64), (64, 4096)])
+                                   (3, 40000), (1024, 64), (64, 4096), (7, 8192), (3000, 32), (70000, 2), (513, 16)])
 def test_batched_rows_persistent(kind, op, shape):
-    """Rows of 4-byte elements on 16-byte aligned arrays of at least one tile
-    whose length does not divide 4096 take the persistent segmented kernel
-    with heads at the multiples of the row length (the others the one-tile
-    kernel, where every tile starts a row): rows shorter than, equal to and
-    longer than a thread's 32 items, a warp's part and the 8192-element tile,
+    """Rows of 4-byte elements on 16-byte aligned arrays of at least one tile:
+    lengths that divide 8192 on the persistent rows kernel (sum, int32 max,
+    float32 sum; every tile whole rows) or else the one-tile kernel, other
+    lengths on the persistent segmented kernel with heads at the multiples of
+    the row length: rows shorter than, equal to and longer than a thread's 32
+    items, a warp's part and the 8192-element tile, with ragged last tiles,
     in place and not."""
     import stream_compaction_gb300 as sc
     from gpu_helpers import CODE, OPC, dev_buffer, stream, to_host
@@ -70,7 +71,10 @@ def test_batched_rows_persistent(kind, op, shape):
             st = sc.sc_scan_batched(CODE[kind], OPC[op], int(exclusive), xin.data_ptr(), xout.data_ptr(), rows, cols,
                                     stream())
             assert st == sc.SC_OK, sc.status_string(st)
-            want = sc.SC_PATH_SCAN_ONE_TILE if 4096 % cols == 0 else sc.SC_PATH_SEGSCAN_PERSISTENT
+            rows_kernel = 8192 % cols == 0 and (kind, op) in (("i32", "sum"), ("u32", "sum"), ("f32", "sum"),
+                                                              ("i32", "max"))
+            want = (sc.SC_PATH_ROWS_PERSISTENT if rows_kernel else
+                    sc.SC_PATH_SCAN_ONE_TILE if 4096 % cols == 0 else sc.SC_PATH_SEGSCAN_PERSISTENT)
             assert sc.sc_debug_last_path() == want, shape
             assert sc.sc_get_device_error(stream()) == sc.SC_OK
             y = to_host(xout, x)
