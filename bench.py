@@ -530,6 +530,14 @@ def measure_configs(args, sc, synth, dev, sampler, peak, headline):
     y = torch.empty_like(x)
     n = x.numel()
     xh = x.cpu().numpy()
+    # what any kernel pays in the same setting: a plain copy of the same bytes
+    # (torch's copy kernel, n reads + n writes) and a one-element fill, both
+    # with L2 flushed before every launch
+    y2, one = torch.empty_like(x), torch.empty(1, dtype=torch.int32, device=dev)
+    t_copy = R.timed(lambda: (y2.copy_(x), 0)[1], flushed=True)
+    t_tiny = R.timed(lambda: (one.fill_(1), 0)[1], flushed=True)
+    floors = {"copy_same_bytes_us_flushed": 1e3 * t_copy[0], "one_element_fill_us_flushed": 1e3 * t_tiny[0]}
+    del y2, one
     for ex in (False, True):
         fn = sc.sc_scan_exclusive if ex else sc.sc_scan_inclusive
         call = lambda: fn(sc.SC_I32, sc.SC_SUM, x.data_ptr(), y.data_ptr(), n, sp)
@@ -540,8 +548,8 @@ def measure_configs(args, sc, synth, dev, sampler, peak, headline):
         c = R.oracle_leg(lambda: oracle.scan(xh, "sum", ex), n, lambda r: np.array_equal(r, yh))
         tw = R.timed(call, flushed=False)
         R.entry(name, n, 8 * n, tf, "recurrence: every output" if ok else "MISMATCH",
-                {"us_flushed": 1e3 * tf[0], "us_warm": 1e3 * tw[0], "clocks_warm": tw[3],
-                 "note": "flushed: one launch between events (includes launch latency); warm: back to back"}, c)
+                dict(floors, us_flushed=1e3 * tf[0], us_warm=1e3 * tw[0], clocks_warm=tw[3],
+                     note="flushed: one launch between events (includes launch latency); warm: back to back"), c)
 
     # 2: float32 exclusive sum, n = 2^26, within 1e-5 * sum_{k<=i} |x_k|
     x = synth.make_torch(W["float32_exsum_n2^26"], device=dev)

@@ -439,7 +439,16 @@ struct StatusIO<float2> {
         if (((lo >> 3) & 0x7fu) != lb.epoch) return ST_INVALID;
         const float hi = __uint_as_float((uint32_t)(w >> 32));
         const int q = (int)lo >> 10;  // arithmetic shift: the signed multiple
-        const float l = ldexpf((float)q, expo(hi) - 171);
+        // l = q * 2^(e - 171), rounded once, without a library call: (float)q
+        // by the 1.5 * 2^23 trick (exact for |q| < 2^22), then two exact
+        // power-of-two factors 2^a * 2^b = 2^(e - 171), each a normal float
+        // (|a|, |b| <= 85; e = 0 and 255 carry q = 0): q * 2^a is exact, so
+        // the result is rounded once, as a correctly rounded ldexpf would be.
+        const int k = max(expo(hi), 1) - 171;
+        const int b = k >> 1, a = k - b;
+        const float qf = __fsub_rn(__int_as_float(0x4B400000 + q), 12582912.0f);
+        const float l = __fmul_rn(__fmul_rn(qf, __uint_as_float((uint32_t)(a + 127) << 23)),
+                                  __uint_as_float((uint32_t)(b + 127) << 23));
         v = make_float2(hi, __uint_as_float((__float_as_uint(l) & ~1u) | (lo & 1u)));
         return (lo >> 1) & 3u;
     }

@@ -10,7 +10,9 @@
 //                   of the pairs, then the CTA's warp totals through shared
 //                   memory (one mbarrier phase per tile, bounded waits);
 //                   results are written back into the stage;
-//   store warp      TMA store of each finished stage, then the stage is freed.
+//   store warp      TMA store of each finished stage; a stage is freed once
+//                   its store has read it, with up to kRowsStoresInFlight
+//                   newer stores still reading theirs.
 //
 // Each element is read once and written once.  The segmented form of the
 // scan is that of "Lecture 7: Parallel pattern -- prefix sum / scan" (UIUC
@@ -26,6 +28,8 @@ using namespace persist;
 
 constexpr int kRowsTileBytes = 32768;            // 256 rows of 128 bytes
 constexpr int kRowsStages = 6;
+constexpr int kRowsStoresInFlight = 3;           // TMA stores that may still read their stage
+static_assert(kRowsStoresInFlight < kRowsStages, "a stage is freed before the producer needs it again");
 constexpr int kRowsComputeWarps = 8;
 constexpr int kRowsCompute = 32 * kRowsComputeWarps;
 constexpr int kRowsProducer = kRowsComputeWarps;  // warp index
@@ -117,12 +121,11 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
                 break;
             }
             const long long t = blockIdx.x + i * gridDim.x;
-            if (t < n_full_tiles) {
+            if (t < n_full_tiles)
                 tma_store_2d_hint(&tm_out, 0, (int)(t * kRowsTileRows), stage0 + s * kRowsTileBytes, once);
-                bulk_commit();
-                bulk_wait_read_all();
-            }
-            mbar_arrive(B(ctl->empty[s]));
+            bulk_commit();  // one group per tile (empty for the ragged tile, stored by the compute warps)
+            bulk_wait_read<kRowsStoresInFlight>();
+            if (i >= kRowsStoresInFlight) mbar_arrive(B(ctl->empty[(i - kRowsStoresInFlight) % kRowsStages]));
         }
         bulk_wait_all();
         return;

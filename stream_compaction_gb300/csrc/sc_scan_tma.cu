@@ -26,7 +26,8 @@ bool tma_shape(int cfg, TmaShape* sh) {
 
 template <class Op>
 cudaError_t launch_scan_tma(const ScanParams& p, bool exclusive, unsigned grid, cudaStream_t s, bool stats, int cfg) {
-    if (cfg == 0) return launch_cfg<Op, Cfg0>(p, exclusive, grid, s, stats);
+    if (cfg == 0) return stats ? launch_cfg<Op, Cfg0>(p, exclusive, grid, s, true)
+                               : launch_cfg<Op, typename DefaultCfg<Op>::type>(p, exclusive, grid, s, false);
     if constexpr (std::is_same<Op, OpSumU32>::value) {
         if (stats) return cudaErrorInvalidValue;
         switch (cfg) {

@@ -139,11 +139,17 @@ struct TmaCfg {
     static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 };
 
-// The shapes compiled in.  0 is the default of every operator (32 KiB tiles,
-// 3 + 3 stages, 8 compute warps, pass-2 lag of 5 tiles, 2-tile chunks, pass 1
-// first: the fastest of the shapes measured on GB300 for uint32 sums of
-// 2^28-2^30 elements, with look-back statuses in lines of their own); the
-// others are uint32-sum variants kept for on-GPU comparison.
+// The shapes compiled in.  0 is the default of every operator but the
+// float32 sum (32 KiB tiles, 3 + 3 stages, 8 compute warps, pass-2 lag of 5
+// tiles, 2-tile chunks, pass 1 first: the fastest of the shapes measured on
+// GB300 for uint32 sums of 2^27-2^30 elements, with look-back statuses in
+// lines of their own); the others are uint32-sum variants kept for on-GPU
+// comparison.  The float32 sum's look-back (float-float statuses) takes
+// longer, so its default waits one tile more before pass 2 (CfgSumF32:
+// measured at 2^26 / 2^27 / 2^28 elements 0.76 / 0.83 / 0.87 of the copy peak
+// at lag 5, 0.79 / 0.85 / 0.89 at lag 6, the same at lag 7, 0.77 / 0.81 /
+// 0.83 at lag 8; the uint32 sum at lag 6: 0.85 / 0.90 / 0.93 against 0.84 /
+// 0.91 / 0.96 at lag 5).
 using Cfg0 = TmaCfg<32768, 3, 3, 8, 5, 2, true>;
 using Cfg1 = TmaCfg<16384, 6, 6, 16, 12, 4>;
 using Cfg2 = TmaCfg<32768, 3, 3, 16, 6, 2>;
@@ -156,6 +162,14 @@ using Cfg6 = TmaCfg<32768, 3, 3, 8, 6, 2, true>;
 using Cfg7 = TmaCfg<32768, 3, 3, 16, 6, 2, true>;
 using Cfg8 = TmaCfg<32768, 3, 3, 8, 6, 1>;
 using Cfg9 = TmaCfg<32768, 3, 3, 16, 5, 2, true>;
+using CfgSumF32 = TmaCfg<32768, 3, 3, 8, 6, 2, true>;
+// The default shape of an operator (same tile, chunk and thread count as Cfg0,
+// which the host sizes launches by).
+template <class Op> struct DefaultCfg { using type = Cfg0; };
+template <> struct DefaultCfg<OpSumF32> { using type = CfgSumF32; };
+static_assert(CfgSumF32::kTileBytes == Cfg0::kTileBytes && CfgSumF32::kChunk == Cfg0::kChunk &&
+                  CfgSumF32::kThreads == Cfg0::kThreads && CfgSumF32::kSmemBytes == Cfg0::kSmemBytes,
+              "the host sizes every default launch by Cfg0");
 constexpr int kNumCfgs = 10;
 
 // For operators with costly combines, pass 1 keeps each compute thread's
@@ -218,6 +232,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
     const unsigned long long wait_limit = p.lb.timeout_ns + 500000000ull;
     unsigned long long* st = p.lb.stats;
     const volatile int* end_k = &ctl->end_k;
+    if (threadIdx.x == 0) {  // fetch both tensor maps while the barriers are set up
+        prefetch_tensormap(&tm_in);
+        prefetch_tensormap(&tm_out);
+    }
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kSA; ++i) {
