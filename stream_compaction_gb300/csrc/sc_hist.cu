@@ -7,8 +7,9 @@
 //
 // counts[b] += number of i with bins[i] == b, 0 <= b < nbins (entries outside
 // are skipped).  Beyond kWarpCopyBins bins, a run of equal neighbouring bins
-// in a warp step (128 consecutive entries) is counted with one atomic, so
-// sorted input (CSR rows) costs about one atomic per row per warp step.  Up to
+// in a warp step (512 consecutive entries, 16 per thread) is counted with one
+// atomic, so sorted input (CSR rows) costs about one atomic per row per warp
+// step.  Up to
 // kWarpCopyBins bins each warp counts into its own
 // shared-memory histogram (plain shared atomics), up to kSmemBins bins each CTA
 // into one shared histogram; the CTA adds its counts to the global ones once
@@ -42,40 +43,84 @@ __global__ void __launch_bounds__(kHistThreads) histogram_kernel(const int32_t* 
     auto add = [&](int b) {  // one shared histogram per warp: plain shared atomics
         if (b >= 0 && b < nbins) atomicAdd(&mine[b], 1u);
     };
-    // The warp step's 128 bins in memory order (lane l holds 4l .. 4l+3): one
-    // atomic per run of equal neighbours, its length from the next run's start
-    // (a shuffle finds the starts, a ballot and one shuffle the next start in
-    // a later lane).  No __match_any_sync: its cost grows with the number of
-    // distinct values and it bounded this kernel (address-divergence unit 90 %
-    // busy on CSR rows).
-    auto add_runs = [&](const int (&b)[4]) {
-        const int prev = __shfl_up_sync(0xffffffffu, b[3], 1);
-        bool h[4];
-        h[0] = lane == 0 || b[0] != prev;
-#pragma unroll
-        for (int k = 1; k < 4; ++k) h[k] = b[k] != b[k - 1];
-        const int fh = h[0] ? 0 : h[1] ? 1 : h[2] ? 2 : h[3] ? 3 : 4;  // first run start in this lane
-        const unsigned any = __ballot_sync(0xffffffffu, fh < 4);
-        const unsigned later = lane == 31 ? 0u : any & (0xffffffffu << (lane + 1));
-        const int nl = later ? __ffs(later) - 1 : 32;
-        const int nfh = __shfl_sync(0xffffffffu, fh, nl & 31);
-        int end = nl < 32 ? 4 * nl + nfh : 128;  // start of the run after this lane's last
-#pragma unroll
-        for (int k = 3; k >= 0; --k) {
-            if (h[k]) {
-                const int pos = 4 * lane + k;
-                if (b[k] >= 0 && b[k] < nbins) {
-                    if constexpr (kMode == 1) atomicAdd(&sh[b[k]], (unsigned)(end - pos));
-                    else atomicAdd(&counts[b[k]], (unsigned long long)(end - pos));
-                }
-                end = pos;
+    if constexpr (kMode != 2) {
+        // Runs of equal neighbours, 16 consecutive bins per thread (a warp step
+        // covers 512): the thread counts its own runs; a run that reaches the
+        // thread's end continues into the next lanes' first runs, whose lengths
+        // a reverse scan over the warp gathers, so each run in the warp step
+        // costs one atomic (a run that crosses warp steps costs one per step).
+        constexpr int kPer = 16;
+        auto emit = [&](int b, unsigned len) {
+            if (b >= 0 && b < nbins) {
+                if constexpr (kMode == 1) atomicAdd(&sh[b], len);
+                else atomicAdd(&counts[b], (unsigned long long)len);
             }
+        };
+        auto step = [&](const int (&v)[kPer]) {
+            const int prev = __shfl_up_sync(0xffffffffu, v[kPer - 1], 1);
+            uint32_t hm = (lane == 0 || v[0] != prev) ? 1u : 0u;  // bit k: a run starts at item k
+#pragma unroll
+            for (int k = 1; k < kPer; ++k) hm |= (v[k] != v[k - 1] ? 1u : 0u) << k;
+            // (c, w): this lane's leading continuation length, and whether the
+            // whole lane continues the run before it; the suffix composition
+            // x -> c + w * x over the later lanes gives the length a run
+            // reaching this lane's end gains from them
+            unsigned c = hm & 1u ? 0u : (hm ? (unsigned)(__ffs(hm) - 1) : (unsigned)kPer);
+            bool w = hm == 0u;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const unsigned c2 = __shfl_down_sync(0xffffffffu, c, d);
+                const bool w2 = __shfl_down_sync(0xffffffffu, (unsigned)w, d) != 0u;
+                if (lane + d < 32) {
+                    if (w) c += c2;
+                    w = w && w2;
+                }
+            }
+            const unsigned after = __shfl_down_sync(0xffffffffu, c, 1);  // every lane takes part
+            const unsigned gain = lane == 31 ? 0u : after;
+            // this lane's runs, last first: the last one gains the later lanes' continuation
+            unsigned end = kPer + gain;
+#pragma unroll
+            for (int k = kPer - 1; k >= 0; --k) {
+                if ((hm >> k) & 1u) {
+                    emit(v[k], end - (unsigned)k);
+                    end = (unsigned)k;
+                }
+            }
+        };
+        constexpr int kSteps = 2;  // warp steps per loop iteration, all loads first
+        const long long nchunks = (n + kPer - 1) / kPer;  // per-thread chunks of 16 bins
+        const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+        const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+        for (long long c0 = wid * 32 * kSteps; c0 < nchunks; c0 += nwarps * 32 * kSteps) {
+            int v[kSteps][kPer];
+#pragma unroll
+            for (int u = 0; u < kSteps; ++u) {
+                const long long i = (c0 + u * 32 + lane) * kPer;
+                if (vec && i + kPer <= n) {
+#pragma unroll
+                    for (int q = 0; q < kPer / 4; ++q) {
+                        const int4 r = __ldg(reinterpret_cast<const int4*>(bins + i) + q);
+                        v[u][4 * q] = r.x; v[u][4 * q + 1] = r.y; v[u][4 * q + 2] = r.z; v[u][4 * q + 3] = r.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < kPer; ++k) v[u][k] = i + k < n ? __ldg(bins + i + k) : -1;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kSteps; ++u) step(v[u]);
         }
-    };
-    // groups of 4 consecutive bins (16-byte loads when aligned), kUnroll warp
-    // steps of 32 groups per loop iteration with all loads issued first; every
-    // lane of a warp runs the same number of iterations, so each match sees all
-    // 32 lanes
+        if constexpr (kMode == 1) {
+            __syncthreads();
+            for (int b = threadIdx.x; b < nbins; b += blockDim.x)
+                if (sh[b]) atomicAdd(&counts[b], (unsigned long long)sh[b]);
+        }
+        return;
+    }
+    // kMode 2: groups of 4 consecutive bins (16-byte loads when aligned),
+    // kUnroll warp steps of 32 groups per loop iteration with all loads issued
+    // first
     constexpr int kUnroll = 4;
     const long long ngroups = (n + 3) / 4;
     const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -99,22 +144,15 @@ __global__ void __launch_bounds__(kHistThreads) histogram_kernel(const int32_t* 
             }
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            if constexpr (kMode == 2) {
+        for (int u = 0; u < kUnroll; ++u)
 #pragma unroll
-                for (int k = 0; k < 4; ++k) add(v[u][k]);
-            } else {
-                add_runs(v[u]);
-            }
-        }
+            for (int k = 0; k < 4; ++k) add(v[u][k]);
     }
-    if constexpr (kMode != 0) {
-        __syncthreads();
-        for (int b = threadIdx.x; b < nbins; b += blockDim.x) {
-            unsigned long long c = 0;
-            for (int w = 0; w < copies; ++w) c += sh[w * nbins + b];
-            if (c) atomicAdd(&counts[b], c);
-        }
+    __syncthreads();
+    for (int b = threadIdx.x; b < nbins; b += blockDim.x) {
+        unsigned long long c = 0;
+        for (int w = 0; w < copies; ++w) c += sh[w * nbins + b];
+        if (c) atomicAdd(&counts[b], c);
     }
 }
 
@@ -144,12 +182,13 @@ cudaError_t launch_histogram(const int32_t* bins, long long n, int nbins, unsign
         const long long want = (ngroups + 32 * unroll - 1) / (32 * unroll) * 32 / kHistThreads + 1;
         return (unsigned)std::max<long long>(1, std::min<long long>(want, (long long)num_sms * per_sm));
     };
-    // shared histograms: a few CTAs per SM, each flush costs nbins atomics
+    // shared histograms: a few CTAs per SM, each flush costs nbins atomics;
+    // the run-counting modes cover 1024 bins (256 groups) per warp iteration
     if (nbins <= kWarpCopyBins)
         return launch_mode<2>(bins, n, nbins, counts, grid_of(2, 4), nbins * 4 * (kHistThreads / 32), vec, s);
     if (nbins <= kSmemBins)
-        return launch_mode<1>(bins, n, nbins, counts, grid_of(nbins <= 8192 ? 2 : 1, 4), nbins * 4, vec, s);
-    return launch_mode<0>(bins, n, nbins, counts, grid_of(4, 4), 0, vec, s);
+        return launch_mode<1>(bins, n, nbins, counts, grid_of(nbins <= 8192 ? 2 : 1, 8), nbins * 4, vec, s);
+    return launch_mode<0>(bins, n, nbins, counts, grid_of(2, 8), 0, vec, s);
 }
 
 }  // namespace scg
