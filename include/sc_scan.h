@@ -154,16 +154,18 @@ sc_status sc_scan_exclusive(sc_dtype dtype, sc_op op, const void *in, void *out,
 
 /* Independent scans of the rows of a row-major rows x cols matrix (leading
  * dimension cols, contiguous): row r of out is the scan of row r of in, each
- * starting again from the identity.  One kernel launch.  When cols divides
- * 8192 (int32/uint32 sum, int32 max, float32 sum; 16-byte aligned arrays of
- * at least 8192 elements) every 8192-element tile holds whole rows and a
- * persistent kernel scans each tile on its own, with no look-back.  Otherwise
- * a scan segmented at the multiples of cols (the heads computed from the
- * element index, no flag array): on the persistent segmented kernel for
- * operators with 4-byte elements and 16-byte aligned arrays of at least 8192
- * elements, else on the one-tile-per-CTA kernel; a chunk or tile that holds a
- * row start publishes its complete prefix at once, so look-backs stop there.
- * Same dtypes, ops and aliasing rules as sc_scan_inclusive. */
+ * starting again from the identity.  One kernel launch.  For the int32/uint32
+ * sum, int32 max and float32 sum on 16-byte aligned arrays of at least 8192
+ * elements with cols <= 8192 a persistent rows kernel runs with no look-back:
+ * when cols divides 8192 every 8192-element tile holds whole rows; otherwise
+ * (out != in only) each CTA takes a contiguous range of tiles and carries the
+ * open row from tile to tile.  Everything else is a scan segmented at the
+ * multiples of cols (the heads computed from the element index, no flag
+ * array): on the persistent segmented kernel for operators with 4-byte
+ * elements and 16-byte aligned arrays of at least 8192 elements, else on the
+ * one-tile-per-CTA kernel; a chunk or tile that holds a row start publishes
+ * its complete prefix at once, so look-backs stop there.  Same dtypes, ops and
+ * aliasing rules as sc_scan_inclusive. */
 sc_status sc_scan_batched(sc_dtype dtype, sc_op op, int exclusive, const void *in, void *out,
                           int64_t rows, int64_t cols, sc_stream_t stream);
 

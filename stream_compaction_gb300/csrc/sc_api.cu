@@ -344,11 +344,14 @@ sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_le
     p.vec_ok = vec_ok;
     p.carry_in = carry_in;
     p.carry_out = carry_out;
-    // Batched rows whose length divides the rows kernel's 8192-element tile:
-    // every tile holds whole rows, so the persistent rows kernel scans each
-    // tile on its own (no look-back, one read of each element).
+    // Batched rows of at most 8192 elements: the persistent rows kernel (no
+    // look-back, one read of each element).  Rows dividing its 8192-element
+    // tile: every tile holds whole rows.  Other lengths: each CTA carries the
+    // fold of the open row from one tile to the next and reads back, once, the
+    // part of its first tile's row before it, so those need out != in.
     const int64_t rows_tile = scg::rows_tma_tile_elems();
-    if (seg_len > 0 && !heads && rows_tile % seg_len == 0 && api_variant == 0 && scg::rows_tma_supported(oid) &&
+    if (seg_len > 0 && seg_len <= rows_tile && !heads && (rows_tile % seg_len == 0 || in != out) &&
+        api_variant == 0 && scg::rows_tma_supported(oid) &&
         vec_ok && n >= rows_tile && !carry_in && !carry_out && n / rows_tile * 256 < (int64_t)INT_MAX &&
         num_sms() > 0) {
         const int64_t tiles = ceil_div(n, rows_tile);

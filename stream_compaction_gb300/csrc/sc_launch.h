@@ -70,10 +70,11 @@ bool segscan_tma_supported(int op_id);
 cudaError_t launch_segscan_tma(int op_id, const ScanParams& p, bool exclusive, unsigned grid, cudaStream_t s);
 cudaError_t launch_segscan_tma_bits(int op_id, const ScanParams& p, bool exclusive, unsigned grid, cudaStream_t s);
 cudaError_t launch_segscan_tma_order(int op_id, const ScanParams& p, bool exclusive, unsigned grid, cudaStream_t s);
-// Batched rows whose length divides the rows kernel's tile (sc_rows_tma.cu):
-// a persistent kernel with no look-back (every tile holds whole rows); the
-// int32/uint32 sum, int32 max and float32 sum on 16-byte aligned arrays of at
-// least one tile.
+// Batched rows of at most one tile (sc_rows_tma.cu): a persistent kernel with
+// no look-back (rows dividing the tile: every tile holds whole rows; other
+// lengths: a contiguous range of tiles per CTA, the open row carried from tile
+// to tile, out != in); the int32/uint32 sum, int32 max and float32 sum on
+// 16-byte aligned arrays of at least one tile.
 int rows_tma_tile_elems();
 bool rows_tma_supported(int op_id);
 cudaError_t launch_rows_tma(int op_id, const ScanParams& p, bool exclusive, unsigned grid, cudaStream_t s);

@@ -1,7 +1,14 @@
-// Batched rows whose length divides the 8192-element tile: every tile holds
-// whole rows, so a tile's scan needs nothing from any other tile -- no
-// look-back, no second read.  A persistent CTA per SM streams tiles through
-// a ring of shared-memory stages:
+// Batched rows of at most 8192 elements.  When the row length divides the
+// 8192-element tile, every tile holds whole rows, so a tile's scan needs
+// nothing from any other tile -- no look-back, no second read; the CTAs take
+// tiles blockIdx.x, blockIdx.x + gridDim.x, ...  Otherwise (kRagged) a tile
+// may start inside a row, but every full tile holds a row start (any 8192
+// consecutive indices hold a multiple of a row length <= 8192), so the carry
+// into tile t + 1 is the fold of tile t since its last row start: each CTA
+// takes a contiguous range of tiles and carries that fold from one tile to
+// the next in registers; only its first tile reads back the part of its row
+// that lies before it.  A persistent CTA per SM streams tiles through a ring
+// of shared-memory stages:
 //
 //   producer warp   2-D TMA loads of the CTA's tiles (tile t = blockIdx.x +
 //                   i * gridDim.x) into the ring;
@@ -41,13 +48,14 @@ struct RowsCtrl {
     unsigned long long full[kRowsStages], empty[kRowsStages], written[kRowsStages];
     unsigned long long totals[kRowsStages];      // every compute warp wrote its total of the stage's tile
     uint2 wtot[kRowsStages][kRowsComputeWarps];  // (value bits, head flag) of each warp's part
+    uint32_t red[kRowsComputeWarps];             // ragged rows: the first tile's read-back, per warp
 };
 constexpr int kRowsSmem = kRowsStages * kRowsTileBytes + 1024 + (int)sizeof(RowsCtrl);
 static_assert(kRowsSmem <= 232448, "shared memory per CTA");
 
 }  // namespace
 
-template <class Op, bool kExcl>
+template <class Op, bool kExcl, bool kRagged>
 __global__ void __launch_bounds__(kRowsThreads, 1)
     rows_tma_kernel(const __grid_constant__ CUtensorMap tm_in, const __grid_constant__ CUtensorMap tm_out,
                     const ScanParams p, const long long n_full_tiles) {
@@ -66,8 +74,17 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long num_tiles = p.n / TILE + (p.n % TILE != 0);
-    // this CTA's tiles: blockIdx.x, blockIdx.x + gridDim.x, ...
-    const long long my_tiles = num_tiles > blockIdx.x ? (num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    // this CTA's tiles: blockIdx.x, blockIdx.x + gridDim.x, ...; ragged rows:
+    // a contiguous range [t_begin, t_begin + my_tiles)
+    long long my_tiles, t_begin = blockIdx.x;
+    if constexpr (kRagged) {
+        const long long q = num_tiles / gridDim.x, rem = num_tiles % gridDim.x;
+        my_tiles = q + ((long long)blockIdx.x < rem);
+        t_begin = (long long)blockIdx.x * q + min((long long)blockIdx.x, rem);
+    } else {
+        my_tiles = num_tiles > blockIdx.x ? (num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    }
+    auto tile_of = [&](long long i) -> long long { return kRagged ? t_begin + i : t_begin + i * gridDim.x; };
     const unsigned long long wait_limit = p.lb.timeout_ns + 500000000ull;
 
     if (threadIdx.x == 0) {
@@ -93,7 +110,7 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
                 raise_error(p.lb.error, DEV_LOOKBACK_TIMEOUT);
                 break;
             }
-            const long long t = blockIdx.x + i * gridDim.x;
+            const long long t = tile_of(i);
             issued = i;
             if (t < n_full_tiles) {
                 mbar_arrive_expect_tx(B(ctl->full[s]), kRowsTileBytes);
@@ -120,7 +137,7 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
                 raise_error(p.lb.error, DEV_LOOKBACK_TIMEOUT);
                 break;
             }
-            const long long t = blockIdx.x + i * gridDim.x;
+            const long long t = tile_of(i);
             if (t < n_full_tiles)
                 tma_store_2d_hint(&tm_out, 0, (int)(t * kRowsTileRows), stage0 + s * kRowsTileBytes, once);
             bulk_commit();  // one group per tile (empty for the ragged tile, stored by the compute warps)
@@ -136,17 +153,49 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
     uint32_t off[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) off[j] = ctid * 128 + ((j ^ (ctid & 7)) << 4);
-    // heads of the thread's items: tiles start at a row head (the row length
-    // divides the tile), so they depend on the thread's place only
+    // Heads of the thread's items from rr, the offset of its first item inside
+    // its row; r0, that of the tile's first element.  Rows dividing the tile:
+    // both the same in every tile.  Ragged: both advance by 8192 mod cols.
     const uint32_t cols = (uint32_t)p.seg_len;
-    uint32_t hm = 0;
-    {
-        const uint32_t r = (uint32_t)(ctid * IPT) % cols;
-        for (uint32_t k = r == 0 ? 0u : cols - r; k < (uint32_t)IPT; k += cols) hm |= 1u << k;
+    const uint32_t adv = (uint32_t)(TILE % cols);
+    uint32_t rr = (uint32_t)(((kRagged ? (unsigned long long)t_begin * TILE : 0ull) + (unsigned)(ctid * IPT)) % cols);
+    uint32_t r0 = kRagged ? (uint32_t)(((unsigned long long)t_begin * TILE) % cols) : 0u;
+    auto heads = [&]() {
+        uint32_t hm = 0;
+        for (uint32_t k = rr == 0 ? 0u : cols - rr; k < (uint32_t)IPT; k += cols) hm |= 1u << k;
+        return hm;
+    };
+    uint32_t hm = heads();
+    // ragged rows: the fold of the current row up to the tile's start
+    T carry = Op::identity();
+    if constexpr (kRagged) {
+        if (r0 != 0 && my_tiles > 0) {
+            // the CTA's first tile: read back its row's first r0 elements, in
+            // order (a contiguous part per thread, then warps, then the CTA)
+            const T* src = static_cast<const T*>(p.in) + (t_begin * TILE - (long long)r0);
+            const uint32_t per = (r0 + kRowsCompute - 1) / kRowsCompute;
+            T acc = Op::identity();
+            for (uint32_t j = ctid * per; j < min(r0, (uint32_t)(ctid + 1) * per); ++j) acc = Op::op(acc, src[j]);
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {  // ordered: lane 0 ends with lanes 0..31
+                const T y = shfl_down_v(acc, d);
+                if (lane + d < 32) acc = Op::op(acc, y);
+            }
+            if (lane == 0) ctl->red[warp] = to_bits32(acc);
+            named_bar_sync(1, kRowsCompute);
+            T c = Op::identity();
+#pragma unroll
+            for (int w = 0; w < kRowsComputeWarps; ++w) {
+                T x;
+                from_bits32(ctl->red[w], x);
+                c = Op::op(c, x);
+            }
+            carry = c;
+        }
     }
     for (long long i = 0; i < my_tiles; ++i) {
         const int s = (int)(i % kRowsStages);
-        const long long t = blockIdx.x + i * gridDim.x;
+        const long long t = tile_of(i);
         const bool full = t < n_full_tiles;
         if (!warp_bar_wait(B(ctl->full[s]), (uint32_t)((i / kRowsStages) & 1), wait_limit)) {
             if (lane == 0) raise_error(p.lb.error, DEV_LOOKBACK_TIMEOUT);
@@ -177,7 +226,8 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
             if (lane == 0) raise_error(p.lb.error, DEV_LOOKBACK_TIMEOUT);
             break;
         }
-        // carry into the thread: the earlier warps' totals, this warp's earlier lanes
+        // carry into the thread: the tile's carry (ragged rows), the earlier
+        // warps' totals, this warp's earlier lanes
         E wv = lane < kRowsComputeWarps ? ctl->wtot[s][lane] : PO::e_identity();
 #pragma unroll
         for (int d = 1; d < kRowsComputeWarps; d <<= 1) {
@@ -186,11 +236,25 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
         }
         E cin = shfl_up_v(x, 1);
         const E wpre = shfl_idx_v(wv, warp > 0 ? warp - 1 : 0);
-        if (lane == 0) cin = warp > 0 ? wpre : PO::e_identity();
-        else if (warp > 0) cin = PO::e_op(wpre, cin);
-        // the carry applies to the items before the thread's first head (the
-        // tile's first element is a head, so thread 0 takes none)
+        const E total = shfl_idx_v(wv, kRowsComputeWarps - 1);  // the whole tile's (fold since its last head, head)
+        // the tile's first element starts a row unless r0 != 0 (ragged rows only)
+        const bool tcarry = kRagged && r0 != 0;
+        const E tp = tcarry ? PO::make(carry, false) : PO::e_identity();
+        E before = warp > 0 ? wpre : tp;  // everything before this warp
+        if (tcarry && warp > 0) before = PO::e_op(tp, wpre);
+        if (lane == 0) cin = before;
+        else if (warp > 0 || tcarry) cin = PO::e_op(before, cin);
+        // the carry applies to the items before the thread's first head
         T run = PO::value(cin);
+        if constexpr (kRagged) {
+            // the next tile's carry: this tile's fold since its last head (a
+            // full tile always holds one); then the next tile's row offsets
+            carry = PO::value(total);
+            r0 += adv;
+            if (r0 >= cols) r0 -= cols;
+            rr += adv;
+            if (rr >= cols) rr -= cols;
+        }
         if constexpr (kExcl) {
 #pragma unroll
             for (int w = 0; w < IPT; ++w) {
@@ -215,13 +279,14 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(B(ctl->written[s]));
+        if constexpr (kRagged) hm = heads();
     }
 }
 
 // ----------------------------------------------------------------- host side
 namespace {
 
-template <class Op, bool kExcl>
+template <class Op, bool kExcl, bool kRagged>
 cudaError_t launch_rows_one(const ScanParams& p, unsigned grid, cudaStream_t s) {
     const long long tile = kRowsTileBytes / 4;
     const long long nfull = p.n / tile;
@@ -230,15 +295,17 @@ cudaError_t launch_rows_one(const ScanParams& p, unsigned grid, cudaStream_t s) 
     if (nfull < 1 || !make_map(&a, p.in, rows, kRowsTileRows) || !make_map(&b, p.out, rows, kRowsTileRows))
         return cudaErrorInvalidValue;
     static std::atomic<unsigned long long> done_mask{0};
-    const cudaError_t e = allow_smem(rows_tma_kernel<Op, kExcl>, kRowsSmem, done_mask);
+    const cudaError_t e = allow_smem(rows_tma_kernel<Op, kExcl, kRagged>, kRowsSmem, done_mask);
     if (e != cudaSuccess) return e;
-    rows_tma_kernel<Op, kExcl><<<grid, kRowsThreads, kRowsSmem, s>>>(a, b, p, nfull);
+    rows_tma_kernel<Op, kExcl, kRagged><<<grid, kRowsThreads, kRowsSmem, s>>>(a, b, p, nfull);
     return cudaGetLastError();
 }
 
 template <class Op>
 cudaError_t launch_rows_op(const ScanParams& p, bool exclusive, unsigned grid, cudaStream_t s) {
-    return exclusive ? launch_rows_one<Op, true>(p, grid, s) : launch_rows_one<Op, false>(p, grid, s);
+    if (kRowsTileBytes / 4 % p.seg_len == 0)
+        return exclusive ? launch_rows_one<Op, true, false>(p, grid, s) : launch_rows_one<Op, false, false>(p, grid, s);
+    return exclusive ? launch_rows_one<Op, true, true>(p, grid, s) : launch_rows_one<Op, false, true>(p, grid, s);
 }
 
 }  // namespace

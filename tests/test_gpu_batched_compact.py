@@ -49,15 +49,19 @@ def test_batched(shape, exclusive, kind):
 @pytest.mark.parametrize("kind,op", [("i32", "sum"), ("u32", "xor"), ("i32", "min"), ("u32", "prod"), ("f32", "max"),
                                      ("f32", "sum"), ("i32", "max")])
 @pytest.mark.parametrize("shape", [(8192, 1), (8192, 5), (4099, 3), (1000, 33), (300, 1000), (20, 8191), (9, 12289),
-                                   (3, 40000), (1024, 64), (64, 4096), (7, 8192), (3000, 32), (70000, 2), (513, 16)])
+                                   (3, 40000), (1024, 64), (64, 4096), (7, 8192), (3000, 32), (70000, 2), (513, 16),
+                                   (40000, 33), (3000, 1000), (700, 2047), (200, 8191), (300000, 7)])
 def test_batched_rows_persistent(kind, op, shape):
     """Rows of 4-byte elements on 16-byte aligned arrays of at least one tile:
-    lengths that divide 8192 on the persistent rows kernel (sum, int32 max,
-    float32 sum; every tile whole rows) or else the one-tile kernel, other
-    lengths on the persistent segmented kernel with heads at the multiples of
-    the row length: rows shorter than, equal to and longer than a thread's 32
-    items, a warp's part and the 8192-element tile, with ragged last tiles,
-    in place and not."""
+    on the persistent rows kernel (sum, int32 max, float32 sum) lengths that
+    divide 8192 (every tile whole rows) and, out of place, other lengths up to
+    8192 (a CTA carries the open row from tile to tile and reads back the part
+    before its first tile: the shapes of 1.3M-3M elements give CTAs several
+    tiles); other operators on the one-tile kernel when the length divides
+    4096; the rest on the persistent segmented kernel with heads at the
+    multiples of the row length.  Rows shorter than, equal to and longer than
+    a thread's 32 items, a warp's part and the 8192-element tile, with ragged
+    last tiles, in place and not."""
     import stream_compaction_gb300 as sc
     from gpu_helpers import CODE, OPC, dev_buffer, stream, to_host
     from test_gpu_ops import make_input
@@ -71,8 +75,9 @@ def test_batched_rows_persistent(kind, op, shape):
             st = sc.sc_scan_batched(CODE[kind], OPC[op], int(exclusive), xin.data_ptr(), xout.data_ptr(), rows, cols,
                                     stream())
             assert st == sc.SC_OK, sc.status_string(st)
-            rows_kernel = 8192 % cols == 0 and (kind, op) in (("i32", "sum"), ("u32", "sum"), ("f32", "sum"),
-                                                              ("i32", "max"))
+            rows_op = (kind, op) in (("i32", "sum"), ("u32", "sum"), ("f32", "sum"), ("i32", "max"))
+            # rows dividing 8192 always; other lengths up to 8192 when out != in
+            rows_kernel = rows_op and (8192 % cols == 0 or (cols <= 8192 and not inplace))
             want = (sc.SC_PATH_ROWS_PERSISTENT if rows_kernel else
                     sc.SC_PATH_SCAN_ONE_TILE if 4096 % cols == 0 else sc.SC_PATH_SEGSCAN_PERSISTENT)
             assert sc.sc_debug_last_path() == want, shape
