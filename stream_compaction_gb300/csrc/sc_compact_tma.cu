@@ -196,9 +196,8 @@ __global__ void __launch_bounds__(CompactShape<CW>::kThreads, 1)
     // ---------------------------------------------- producer A: fresh tiles
     if (warp == kProducerA) {
         if (lane != 0) return;
-        unsigned long long* ctr = p.lb.counter;
-        const unsigned long long base = p.lb.counter_base;
-        unsigned long long a0 = atomicAdd(ctr, 1ull);  // chunk ids one chunk ahead of use
+        ChunkIds ids{p.lb.counter, p.lb.counter_base, num_chunks, (long long)gridDim.x, p.lb.error};
+        ids.start();  // chunk ids one chunk ahead of use, except near the end
         const uint64_t keep_l2 = l2_policy_evict_last();
         int issued = -1;
         long long c = 0;
@@ -209,10 +208,7 @@ __global__ void __launch_bounds__(CompactShape<CW>::kThreads, 1)
                 break;
             }
             const int pos = k % kChunk;
-            if (pos == 0) {
-                c = (long long)(a0 - base);
-                a0 = atomicAdd(ctr, 1ull);
-            }
+            if (pos == 0) c = ids.take();
             const bool done = c >= num_chunks;
             const long long t = c * kChunk + pos;
             ctl->tile[k % kRing] = done ? kSentinel : (t < num_tiles ? (unsigned)t : kVoid);
@@ -228,7 +224,6 @@ __global__ void __launch_bounds__(CompactShape<CW>::kThreads, 1)
         }
         for (int k = vload(&ctl->consumed_a) + 1; k <= issued; ++k)
             bar_wait(B(ctl->a_full[k % kSA]), (k / kSA) & 1, wait_limit);
-        asm volatile("" ::"l"(a0));
         return;
     }
 

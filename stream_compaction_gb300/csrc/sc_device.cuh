@@ -427,7 +427,14 @@ struct StatusIO<float2> {
         const uint32_t lob = __float_as_uint(v.y);
         const int e = expo(v.x);
         int q = 0;
-        if (e != 0 && e != 255) q = __float2int_rn(ldexpf(__uint_as_float(lob & ~1u), 171 - e));
+        if (e != 0 && e != 255) {
+            // low * 2^(171 - e) by two exact power-of-two factors, each a normal
+            // float (|a|, |b| <= 85; |low| <= ulp(high) / 2, so the product is at
+            // most 2^20 and every step is exact), then rounded to an integer
+            const int k = 171 - e, b = k >> 1, a = k - b;
+            q = __float2int_rn(__fmul_rn(__fmul_rn(__uint_as_float(lob & ~1u), __uint_as_float((uint32_t)(a + 127) << 23)),
+                                         __uint_as_float((uint32_t)(b + 127) << 23)));
+        }
         q = max(-(1 << 21), min((1 << 21) - 1, q));
         const uint32_t lo = ((uint32_t)q << 10) | ((lb.epoch & 0x7fu) << 3) | ((flag & 3u) << 1) | (lob & 1u);
         st_relaxed_u64(slot(lb, tile), ((unsigned long long)__float_as_uint(v.x) << 32) | lo);

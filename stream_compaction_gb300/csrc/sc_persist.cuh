@@ -94,6 +94,45 @@ inline bool make_map(CUtensorMap* m, const void* base, unsigned long long rows, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Chunk ids of a persistent kernel, taken by its producer thread from the
+// launch's monotone counter.  Far from the end each id is requested one chunk
+// ahead of use, which hides the atomic's latency; within the last `margin`
+// chunks (a round of the grid) an id is requested only when it is needed, so
+// the last chunks go to CTAs that are free instead of to CTAs that reserved
+// them while still busy (measured on GB300 the same as requesting every id
+// ahead: the CTAs' end times spread over about two chunks either way).  A CTA
+// stops at its first id >= num_chunks and requests
+// none after it, so a launch advances the counter by exactly num_chunks +
+// grid, which the host adds to the base for the next launch (the counter must
+// start every launch at the base: an id below it would name a negative chunk,
+// which take() turns into an error and the end of the CTA's work).
+struct ChunkIds {
+    unsigned long long* ctr;
+    unsigned long long base;
+    long long num_chunks, margin;
+    unsigned int* err;
+    unsigned long long next = 0;
+    bool have = false;
+    __device__ __forceinline__ void start() {
+        next = atomicAdd(ctr, 1ull);
+        have = true;
+    }
+    __device__ __forceinline__ long long take() {
+        if (!have) next = atomicAdd(ctr, 1ull);
+        long long c = (long long)(next - base);
+        have = false;
+        if (c < 0) {  // the counter is behind the host's base: never use the id
+            atomicCAS(err, 0u, (unsigned)DEV_INTERNAL);
+            return num_chunks;
+        }
+        if (c + margin < num_chunks) {
+            next = atomicAdd(ctr, 1ull);
+            have = true;
+        }
+        return c;
+    }
+};
+
 // Opt a kernel in to more than 48 KiB of dynamic shared memory, once per device.
 template <class K>
 inline cudaError_t allow_smem(K kernel, int bytes, std::atomic<unsigned long long>& done_mask) {

@@ -6,7 +6,7 @@
 namespace scg {
 
 int tma_num_cfgs() { return kNumCfgs; }
-int tma_ids_per_cta() { return 2; }  // one requested ahead + the one that ends the CTA's loop
+int tma_ids_per_cta() { return 1; }  // the id that ends the CTA's loop (ChunkIds)
 
 bool tma_shape(int cfg, TmaShape* sh) {
     switch (cfg) {

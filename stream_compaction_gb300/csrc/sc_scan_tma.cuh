@@ -70,9 +70,9 @@ template <int TileBytes, int SA, int SB, int CW, int Lag, int Chunk, bool P1Firs
           int MinBlocks = 1>
 struct TmaCfg {
     static constexpr bool kP1First = P1First;
-    // chunk ids each CTA takes beyond the chunks it works on: the one that
-    // ends its loop and the one requested ahead of it
-    static constexpr int kIdsPerCta = 2;
+    // counter ticks per CTA beyond the chunks: the id that ends its loop (see
+    // ChunkIds); the host advances the counter's base by exactly this
+    static constexpr int kIdsPerCta = 1;
     static constexpr int kMinBlocks = MinBlocks;
     static constexpr int kTileBytes = TileBytes;  // rows of 128 bytes
     static constexpr int kSA = SA;                // pass-1 stages: fresh tiles from HBM
@@ -263,12 +263,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
     // ---------------------------------------------- producer A: fresh tiles
     if (warp == kProducerA) {
         if (lane != 0) return;
-        unsigned long long* ctr = p.lb.counter;
-        const unsigned long long base = p.lb.counter_base;
-        // chunk ids requested one chunk ahead of use: early enough to hide the
-        // atomic's latency, late enough that chunks are published in about the
-        // order in which they were handed out
-        unsigned long long a0 = atomicAdd(ctr, 1ull);
+        // chunk ids requested one chunk ahead of use (except near the end):
+        // early enough to hide the atomic's latency, late enough that chunks
+        // are published in about the order in which they were handed out
+        ChunkIds ids{p.lb.counter, p.lb.counter_base, num_chunks, (long long)gridDim.x, p.lb.error};
+        ids.start();
         // fresh tiles stay in L2 until their pass-2 re-load
         const uint64_t keep = l2_policy_evict_last();
         int issued = -1;
@@ -285,10 +284,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
                 if (kStats) waited += global_ns() - w0;
             }
             const int pos = k % kChunk;
-            if (pos == 0) {
-                c = (long long)(a0 - base);
-                a0 = atomicAdd(ctr, 1ull);
-            }
+            if (pos == 0) c = ids.take();
             const bool done = c >= num_chunks;
             const long long t = c * kChunk + pos;
             ctl->tile[k % kRing] = done ? kSentinel : (t < num_tiles ? (unsigned)t : kVoid);
@@ -307,7 +303,6 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
         // its stage's newest phase.
         for (int k = vload(&ctl->consumed_a) + 1; k <= issued; ++k)
             bar_wait(B(ctl->a_full[k % kSA]), (k / kSA) & 1, wait_limit);
-        asm volatile("" ::"l"(a0));  // the id requested ahead is part of the counter's advance
         if (kStats) atomicAdd(st + 7, waited);
         return;
     }

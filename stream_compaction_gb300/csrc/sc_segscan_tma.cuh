@@ -198,9 +198,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     // ---------------------------------------------- producer A: fresh tiles
     if (warp == kProducerA) {
         if (lane != 0) return;
-        unsigned long long* ctr = p.lb.counter;
-        const unsigned long long base = p.lb.counter_base;
-        unsigned long long a0 = atomicAdd(ctr, 1ull);  // chunk ids requested one chunk ahead
+        ChunkIds ids{p.lb.counter, p.lb.counter_base, num_chunks, (long long)gridDim.x, p.lb.error};
+        ids.start();  // chunk ids one chunk ahead of use, except near the end
         const uint64_t keep = l2_policy_evict_last();   // values stay in L2 for the re-load
         const uint64_t drop = l2_policy_evict_first();  // flags are read once
         int issued = -1;
@@ -212,10 +211,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 break;
             }
             const int pos = k % kChunk;
-            if (pos == 0) {
-                c = (long long)(a0 - base);
-                a0 = atomicAdd(ctr, 1ull);
-            }
+            if (pos == 0) c = ids.take();
             const bool done = c >= num_chunks;
             const long long t = c * kChunk + pos;
             ctl->tile[k % kRing] = done ? kSentinel : (t < num_tiles ? (unsigned)t : kVoid);
@@ -234,7 +230,6 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
         for (int k = vload(&ctl->consumed_a) + 1; k <= issued; ++k)
             bar_wait(B(ctl->a_full[k % kSA]), (k / kSA) & 1, wait_limit);
-        asm volatile("" ::"l"(a0));
         return;
     }
 
