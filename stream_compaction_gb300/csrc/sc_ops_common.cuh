@@ -10,7 +10,7 @@ template <class Op>
 cudaError_t launch_op(const ScanParams& p, bool exclusive, bool segmented, unsigned tma_grid, cudaStream_t s) {
     if (tma_grid) {
         if (segmented) return cudaErrorInvalidValue;
-        return launch_cfg<Op, Cfg0>(p, exclusive, tma_grid, s, false);
+        return launch_cfg<Op, typename DefaultCfg<Op>::type>(p, exclusive, tma_grid, s, false);
     }
     if constexpr (sizeof(typename Op::T) == 8)
         return launch_shape<Op, SC_SHAPE_ARGS(kShapeExtra8)>(p, exclusive, segmented, s);
