@@ -103,6 +103,27 @@ def test_workload_int32_rows_65536x4096():
     assert np.array_equal(y, oracle.scan_batched(x, "sum", True))
 
 
+@pytest.mark.parametrize("cols", [33, 1000, 2047])
+def test_workload_int32_ragged_rows_full_size(cols):
+    """The benchmark's ragged-row shapes: the 65536 x 4096 input's first
+    rows * cols elements viewed as rows of 33, 1000 and 2047 (tiles start
+    inside rows, so every CTA carries the open row from tile to tile and reads
+    back the part of its first tile's row before it), on the rows kernel."""
+    import torch
+    import stream_compaction_gb300 as sc
+    spec = synth.WORKLOADS["int32_rows_65536x4096"]
+    xt = synth.make_torch(spec, device="cuda")
+    rows = xt.numel() // cols
+    xt = xt[:rows * cols].contiguous()
+    yt = torch.empty_like(xt)
+    st = sc.sc_scan_batched(sc.SC_I32, sc.SC_SUM, 1, xt.data_ptr(), yt.data_ptr(), rows, cols, stream())
+    assert st == sc.SC_OK, sc.status_string(st)
+    assert sc.sc_debug_last_path() == sc.SC_PATH_ROWS_PERSISTENT
+    assert sc.sc_get_device_error(stream()) == sc.SC_OK
+    x = xt.cpu().numpy().reshape(rows, cols)
+    assert np.array_equal(yt.cpu().numpy().reshape(rows, cols), oracle.scan_batched(x, "sum", True))
+
+
 # ------------------------------------------------------------- compaction
 CSIZES = [1, 2, 33, 4095, 4096, 4097, 3 * 4096 + 17, 100003, (1 << 20) + 17]
 
