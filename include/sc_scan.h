@@ -317,8 +317,9 @@ uint64_t sc_launch_count(void);
 
 /* Select the kernel of the uint32/int32 sum.  0 (default): the persistent
  * TMA-pipelined kernel wherever it applies (16-byte aligned arrays of more
- * than 2^22 elements; scans segmented by head flags and batched rows whose
- * length does not divide 4096 on its segmented form), else the
+ * than 2^22 elements -- 2^20 for the other operators' 8-byte elements; scans
+ * segmented by head flags and batched rows on its segmented form or the rows
+ * kernel), else the
  * one-tile-per-CTA kernel (for n <= 2^22 its shape of 8192-element tiles of
  * 512 threads, variant 4); v >= 1: one of the precompiled shapes (see
  * sc_scan_variant_info), kept for on-GPU comparison (always on the kernel the

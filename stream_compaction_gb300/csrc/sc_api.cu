@@ -43,8 +43,12 @@ constexpr int kTmaStatsVariant = scg::kNumSumU32Variants + 1;
 // (7.0 us back to back), against 12.4 (8.2) for 16384-element tiles and 11.5
 // (7.4) for 4096-element ones; up to 2^22 + 17 elements that shape also beats
 // the persistent kernel (16.3 against 18.6 us), at 2^23 the persistent kernel
-// wins (24.8 against 25.7 us).
-constexpr int64_t kSmallScanMax = int64_t(1) << 22;
+// wins (24.8 against 25.7 us).  8-byte elements (2048-element tiles on the
+// one-tile kernel) cross over near 2^20 (8 MiB): int64 sums with the L2
+// flushed took 14.3 / 16.4 / 24.6 / 37.9 us at 2^19 + 3 / 2^20 + 1 / 2^21 + 8
+// / 2^22 on the one-tile kernel and 14.7 / 16.4 / 20.5 / 25.4 us persistent.
+constexpr int64_t kSmallScanMax = int64_t(1) << 22;   // elements of 4 bytes
+constexpr int64_t kSmallScanMax8 = int64_t(1) << 20;  // elements of 8 bytes
 constexpr int kSmallShape = 3;  // 8192-element tiles, 512 threads x 16 items
 // Scans segmented by head flags (int32/uint32 sums): 4096-element tiles, 128-tile
 // look-back windows, 8 CTAs per SM; measured on GB300 with 2^27 elements and a
@@ -303,7 +307,8 @@ cudaError_t dispatch_scan_tma(int oid, const ScanParams& p, bool excl, unsigned 
 
 // One single-pass scan launch (plain or segmented), with optional carries.
 // Public variant 0 is the persistent TMA kernel where it applies (16-byte
-// aligned, unsegmented, more than kSmallScanMax elements); every other case,
+// aligned, unsegmented, more than kSmallScanMax elements of 4 bytes or
+// kSmallScanMax8 of 8 bytes); every other case,
 // and public variants v >= 1 of the uint32 sum, use the one-tile-per-CTA
 // kernel (shape v - 1; by default shape 0, kSmallShape for short uint32 sums
 // and kHeadsShape for uint32 sums segmented by head flags).  Segmented scans
@@ -319,7 +324,7 @@ sc_status run_scan(int oid, const void* in, void* out, int64_t n, int64_t seg_le
     if (cfg >= 0) scg::tma_shape(cfg, &sh);
     const int64_t tma_tile = cfg >= 0 ? sh.tile_bytes / eb : 0;
     const bool tma_stats = api_variant == kTmaStatsVariant;
-    const bool small = api_variant == 0 && n <= kSmallScanMax;
+    const bool small = api_variant == 0 && n <= (eb == 4 ? kSmallScanMax : kSmallScanMax8);
     const bool use_tma = cfg >= 0 && !small && !segmented && vec_ok && n >= tma_tile &&
                          n / tma_tile * (sh.tile_bytes / 128) < (int64_t)INT_MAX && num_sms() > 0;
     int legacy_variant = (small && oid == 0 && !segmented) ? kSmallShape

@@ -10,8 +10,8 @@
 // that lies before it.  A persistent CTA per SM streams tiles through a ring
 // of shared-memory stages:
 //
-//   producer warp   2-D TMA loads of the CTA's tiles (tile t = blockIdx.x +
-//                   i * gridDim.x) into the ring;
+//   producer warp   2-D TMA loads of the CTA's tiles (blockIdx.x +
+//                   i * gridDim.x, or its contiguous range) into the ring;
 //   compute warps   each thread scans its 32 items as (value, head) pairs
 //                   (heads at the multiples of the row length), a warp scan
 //                   of the pairs, then the CTA's warp totals through shared

@@ -242,6 +242,28 @@ def test_persistent_scan_in_place_at_boundaries(kind, op, n):
                 assert np.array_equal(y, ref), what
 
 
+@pytest.mark.parametrize("kind,op", [("affine", "affine"), ("i64", "sum"), ("f64", "sum"), ("maxcount", "maxcount")])
+@pytest.mark.parametrize("n", [1 << 20, (1 << 20) + 1, (1 << 20) + 2 * 4096 + 3, (1 << 21) + 77])
+def test_eight_byte_short_scan_limit(kind, op, n):
+    """8-byte elements take the one-tile-per-CTA kernel up to 2^20 elements and
+    the persistent kernel above (their crossover measured on GB300); both
+    sides of the limit, in place and not, against the oracle."""
+    import stream_compaction_gb300 as sc
+    from gpu_helpers import check_f64
+    x = _p_input(kind, op, n, seed=n % 991 + len(kind))
+    want = sc.SC_PATH_SCAN_ONE_TILE if n <= (1 << 20) else sc.SC_PATH_SCAN_PERSISTENT
+    for exclusive in (False, True):
+        ref = oracle.scan(x, op, exclusive)
+        for inplace in (False, True):
+            y = gpu_scan(x, op, exclusive, inplace=inplace)
+            assert sc.sc_debug_last_path() == want, (kind, n)
+            what = "%s n=%d excl=%d inplace=%d" % (kind, n, exclusive, inplace)
+            if kind == "f64":
+                check_f64(y, ref, oracle.abs_prefix(x), what)
+            else:
+                assert np.array_equal(y, ref), what
+
+
 @pytest.mark.parametrize("kind,op,n", [("u32", "sum", (1 << 24) + 4097), ("affine", "affine", (1 << 23) + 5),
                                        ("f32", "sum", (1 << 24) + 3)])
 def test_host_scan_in_place_across_chunks(kind, op, n):
