@@ -58,10 +58,13 @@ def test_histogram_and_offsets(kind, nbins, n):
     assert np.array_equal(offs, oracle.bin_offsets(bins, nbins)[0])
 
 
-def test_unaligned_bins():
-    bins = _bins(100003, 300, "uniform", 1)
+@pytest.mark.parametrize("nbins", [200, 300, 5000])
+def test_unaligned_bins(nbins):
+    """Bins not 16-byte aligned (element loads) on the lane-counter (<= 256
+    bins), per-warp (<= 1024) and per-CTA histograms."""
+    bins = _bins(100003, nbins, "outside", 1)
     for off in (1, 2, 3):
-        assert np.array_equal(gpu_bins(bins, 300, True, off=off), oracle.bin_offsets(bins, 300)[0])
+        assert np.array_equal(gpu_bins(bins, nbins, True, off=off), oracle.bin_offsets(bins, nbins)[0])
 
 
 def test_csr_rows_workload():
