@@ -58,10 +58,10 @@ def test_histogram_and_offsets(kind, nbins, n):
     assert np.array_equal(offs, oracle.bin_offsets(bins, nbins)[0])
 
 
-@pytest.mark.parametrize("nbins", [200, 300, 5000])
+@pytest.mark.parametrize("nbins", [200, 300, 5000, 40000])
 def test_unaligned_bins(nbins):
-    """Bins not 16-byte aligned (element loads) on the lane-counter (<= 256
-    bins), per-warp (<= 1024) and per-CTA histograms."""
+    """Bins not 16-byte aligned (element loads) on the per-warp (<= 1024
+    bins), per-CTA (<= 32768) and global-atomic histograms."""
     bins = _bins(100003, nbins, "outside", 1)
     for off in (1, 2, 3):
         assert np.array_equal(gpu_bins(bins, nbins, True, off=off), oracle.bin_offsets(bins, nbins)[0])
