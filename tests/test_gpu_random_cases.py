@@ -87,3 +87,45 @@ def test_random_compaction(case):
     ref, rc = oracle.compact(x, pred, t)
     assert c == rc
     assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+ROW_OPS = [("i32", "sum"), ("u32", "sum"), ("i32", "max"), ("f32", "sum"), ("u32", "xor"), ("f32", "max"),
+           ("i64", "sum"), ("affine", "affine")]
+
+
+@pytest.mark.parametrize("case", range(24))
+def test_random_batched_rows(case):
+    """Batched rows with random row lengths (dividing 8192 or not, shorter and
+    longer than a tile), row counts (one tile up to several tiles per CTA),
+    element offsets and in-place calls: the rows kernel, its ragged form, the
+    segmented kernels and the one-tile kernel, each against the oracle."""
+    import stream_compaction_gb300 as sc
+    from gpu_helpers import CODE, OPC, dev_buffer, stream, to_device, to_host
+    rng = np.random.default_rng(4000 + case)
+    kind, op = ROW_OPS[case % len(ROW_OPS)]
+    cols = int(rng.choice([1, 3, 16, 31, 33, 64, 100, 1000, 2047, 2048, 4095, 8191, 8192, 12289]))
+    n_target = int(rng.choice([8192, 65536, 1 << 20, 3 << 20]))
+    rows = max(1, n_target // cols + int(rng.integers(0, 3)))
+    if kind == "affine":
+        x = np.random.default_rng(case + 90).integers(0, 1 << 32, (rows, cols, 2), dtype=np.uint64).astype(np.uint32)
+    else:
+        x = make_input(kind, op, rows * cols, seed=case + 90).reshape(rows, cols)
+    ex = bool(rng.integers(0, 2))
+    off = int(rng.integers(0, 2)) * (2 if kind == "affine" else 1)
+    inplace = bool(rng.integers(0, 2))
+    _, xin = to_device(x, off)
+    xout = xin if inplace else dev_buffer(xin.numel(), xin.dtype, off)[1]
+    st = sc.sc_scan_batched(CODE[kind], OPC[op], int(ex), xin.data_ptr(), xout.data_ptr(), rows, cols, stream())
+    assert st == sc.SC_OK, sc.status_string(st)
+    assert sc.sc_get_device_error(stream()) == sc.SC_OK
+    y = to_host(xout, x)
+    ref = oracle.scan_batched(x, op, ex)
+    what = "%s %s rows=%d cols=%d excl=%d off=%d inplace=%d" % (kind, op, rows, cols, ex, off, inplace)
+    if kind == "f32" and op == "sum":
+        s_abs = np.stack([oracle.abs_prefix(r) for r in x])
+        check_f32(y.reshape(-1), ref.reshape(-1), s_abs.reshape(-1), what)
+    elif kind != "f32":
+        assert np.array_equal(y, ref), what
+    else:
+        assert same_float(y, ref), what
+
