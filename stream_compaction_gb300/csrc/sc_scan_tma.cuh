@@ -147,9 +147,10 @@ struct TmaCfg {
 // comparison.  The float32 sum's look-back (float-float statuses) takes
 // longer, so its default waits one tile more before pass 2 (CfgSumF32:
 // measured at 2^26 / 2^27 / 2^28 elements 0.76 / 0.83 / 0.87 of the copy peak
-// at lag 5, 0.79 / 0.85 / 0.89 at lag 6, the same at lag 7, 0.77 / 0.81 /
-// 0.83 at lag 8; the uint32 sum at lag 6: 0.85 / 0.90 / 0.93 against 0.84 /
-// 0.91 / 0.96 at lag 5).
+// at lag 5, 0.79 / 0.85 / 0.89 at lag 6, 0.79 / 0.86 / 0.89 at lag 7 (on the
+// final code: lag 7 +1 % at 2^26, -1.2 % at 2^28 against lag 6; lag 6 without
+// pass 1 first -1 %), 0.77 / 0.81 / 0.83 at lag 8; the uint32 sum at lag 6:
+// 0.85 / 0.90 / 0.93 against 0.84 / 0.91 / 0.96 at lag 5).
 using Cfg0 = TmaCfg<32768, 3, 3, 8, 5, 2, true>;
 using Cfg1 = TmaCfg<16384, 6, 6, 16, 12, 4>;
 using Cfg2 = TmaCfg<32768, 3, 3, 16, 6, 2>;
