@@ -66,6 +66,9 @@ def parse():
                     help="which kernel --profile-case runs")
     ap.add_argument("--compact-variant", type=int, default=0,
                     help="compaction kernel for --profile-op compact (sc_set_compact_variant)")
+    ap.add_argument("--phase-timers", action="store_true",
+                    help="with --profile-case and --variant 16 (the instrumented persistent scan): print the "
+                         "per-role phase timers of those launches, per tile")
     return ap.parse_args()
 
 
@@ -855,6 +858,9 @@ def profile_case(args):
             run = lambda: sc.sc_scan_hierarchical(sc.SC_U32, sc.SC_SUM, 1, x.data_ptr(), y.data_ptr(), n, sp)
         else:
             run = lambda: sc.sc_scan_exclusive(sc.SC_U32, sc.SC_SUM, x.data_ptr(), y.data_ptr(), n, sp)
+    if args.phase_timers:
+        run()  # warm-up launch, then clear the counters
+        sc.sc_debug_lookback_stats(sp)
     for _ in range(max(1, args.steps)):
         st = run()
         if st != sc.SC_OK:
@@ -862,6 +868,21 @@ def profile_case(args):
     torch.cuda.synchronize()
     if sc.sc_get_device_error(sp) != sc.SC_OK:
         raise SystemExit("device error")
+    if args.phase_timers:
+        # counters of the instrumented persistent scan: [0] tiles, [1] ns the
+        # compute warps waited for fresh tiles, [2] ns they waited for chunk
+        # prefixes or re-loaded tiles, [3] ns in look-backs, [4] look-back
+        # windows, [5] polls that found a predecessor unpublished, [6] ns the
+        # look-back warps waited for chunk aggregates, [7] ns producer A waited
+        # for a free fresh stage (compute-warp figures are warp 0's)
+        st, c = sc.sc_debug_lookback_stats(sp)
+        tiles = max(1, c[0])
+        chunks = max(1, tiles // 2)
+        print(json.dumps({"tiles": c[0], "compute_fresh_wait_ns_per_tile": c[1] / tiles,
+                          "compute_pass2_wait_ns_per_tile": c[2] / tiles,
+                          "lookback_ns_per_chunk": c[3] / chunks, "windows_per_chunk": c[4] / chunks,
+                          "polls_per_chunk": c[5] / chunks, "lookback_agg_wait_ns_per_chunk": c[6] / chunks,
+                          "producer_a_wait_ns_per_tile": c[7] / tiles}))
     print("profile case ok: %s n=%d x%d" % (args.profile_op, n, max(1, args.steps)))
 
 
